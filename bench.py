@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark: fp8-latent absorbed MLA decode on GB300.
+
+Default workload "long": B=2 sequences x T=262144 cached tokens, H=128 heads,
+kv_lora 512 + qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token,
+306 MB of KV per step: larger than L2, and L2 is flushed between steps anyway).
+One step = one decode query per sequence over its whole cache (the "append"
+workload also quantizes 65536 fresh rows into the cache inside the step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--variant auto|simt|tcgen05] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` = KV GB/s over all ranks (KV bytes the
+step attends over / device time of the step); token*heads/s rides along.
+Under torchrun (N > 1) every rank runs an independent replica (the decode of
+independent sequences needs no exchange): value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp8-latent MLA decode: KV GB/s & token·heads/s, % of roofline (1 GB300)"
+ROW_BYTES = 576 + 8                 # e4m3 row + two f32 scales
+FLOP_PER_TOKEN_HEAD = 2 * (576 + 512)  # score dot over 576 + context over 512
+FP32_LANES_PER_SM = 128
+NUM_SMS = 152
+SM_MAX_MHZ_NOMINAL = 2070.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL)), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": SM_MAX_MHZ_NOMINAL, "src": "fallback"}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "decode_simt": ["fp8_mla_latent_gb300/csrc/decode_simt.cu",
+                    "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+}
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(f"{kernel}/{workload}")
+    except Exception:
+        return None
+    if not d or d.get("source_sha") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return float(d["bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kv8_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swpc=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 0.3 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in loaded:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swpc", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
+                "sm_max_mhz": float(max(r["smax"] for r in rows)),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import fp8_mla_latent_gb300 as pkg
+    from fp8_mla_latent_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    variant = {"auto": pkg.KV8_DECODE_AUTO, "simt": pkg.KV8_DECODE_SIMT,
+               "tcgen05": pkg.KV8_DECODE_TCGEN05}[args.variant]
+
+    w = workloads.make(args.workload)
+    codes = torch.zeros((w.n_slots, 576), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((w.n_slots, 2), dtype=torch.float32, device=dev)
+    pkg.kv8_quantize_rows(torch.from_numpy(w.cache_rows).to(dev), codes, scales,
+                          dst_slot=torch.from_numpy(w.cache_slots).to(dev))
+    fresh = fresh_slots = None
+    if w.fresh_rows is not None:
+        fresh = torch.from_numpy(w.fresh_rows).to(dev)
+        fresh_slots = torch.from_numpy(w.fresh_slots).to(dev)
+    ql = torch.from_numpy(w.q_lat).to(dev)
+    qr = torch.from_numpy(w.q_rope).to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty((w.B, w.H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    ws_bytes = pkg.mla_absorb_decode_fp8_batch_workspace_size(w.B, w.H, w.max_blocks,
+                                                              variant=variant)
+    ws = pkg.alloc_workspace(ws_bytes, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x L2
+    stream = torch.cuda.current_stream()
+    plan_variant = variant
+    if variant == pkg.KV8_DECODE_AUTO:
+        plan_variant = pkg.KV8_DECODE_TCGEN05 if (w.H >= 16 and tc_built(pkg, dev)) \
+            else pkg.KV8_DECODE_SIMT
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        if fresh is not None:
+            pkg.kv8_quantize_rows(fresh, codes, scales, dst_slot=fresh_slots)
+        if evs is not None:
+            evs[1].record(stream)
+        pkg.mla_absorb_decode_fp8_batch_partials(ql, qr, codes, scales, bt, sl, w.sm_scale, ws,
+                                                 variant=variant)
+        if evs is not None:
+            evs[2].record(stream)
+        pkg.mla_absorb_decode_fp8_batch_combine(sl, w.H, w.max_blocks, out, lse, ws,
+                                                variant=variant)
+        if evs is not None:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkg.kv8_workspace_error(ws) == 0
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    # keep the GPU busy for the sampler's first samples, then time exactly K steps
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()  # evict L2 between timed steps (outside the step's events)
+        step(evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    dec_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    q_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    comb_ms = np.array([e[2].elapsed_time(e[3]) for e in evs])
+    ms_step = float(step_ms.mean())
+    ms_dec = float(dec_ms.mean())
+
+    # ---- e2e through the public fused call, host buffers in the timed region
+    q_host = torch.cat([ql, qr], dim=2).cpu().pin_memory()
+    ql_h = q_host[..., :512].contiguous().pin_memory()
+    qr_h = q_host[..., 512:].contiguous().pin_memory()
+    fr_h = w.fresh_rows
+    fresh_h = torch.from_numpy(fr_h).pin_memory() if fr_h is not None else None
+    out_h = torch.empty((w.B, w.H, 512), dtype=torch.float32).pin_memory()
+    ql_d, qr_d = torch.empty_like(ql), torch.empty_like(qr)
+    fresh_d = torch.empty_like(fresh) if fresh is not None else None
+
+    def e2e_step():
+        ql_d.copy_(ql_h, non_blocking=True)
+        qr_d.copy_(qr_h, non_blocking=True)
+        if fresh_d is not None:
+            fresh_d.copy_(fresh_h, non_blocking=True)
+            pkg.kv8_quantize_rows(fresh_d, codes, scales, dst_slot=fresh_slots)
+        pkg.mla_absorb_decode_fp8_batch(ql_d, qr_d, codes, scales, bt, sl, w.sm_scale, out=out,
+                                        workspace=ws, variant=variant)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_evs[k][0].record(stream)
+        e2e_step()
+        e2e_evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_evs]))
+    h2d = ql_h.numel() * 4 + qr_h.numel() * 4 + (fresh_h.numel() * 4 if fresh_h is not None else 0)
+    d2h = out_h.numel() * 4
+
+    # ---- max over ranks
+    t = torch.tensor([ms_step, ms_dec, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step, ms_dec, e2e_ms = (float(x) for x in t.tolist())
+    if rank != 0:
+        return None
+
+    kv_bytes = w.kv_bytes() * world
+    tok_heads = w.total_tokens * w.H * world
+    value = kv_bytes / (ms_step * 1e-3) / 1e9
+    peaks = load_peaks()
+    flops = FLOP_PER_TOKEN_HEAD * w.total_tokens * w.H
+    if plan_variant == pkg.KV8_DECODE_TCGEN05:
+        kernel = "decode_tc"
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = w.kv_bytes() / (peaks["hbm_gbs"] * 1e9)
+        if t_tensor >= t_hbm:
+            roof = {"bound": "tensor", "achieved": flops / (ms_dec * 1e-3) / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "peak_note": f"{peaks['src']} bf16 dense burst; fp16 operands run at the bf16 rate"}
+        else:
+            roof = {"bound": "hbm", "achieved": w.kv_bytes() / (ms_dec * 1e-3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_note": f"{peaks['src']} copy"}
+    else:
+        kernel = "decode_simt"
+        alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": flops / (ms_dec * 1e-3) / 1e12, "peak": alu_peak,
+                "unit": "TFLOP/s",
+                "peak_note": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(kernel, args.workload)
+    roof["kernel"] = kernel
+    roof["ms_per_launch"] = ms_dec
+    roof["algorithmic"] = {"bytes": w.kv_bytes(), "flops": flops,
+                           "per_unit": "584 B and 2176*H FLOP per (token, sequence)"}
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f32 accum",
+        "data": "synthetic (seeded; shapes and value mix of the workload, see DESIGN.md)",
+        "token_heads_per_s": tok_heads / (ms_step * 1e-3),
+        "config": {"workload": args.workload, "B": w.B, "H": w.H,
+                   "T_total": w.total_tokens, "kv_lora": 512, "qk_rope": 64,
+                   "variant": {1: "simt", 2: "tcgen05"}[plan_variant],
+                   "l2": "flushed between steps (256 MB write) and KV > L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "phases_ms": {"quantize": float(q_ms.mean()), "decode": ms_dec,
+                      "combine": float(comb_ms.mean())},
+        "roofline": roof,
+        "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 + (1 if fresh is not None else 0)),
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    return res, w
+
+
+def tc_built(pkg, dev):
+    import torch
+    try:
+        q = torch.zeros((16, 512), device=dev)
+        r = torch.zeros((16, 64), device=dev)
+        c = torch.zeros((1, 576), dtype=torch.uint8, device=dev)
+        s = torch.zeros((1, 2), device=dev)
+        pkg.mla_absorb_decode_fp8(q, r, c, s, 1, 0.1, variant=pkg.KV8_DECODE_TCGEN05)
+        torch.cuda.synchronize()
+        return True
+    except pkg.Kv8Error:
+        return False
+
+
+# ----------------------------------------------------------------- oracle (CPU) arm
+def oracle_sample(w, budget_s, codes=None, scales=None):
+    """Time the f32 oracle (OpenMP, all cores) on a bounded sample of the workload:
+    sequence 0, the first n heads, n sized to about budget_s of wall time."""
+    import oracle
+    if codes is None:
+        codes, scales = oracle.quantize_rows(w.cache_rows, dst_slot=w.cache_slots,
+                                             n_slots=w.n_slots)
+        if w.fresh_rows is not None:
+            oracle.quantize_rows(w.fresh_rows, dst_slot=w.fresh_slots, codes=codes, scales=scales)
+    cores = oracle.max_threads()
+    b = 0
+    T = int(w.seq_lens[b])
+
+    def run(nh):
+        t0 = time.perf_counter()
+        oracle.attention_batch_f32(w.q_lat[b:b + 1, :nh], w.q_rope[b:b + 1, :nh], codes, scales,
+                                   w.block_table[b:b + 1], w.seq_lens[b:b + 1], w.sm_scale,
+                                   n_threads=cores)
+        return time.perf_counter() - t0
+
+    nh = min(w.H, cores)
+    t1 = run(nh)
+    per_head = t1 / nh
+    n2 = int(max(1, min(w.H, budget_s / max(per_head, 1e-6))))
+    if n2 > nh:
+        nh, t1 = n2, run(n2)
+    # full-job time: every (sequence, head) at the sample's per-head rate
+    per_tok_head = t1 / (nh * T)
+    t_full = per_tok_head * w.total_tokens * w.H
+    value = w.kv_bytes() / t_full / 1e9
+    sample = f"sequence 0 ({T} tokens) x {nh} of {w.H} heads, f32 oracle, {t1:.2f} s wall"
+    return {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "seconds": t1}, (codes, scales)
+
+
+def run_reference(args, world):
+    from fp8_mla_latent_gb300 import workloads
+    import oracle
+    w = workloads.make(args.workload)
+    cache = None
+    for _ in range(args.warmup):
+        _, cache = oracle_sample(w, 0.2, *(cache or (None, None)))
+    vals, secs = [], []
+    cb = None
+    for _ in range(args.steps):
+        cb, cache = oracle_sample(w, 1.0, *cache)
+        vals.append(cb["value"])
+        secs.append(cb["seconds"])
+    value = float(np.mean(vals))
+    ms = w.kv_bytes() / (value * 1e9) * 1e3
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; same workload as our arm)",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "T_total": w.total_tokens},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+                         "sample": cb["sample"] + f"; {args.steps} steps"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the CPU oracle (plain C, OpenMP over heads) stands in for the reference; "
+                "the source pages ship no runnable implementation",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long")
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    r = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        res, w = r
+        if not args.no_cpu_baseline:
+            cb, _ = oracle_sample(w, 8.0)
+            cb.pop("seconds", None)
+            res["cpu_baseline"] = cb
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+"""ctypes binding of libfp8mla.so with the same names as the C ABI (include/fp8mla.h).
+
+Argument marshalling only: tensors are checked for device, dtype and layout,
+their device pointers and the current CUDA stream are passed through, and a
+non-zero status raises.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU fallback, and a missing library or missing CUDA
+device raises instead of computing anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KV8_DL, KV8_DR, KV8_D, KV8_BLOCK = 512, 64, 576, 64
+KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05 = 0, 1, 2
+STATUS = {0: "KV8_OK", -1: "KV8_EINVAL", -2: "KV8_EALIGN", -3: "KV8_EUNSUPPORTED",
+          -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Kv8Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().kv8_status_string(status).decode()
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({msg})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8mla.so, building it in-tree first if it is missing or stale."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not _build.up_to_date():
+                _build.build()
+            L = ctypes.CDLL(_build.LIB)
+            P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            sig = {
+                "kv8_quantize_rows": (i32, [P, i64, i64, P, P, P, i64, P]),
+                "mla_absorb_decode_fp8_workspace_size": (i64, [i64, i32, i32]),
+                "mla_absorb_decode_fp8": (i32, [P, P, P, P, i64, i32, f32, P, P, P, i64, i32, P]),
+                "mla_absorb_decode_fp8_batch_workspace_size": (i64, [i32, i32, i32, i32, i32]),
+                "mla_absorb_decode_fp8_batch": (i32, [P, P, P, P, P, P, i32, i32, i32, i32, i64, f32,
+                                                      P, P, P, i64, i32, P]),
+                "mla_absorb_decode_fp8_batch_partials": (i32, [P, P, P, P, P, P, i32, i32, i32, i32,
+                                                               i64, f32, P, i64, i32, P]),
+                "mla_absorb_decode_fp8_batch_combine": (i32, [P, i32, i32, i32, i32, P, P, P, i64,
+                                                              i32, P]),
+                "kv8_workspace_error": (i32, [P, P]),
+                "kv8_status_string": (ctypes.c_char_p, [i32]),
+                "kv8_abi_version": (i32, []),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return os.path.abspath(_build.LIB)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None, device=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _check(fn, status):
+    if status != 0:
+        raise Kv8Error(fn, status)
+
+
+# ----------------------------------------------------------------- quantizer
+def kv8_quantize_rows(src, kv_codes, kv_scales, dst_slot=None, stream=None):
+    """Quantize f32 rows src [n, >=576] (row stride = src.stride(0)) into the cache."""
+    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and src.is_cuda
+            and src.dim() == 2 and src.stride(1) == 1):
+        raise ValueError("src must be a CUDA float32 [n, >=576] tensor with unit column stride")
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    if dst_slot is not None:
+        _need(dst_slot, "dst_slot", torch.int64, 1)
+        if dst_slot.numel() != src.shape[0]:
+            raise ValueError("dst_slot must have one entry per source row")
+    st = lib().kv8_quantize_rows(_ptr(src), src.shape[0], src.stride(0), _ptr(dst_slot),
+                                 _ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0],
+                                 _stream(stream))
+    _check("kv8_quantize_rows", st)
+
+
+# ----------------------------------------------------------------- decode
+def mla_absorb_decode_fp8_workspace_size(T: int, H: int, variant: int = KV8_DECODE_AUTO) -> int:
+    n = lib().mla_absorb_decode_fp8_workspace_size(int(T), int(H), int(variant))
+    if n < 0:
+        raise ValueError("invalid T, H or variant")
+    return int(n)
+
+
+def mla_absorb_decode_fp8_batch_workspace_size(B: int, H: int, max_blocks: int,
+                                               block_size: int = KV8_BLOCK,
+                                               variant: int = KV8_DECODE_AUTO) -> int:
+    n = lib().mla_absorb_decode_fp8_batch_workspace_size(int(B), int(H), int(max_blocks),
+                                                         int(block_size), int(variant))
+    if n < 0:
+        raise ValueError("invalid B, H, max_blocks, block_size or variant")
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_absorb_decode_fp8(q_lat, q_rope, kv_codes, kv_scales, T, sm_scale, out=None, lse=None,
+                          workspace=None, variant=KV8_DECODE_AUTO, stream=None):
+    """One query (q_lat [H,512], q_rope [H,64]) against kv rows 0..T-1 -> out [H,512]."""
+    _need(q_lat, "q_lat", torch.float32, 2)
+    _need(q_rope, "q_rope", torch.float32, 2)
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    H = q_lat.shape[0]
+    if q_lat.shape[1] != KV8_DL or tuple(q_rope.shape) != (H, KV8_DR):
+        raise ValueError("q_lat must be [H,512] and q_rope [H,64]")
+    if T > kv_codes.shape[0] or T > kv_scales.shape[0]:
+        raise ValueError("T exceeds the cache rows")
+    if out is None:
+        out = torch.empty((H, KV8_DL), dtype=torch.float32, device=q_lat.device)
+    _need(out, "out", torch.float32, 2)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 1)
+    need = mla_absorb_decode_fp8_workspace_size(T, H, variant)
+    if workspace is None:
+        workspace = alloc_workspace(need, q_lat.device)
+    st = lib().mla_absorb_decode_fp8(_ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales),
+                                     int(T), H, float(sm_scale), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     int(variant), _stream(stream))
+    _check("mla_absorb_decode_fp8", st)
+    return out
+
+
+def mla_absorb_decode_fp8_batch(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
+                                sm_scale, out=None, lse=None, workspace=None,
+                                variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK, stream=None):
+    """B queries (q_lat [B,H,512], q_rope [B,H,64]) over a paged cache -> out [B,H,512]."""
+    _need(q_lat, "q_lat", torch.float32, 3)
+    _need(q_rope, "q_rope", torch.float32, 3)
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, H = q_lat.shape[:2]
+    if q_lat.shape[2] != KV8_DL or tuple(q_rope.shape) != (B, H, KV8_DR):
+        raise ValueError("q_lat must be [B,H,512] and q_rope [B,H,64]")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table and seq_lens need one row per sequence")
+    if out is None:
+        out = torch.empty((B, H, KV8_DL), dtype=torch.float32, device=q_lat.device)
+    _need(out, "out", torch.float32, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    max_blocks = block_table.shape[1]
+    n_blocks = kv_codes.shape[0] // block_size
+    need = mla_absorb_decode_fp8_batch_workspace_size(B, H, max_blocks, block_size, variant)
+    if workspace is None:
+        workspace = alloc_workspace(need, q_lat.device)
+    st = lib().mla_absorb_decode_fp8_batch(
+        _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
+        _ptr(seq_lens), B, H, max_blocks, int(block_size), int(n_blocks), float(sm_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        int(variant), _stream(stream))
+    _check("mla_absorb_decode_fp8_batch", st)
+    return out
+
+
+def mla_absorb_decode_fp8_batch_partials(q_lat, q_rope, kv_codes, kv_scales, block_table,
+                                         seq_lens, sm_scale, workspace,
+                                         variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK,
+                                         stream=None):
+    """Split phase 1: the split-T kernel only; partials stay in ``workspace``."""
+    B, H = q_lat.shape[:2]
+    st = lib().mla_absorb_decode_fp8_batch_partials(
+        _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
+        _ptr(seq_lens), B, H, block_table.shape[1], int(block_size),
+        int(kv_codes.shape[0] // block_size), float(sm_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(variant), _stream(stream))
+    _check("mla_absorb_decode_fp8_batch_partials", st)
+
+
+def mla_absorb_decode_fp8_batch_combine(seq_lens, H, max_blocks, out, lse, workspace,
+                                        variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK,
+                                        stream=None):
+    """Split phase 2: merge the workspace partials into ``out`` / ``lse``."""
+    st = lib().mla_absorb_decode_fp8_batch_combine(
+        _ptr(seq_lens), seq_lens.shape[0], int(H), int(max_blocks), int(block_size), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), int(variant),
+        _stream(stream))
+    _check("mla_absorb_decode_fp8_batch_combine", st)
+
+
+def kv8_workspace_error(workspace, stream=None) -> int:
+    return int(lib().kv8_workspace_error(_ptr(workspace), _stream(stream)))

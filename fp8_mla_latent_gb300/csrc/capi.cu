@@ -1,0 +1,263 @@
+// capi.cu -- the extern "C" boundary of libfp8mla.so: argument checks, split
+// planning and kernel dispatch.  Declarations and the contract of every call
+// are in include/fp8mla.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fp8mla.h"
+#include "kv8_internal.h"
+
+namespace kv8 {
+
+static int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool tc_available();  // decode_tc.cu
+
+SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
+  SplitPlan p{};
+  int v = variant;
+  if (v == kAuto) v = (H >= 16 && tc_available()) ? kTc : kSimt;
+  p.variant = v;
+  if (v == kTc) {
+    p.hg = H > 64 ? 64 : (int)align_up(H, 16);
+  } else {
+    p.hg = 4;
+  }
+  p.n_hg = (H + p.hg - 1) / p.hg;
+  const int64_t tiles = max_len > 0 ? (max_len + TILE - 1) / TILE : 1;
+  // One wave: the tensor-core kernel holds a whole SM per CTA, the SIMT kernel
+  // runs about four CTAs per SM.
+  const int64_t target = (int64_t)NUM_SMS * (v == kTc ? 1 : 4);
+  const int64_t jobs = (int64_t)B * p.n_hg * tiles;
+  int64_t st = (jobs + target - 1) / target;
+  if (st < 1) st = 1;
+  if (st > tiles) st = tiles;
+  p.split_tiles = (int)st;
+  p.n_splits = (int)((tiles + st - 1) / st);
+  const int64_t parts = (int64_t)B * p.n_splits * H;
+  int64_t off = 256;  // header: error word
+  p.off_m = off;
+  off = align_up(off + parts * 4, 256);
+  p.off_l = off;
+  off = align_up(off + parts * 4, 256);
+  p.off_o = off;
+  off = align_up(off + parts * DL * 4, 256);
+  p.ws_bytes = off;
+  return p;
+}
+
+}  // namespace kv8
+
+using namespace kv8;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes) {
+  if (workspace == nullptr || workspace_bytes < a.plan.ws_bytes) return KV8_EWORKSPACE;
+  if (!aligned(workspace, 256)) return KV8_EALIGN;
+  char* ws = static_cast<char*>(const_cast<void*>(workspace));
+  a.err = reinterpret_cast<unsigned*>(ws);
+  a.ws_m = reinterpret_cast<float*>(ws + a.plan.off_m);
+  a.ws_l = reinterpret_cast<float*>(ws + a.plan.off_l);
+  a.ws_o = reinterpret_cast<float*>(ws + a.plan.off_o);
+  return KV8_OK;
+}
+
+int run_partials(DecodeArgs& a, cudaStream_t s) {
+  if (cudaMemsetAsync(a.err, 0, sizeof(unsigned), s) != cudaSuccess) return KV8_ECUDA;
+  cudaError_t e = (a.plan.variant == kTc) ? launch_decode_tc(a, s) : launch_decode_simt(a, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? KV8_EUNSUPPORTED : KV8_ECUDA;
+  return KV8_OK;
+}
+
+int run_decode(DecodeArgs& a, void* workspace, int64_t workspace_bytes, cudaStream_t s) {
+  int st = bind_workspace(a, workspace, workspace_bytes);
+  if (st != KV8_OK) return st;
+  st = run_partials(a, s);
+  if (st != KV8_OK) return st;
+  if (launch_combine(a, s) != cudaSuccess) return KV8_ECUDA;
+  return KV8_OK;
+}
+
+bool valid_variant(int v) { return v == kAuto || v == kSimt || v == kTc; }
+
+}  // namespace
+
+extern "C" {
+
+int kv8_abi_version(void) { return 100; }
+
+const char* kv8_status_string(int status) {
+  switch (status) {
+    case KV8_OK: return "ok";
+    case KV8_EINVAL: return "invalid argument";
+    case KV8_EALIGN: return "pointer or stride misaligned";
+    case KV8_EUNSUPPORTED: return "unsupported size or variant";
+    case KV8_ECUDA: return "CUDA error";
+    case KV8_EBOUNDS: return "device-side index out of range";
+    case KV8_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int kv8_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                      const int64_t* dst_slot, uint8_t* kv_codes, float* kv_scales,
+                      int64_t n_slots, void* stream) {
+  if (n_rows < 0 || n_slots < 0) return KV8_EINVAL;
+  if (n_rows == 0) return KV8_OK;
+  if (src == nullptr || kv_codes == nullptr || kv_scales == nullptr) return KV8_EINVAL;
+  if (src_row_stride < KV8_D) return KV8_EINVAL;
+  if (dst_slot == nullptr && n_rows > n_slots) return KV8_EINVAL;
+  if (!aligned(src, 16) || (src_row_stride % 4) != 0 || !aligned(kv_codes, 16) ||
+      !aligned(kv_scales, 8))
+    return KV8_EALIGN;
+  cudaError_t e = launch_quantize(src, n_rows, src_row_stride, dst_slot, kv_codes, kv_scales,
+                                  n_slots, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
+}
+
+int64_t mla_absorb_decode_fp8_workspace_size(int64_t T, int H, int variant) {
+  if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant)) return -1;
+  return plan_decode(1, H, T, variant).ws_bytes;
+}
+
+int mla_absorb_decode_fp8(const float* q_lat, const float* q_rope, const uint8_t* kv_codes,
+                          const float* kv_scales, int64_t T, int H, float sm_scale, float* out,
+                          float* lse, void* workspace, int64_t workspace_bytes, int variant,
+                          void* stream) {
+  if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant)) return KV8_EINVAL;
+  if (q_lat == nullptr || q_rope == nullptr || out == nullptr) return KV8_EINVAL;
+  if (T > 0 && (kv_codes == nullptr || kv_scales == nullptr)) return KV8_EINVAL;
+  if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16) ||
+      !aligned(kv_codes, 16) || !aligned(kv_scales, 8) || !aligned(lse, 4))
+    return KV8_EALIGN;
+  DecodeArgs a{};
+  a.q_lat = q_lat;
+  a.q_rope = q_rope;
+  a.codes = kv_codes;
+  a.scales = kv_scales;
+  a.block_table = nullptr;
+  a.seq_lens = nullptr;
+  a.T_contig = T;
+  a.B = 1;
+  a.H = H;
+  a.max_blocks = 0;
+  a.n_blocks = 0;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.plan = plan_decode(1, H, T, variant);
+  return run_decode(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int64_t mla_absorb_decode_fp8_batch_workspace_size(int B, int H, int max_blocks, int block_size,
+                                                   int variant) {
+  if (B < 0 || H < 1 || H > 1024 || max_blocks < 1 || block_size != KV8_BLOCK ||
+      !valid_variant(variant))
+    return -1;
+  return plan_decode(B, H, (int64_t)max_blocks * block_size, variant).ws_bytes;
+}
+
+}  // extern "C"
+
+namespace {
+
+int batch_args(DecodeArgs& a, const float* q_lat, const float* q_rope, const uint8_t* kv_codes,
+               const float* kv_scales, const int32_t* block_table, const int32_t* seq_lens,
+               int B, int H, int max_blocks, int block_size, int64_t n_blocks, float sm_scale,
+               float* out, float* lse, int variant, bool need_inputs, bool need_outputs) {
+  if (B < 0 || H < 1 || H > 1024 || max_blocks < 1 || !valid_variant(variant)) return KV8_EINVAL;
+  if (need_inputs && n_blocks < 1) return KV8_EINVAL;
+  if (block_size != KV8_BLOCK) return KV8_EUNSUPPORTED;
+  if (seq_lens == nullptr || !aligned(seq_lens, 4)) return seq_lens ? KV8_EALIGN : KV8_EINVAL;
+  if (need_inputs) {
+    if (q_lat == nullptr || q_rope == nullptr || kv_codes == nullptr || kv_scales == nullptr ||
+        block_table == nullptr)
+      return KV8_EINVAL;
+    if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_codes, 16) ||
+        !aligned(kv_scales, 8) || !aligned(block_table, 4))
+      return KV8_EALIGN;
+  }
+  if (need_outputs) {
+    if (out == nullptr) return KV8_EINVAL;
+    if (!aligned(out, 16) || !aligned(lse, 4)) return KV8_EALIGN;
+  }
+  a = DecodeArgs{};
+  a.q_lat = q_lat;
+  a.q_rope = q_rope;
+  a.codes = kv_codes;
+  a.scales = kv_scales;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.T_contig = 0;
+  a.B = B;
+  a.H = H;
+  a.max_blocks = max_blocks;
+  a.n_blocks = n_blocks;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.plan = plan_decode(B, H, (int64_t)max_blocks * block_size, variant);
+  return KV8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_absorb_decode_fp8_batch(const float* q_lat, const float* q_rope, const uint8_t* kv_codes,
+                                const float* kv_scales, const int32_t* block_table,
+                                const int32_t* seq_lens, int B, int H, int max_blocks,
+                                int block_size, int64_t n_blocks, float sm_scale, float* out,
+                                float* lse, void* workspace, int64_t workspace_bytes,
+                                int variant, void* stream) {
+  DecodeArgs a;
+  int st = batch_args(a, q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, B, H,
+                      max_blocks, block_size, n_blocks, sm_scale, out, lse, variant, true, true);
+  if (st != KV8_OK || B == 0) return st;
+  return run_decode(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int mla_absorb_decode_fp8_batch_partials(const float* q_lat, const float* q_rope,
+                                         const uint8_t* kv_codes, const float* kv_scales,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int B, int H, int max_blocks, int block_size,
+                                         int64_t n_blocks, float sm_scale, void* workspace,
+                                         int64_t workspace_bytes, int variant, void* stream) {
+  DecodeArgs a;
+  int st = batch_args(a, q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, B, H,
+                      max_blocks, block_size, n_blocks, sm_scale, nullptr, nullptr, variant, true,
+                      false);
+  if (st != KV8_OK || B == 0) return st;
+  st = bind_workspace(a, workspace, workspace_bytes);
+  if (st != KV8_OK) return st;
+  return run_partials(a, static_cast<cudaStream_t>(stream));
+}
+
+int mla_absorb_decode_fp8_batch_combine(const int32_t* seq_lens, int B, int H, int max_blocks,
+                                        int block_size, float* out, float* lse,
+                                        const void* workspace, int64_t workspace_bytes,
+                                        int variant, void* stream) {
+  DecodeArgs a;
+  int st = batch_args(a, nullptr, nullptr, nullptr, nullptr, nullptr, seq_lens, B, H,
+                      max_blocks, block_size, 0, 0.f, out, lse, variant, false, true);
+  if (st != KV8_OK || B == 0) return st;
+  st = bind_workspace(a, workspace, workspace_bytes);
+  if (st != KV8_OK) return st;
+  return launch_combine(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV8_OK : KV8_ECUDA;
+}
+
+int kv8_workspace_error(const void* workspace, void* stream) {
+  if (workspace == nullptr) return KV8_EINVAL;
+  unsigned w = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&w, workspace, sizeof w, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KV8_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+  return w ? KV8_EBOUNDS : KV8_OK;
+}
+
+}  // extern "C"

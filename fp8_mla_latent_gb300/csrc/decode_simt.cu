@@ -1,0 +1,152 @@
+// decode_simt.cu -- CUDA-core split-T absorbed MLA decode over the e4m3 cache.
+//
+// KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"),
+// PR description: the latent is both key and value; the score and context loops
+// dequantize inline with the per-row scale hoisted out of each dot; closing
+// note: split-T kernels for long caches.
+//
+// Grid (split, head group, sequence); 8 warps per CTA, HG_SIMT heads per CTA.
+// Lane l owns latent channels [16l, 16l+16) and RoPE channels [512+2l, 512+2l+2),
+// so one token row (576 B) is read by the warp as 32 x 16 B + 32 x 2 B.  Each warp
+// walks tokens t0 + w, t0 + w + 8, ... keeping an online softmax per head in log2
+// units; the 8 warps are merged through shared memory and the split's partial
+// (m, l, o) goes to the workspace for the combine kernel.
+//
+// This is the kernel for small head counts (and a cross-check of the tensor-core
+// kernel): at H >= 16 its FP32 lanes, not HBM, bound it.
+#include "kv8_common.cuh"
+
+namespace kv8 {
+namespace {
+
+constexpr int HG_SIMT = 4;
+constexpr int SWARPS = 8;
+constexpr float LOG2E = 1.4426950408889634f;
+
+__global__ void __launch_bounds__(SWARPS * 32)
+decode_simt_kernel(DecodeArgs a) {
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t T = seq_len_of(a, b);
+  const int64_t split_len = (int64_t)a.plan.split_tiles * TILE;
+  const int64_t t0 = (int64_t)split * split_len;
+  if (t0 >= T) return;  // this split is empty; the combine kernel skips it
+  const int64_t t1 = (t0 + split_len < T) ? t0 + split_len : T;
+  const int h0 = g * HG_SIMT;
+
+  // query slices, pre-multiplied by sm_scale * log2(e) so scores come out in log2 units
+  const float c = a.sm_scale * LOG2E;
+  float qL[HG_SIMT][16], qR[HG_SIMT][2];
+#pragma unroll
+  for (int j = 0; j < HG_SIMT; ++j) {
+    const int h = h0 + j;
+    if (h < a.H) {
+      const float4* ql = reinterpret_cast<const float4*>(a.q_lat + ((int64_t)b * a.H + h) * DL);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = __ldg(&ql[lane * 4 + k]);
+        qL[j][4 * k] = v.x * c; qL[j][4 * k + 1] = v.y * c;
+        qL[j][4 * k + 2] = v.z * c; qL[j][4 * k + 3] = v.w * c;
+      }
+      const float2 r = __ldg(reinterpret_cast<const float2*>(
+          a.q_rope + ((int64_t)b * a.H + h) * DR + 2 * lane));
+      qR[j][0] = r.x * c; qR[j][1] = r.y * c;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) qL[j][k] = 0.f;
+      qR[j][0] = qR[j][1] = 0.f;
+    }
+  }
+
+  float m[HG_SIMT], l[HG_SIMT], o[HG_SIMT][16];
+#pragma unroll
+  for (int j = 0; j < HG_SIMT; ++j) {
+    m[j] = -INFINITY; l[j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[j][k] = 0.f;
+  }
+
+  for (int64_t t = t0 + warp; t < t1; t += SWARPS) {
+    const int64_t slot = slot_of(a, b, t);
+    if (slot < 0) continue;  // bad page: counted in the error word, read as empty
+    const uint8_t* row = a.codes + slot * D;
+    const uint4 cl = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+    const uint16_t cr = __ldg(reinterpret_cast<const uint16_t*>(row + DL) + lane);
+    const float2 sc = __ldg(reinterpret_cast<const float2*>(a.scales + slot * 2));
+    float v[16], vr[2];
+    e4m3x4_to_f32(cl.x, v); e4m3x4_to_f32(cl.y, v + 4);
+    e4m3x4_to_f32(cl.z, v + 8); e4m3x4_to_f32(cl.w, v + 12);
+    {
+      const uint32_t h2 = e4m3x2_to_f16x2(cr);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      vr[0] = f.x; vr[1] = f.y;
+    }
+#pragma unroll
+    for (int j = 0; j < HG_SIMT; ++j) {
+      float dl = 0.f, dr = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) dl = fmaf(qL[j][k], v[k], dl);
+      dr = fmaf(qR[j][0], vr[0], dr);
+      dr = fmaf(qR[j][1], vr[1], dr);
+      float z = sc.x * dl + sc.y * dr;  // scales hoisted out of the dots
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      const float mn = fmaxf(m[j], z);
+      const float alpha = exp2f(m[j] - mn);  // 0 on the first token (m = -inf)
+      const float p = exp2f(z - mn);
+      l[j] = l[j] * alpha + p;
+      const float w = p * sc.x;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[j][k] = fmaf(w, v[k], o[j][k] * alpha);
+      m[j] = mn;
+    }
+  }
+
+  // merge the 8 warps: max, then rescaled sums into shared memory
+  __shared__ float sm_m[SWARPS][HG_SIMT];
+  __shared__ float sm_M[HG_SIMT], sm_l[HG_SIMT];
+  __shared__ float sm_o[HG_SIMT][DL];
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < HG_SIMT; ++j) sm_m[warp][j] = m[j];
+  }
+  for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) (&sm_o[0][0])[i] = 0.f;
+  if (threadIdx.x < HG_SIMT) sm_l[threadIdx.x] = 0.f;
+  __syncthreads();
+  if (threadIdx.x < HG_SIMT) {
+    float M = -INFINITY;
+    for (int w = 0; w < SWARPS; ++w) M = fmaxf(M, sm_m[w][threadIdx.x]);
+    sm_M[threadIdx.x] = M;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < HG_SIMT; ++j) {
+    const float M = sm_M[j];
+    const float f = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - M);
+    if (f != 0.f) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) atomicAdd(&sm_o[j][lane * 16 + k], o[j][k] * f);
+      if (lane == 0) atomicAdd(&sm_l[j], l[j] * f);
+    }
+  }
+  __syncthreads();
+  const int64_t base = ((int64_t)b * a.plan.n_splits + split) * a.H;
+  for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) {
+    const int j = i / DL, d = i % DL, h = h0 + j;
+    if (h < a.H) a.ws_o[(base + h) * DL + d] = sm_o[j][d];
+  }
+  if (threadIdx.x < HG_SIMT && h0 + threadIdx.x < a.H) {
+    a.ws_m[base + h0 + threadIdx.x] = sm_M[threadIdx.x];
+    a.ws_l[base + h0 + threadIdx.x] = sm_l[threadIdx.x];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
+  dim3 grid(a.plan.n_splits, a.plan.n_hg, a.B);
+  decode_simt_kernel<<<grid, SWARPS * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kv8

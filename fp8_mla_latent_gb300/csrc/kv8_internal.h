@@ -1,0 +1,63 @@
+// kv8_internal.h -- launch interface shared by the C-ABI shim and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kv8 {
+
+constexpr int DL = 512;    // kv_lora latent width
+constexpr int DR = 64;     // qk_rope width
+constexpr int D = 576;     // bytes per cached row
+constexpr int PAGE = 64;   // tokens per page in the paged layout
+constexpr int TILE = 128;  // tokens per decode tile (the M of the score MMA)
+constexpr int NUM_SMS = 152;  // GB300: 2 dies x 76 SMs
+
+// Device-side error bits written into the workspace header.
+constexpr unsigned ERR_BLOCK_TABLE = 1u;
+constexpr unsigned ERR_SEQ_LEN = 2u;
+
+enum Variant { kAuto = 0, kSimt = 1, kTc = 2 };
+
+struct SplitPlan {
+  int variant;      // resolved: kSimt or kTc
+  int hg;           // heads per CTA (head group)
+  int n_hg;         // head groups
+  int split_tiles;  // tiles of TILE tokens per split
+  int n_splits;     // splits of the longest sequence
+  int64_t ws_bytes; // workspace bytes needed
+  // byte offsets inside the workspace
+  int64_t off_m, off_l, off_o;
+};
+
+// Deterministic in its arguments (no device query), so the workspace-size call
+// and the decode call always agree.
+SplitPlan plan_decode(int B, int H, int64_t max_len, int variant);
+
+struct DecodeArgs {
+  const float* q_lat;          // [B][H][512]
+  const float* q_rope;         // [B][H][64]
+  const uint8_t* codes;        // [slots][576]
+  const float* scales;         // [slots][2]
+  const int32_t* block_table;  // [B][max_blocks] or nullptr (contiguous, B == 1)
+  const int32_t* seq_lens;     // [B] or nullptr (then T_contig)
+  int64_t T_contig;
+  int B, H, max_blocks;
+  int64_t n_blocks;
+  float sm_scale;
+  float* out;                  // [B][H][512]
+  float* lse;                  // [B][H] or nullptr
+  unsigned* err;               // workspace header word
+  float* ws_m;                 // [B][n_splits][H]   running max, log2 units
+  float* ws_l;                 // [B][n_splits][H]   sum of exp2(z - m)
+  float* ws_o;                 // [B][n_splits][H][512] unnormalised context
+  SplitPlan plan;
+};
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_quantize(const float* src, int64_t n_rows, int64_t stride,
+                            const int64_t* dst_slot, uint8_t* codes, float* scales,
+                            int64_t n_slots, cudaStream_t s);
+
+}  // namespace kv8

@@ -1,0 +1,191 @@
+/*
+ * fp8mla.h -- C ABI of libfp8mla.so: an fp8 e4m3 latent KV cache and absorbed
+ * MLA decode attention over it, hand-written CUDA for one GB300 (sm_103a).
+ *
+ * Source of the method: the pull-request page "KV8=1: fp8 e4m3 latent KV cache
+ * (CPU + CUDA) with .coli_kv v2" (the "KV8 page").  The page names the calls
+ * (c/kv_fp8.h per-row quantizer; CUDA entry points for absorbed decode and its
+ * batched form) but prints no signatures; the ones below are ours.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
+ *   caller owns all memory, including the decode workspace; the library never
+ *   allocates device memory and keeps no state between calls.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call is asynchronous on it: nothing synchronises, and
+ *   results are ready only when the stream reaches them.  Calls are thread-safe.
+ * - A call first validates its arguments on the host and returns a negative
+ *   kv8_status before launching anything if they are bad.  A failed kernel
+ *   launch returns KV8_ECUDA.  No kernel traps or spins without a bound.
+ * - Cache layout (one layer; our reading, the page states no byte layout):
+ *     kv_codes [n_slots][576] uint8 -- e4m3fn bytes; bytes 0..511 are the
+ *               latent Lc (kv_lora, both key and value), 512..575 the RoPE key
+ *               Rc (qk_rope).  Rows are 576 = 36 x 16 bytes, so every row starts
+ *               on a 16-byte boundary when kv_codes does.
+ *     kv_scales[n_slots][2]  float  -- {sLc, sRc}, each amax/448 of its segment.
+ */
+#ifndef FP8MLA_H
+#define FP8MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV8_DL 512    /* kv_lora: latent width (key and value)    */
+#define KV8_DR 64     /* qk_rope: RoPE key width (key only)        */
+#define KV8_D 576     /* bytes per cached row                      */
+#define KV8_BLOCK 64  /* tokens per page of the paged batch layout */
+
+typedef enum {
+    KV8_OK = 0,
+    KV8_EINVAL = -1,        /* null pointer, negative size, bad dimension            */
+    KV8_EALIGN = -2,        /* a pointer or stride breaks the alignment rule stated  */
+    KV8_EUNSUPPORTED = -3,  /* a size this build does not handle (e.g. block_size)   */
+    KV8_ECUDA = -4,         /* a CUDA launch or runtime call failed                  */
+    KV8_EBOUNDS = -5,       /* a device-side index (block table, seq_len) was bad    */
+    KV8_EWORKSPACE = -6     /* workspace missing or smaller than *_workspace_size    */
+} kv8_status;
+
+/* Decode kernel choice.  Both accumulate in f32; the tensor-core kernel rounds
+ * the query and the softmax weights to fp16 for the MMA (the cache's e4m3
+ * values convert to fp16 exactly).  Tolerance class of both: max-abs error
+ * <= 2e-3 * max|out| against the exact attention of the stored cache.          */
+typedef enum {
+    KV8_DECODE_AUTO = 0,     /* tcgen05 when H >= 16, else SIMT                   */
+    KV8_DECODE_SIMT = 1,     /* CUDA-core split-T kernel, any H >= 1              */
+    KV8_DECODE_TCGEN05 = 2   /* tcgen05 tensor-core split-T kernel, H >= 1        */
+} kv8_decode_variant;
+
+/* ---------------------------------------------------------------------------
+ * kv8_quantize_rows -- KV8 page, PR description, c/kv_fp8.h item ("per-row
+ * quantizer with a subnormal-amax guard") and attention_rows item (the producer
+ * quantizes the fresh normed/roped row instead of copying f32).
+ *
+ * For each source row r, and for each segment (Lc = floats 0..511, Rc = floats
+ * 512..575) separately:
+ *   amax = max |x| over non-NaN entries;  scale = amax / 448 (f32, RN);
+ *   inv  = 448 / amax (f32, RN);
+ *   if inv is not finite (amax == 0 or amax < 448/FLT_MAX): every code is a
+ *     signed zero (0x80 for negative x, 0x00 otherwise and for NaN);
+ *   else code = e4m3(x * inv) with the product rounded once (no FMA), rounding
+ *     to nearest even, saturating to +-448 (0x7E/0xFE), keeping the sign of
+ *     zero, and storing NaN as 0x00.
+ * The 576 codes go to kv_codes[slot] and {sLc, sRc} to kv_scales[slot], where
+ * slot = dst_slot[r] (device int64 array), or r when dst_slot is NULL.
+ * The result is bit-identical to the oracle for every f32 input.
+ *
+ *   src            device f32 [n_rows][src_row_stride]; 16-byte aligned,
+ *                  src_row_stride (in floats) >= 576 and a multiple of 4.
+ *   n_rows         >= 0 (0 launches nothing).
+ *   dst_slot       device int64 [n_rows] or NULL.  A slot outside [0, n_slots)
+ *                  is skipped (that row writes nothing).
+ *   kv_codes       device uint8 [n_slots][576], 16-byte aligned.
+ *   kv_scales      device f32 [n_slots][2], 8-byte aligned.
+ *   n_slots        rows in the cache pool; with dst_slot == NULL, >= n_rows.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int kv8_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                      const int64_t* dst_slot, uint8_t* kv_codes, float* kv_scales,
+                      int64_t n_slots, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph ("the
+ * latent is both key and value in the absorbed attention"), attention_rows item
+ * (score and context loops dequantize inline "with the scale hoisted out of the
+ * dot"), CUDA item (absorbed decode kernel over fp8 rows); the closing note's
+ * split-T kernels for long caches.
+ *
+ * One decode query (H heads) against one contiguous cache of T rows (slots
+ * 0..T-1).  For each head h:
+ *   z_t  = sm_scale * ( sLc_t * <q_lat[h], dec(Lc_t)> + sRc_t * <q_rope[h], dec(Rc_t)> )
+ *   p_t  = softmax_t(z)_t
+ *   out[h][:] = sum_t p_t * sLc_t * dec(Lc_t)        (latent-space context)
+ *   lse[h]    = log sum_t exp(z_t)                   (natural log)
+ * T == 0 gives out = 0 and lse = -inf.
+ *
+ *   q_lat     device f32 [H][512], 16-byte aligned.
+ *   q_rope    device f32 [H][64],  16-byte aligned.
+ *   kv_codes  device uint8 [>= T][576], 16-byte aligned.
+ *   kv_scales device f32 [>= T][2], 8-byte aligned.
+ *   T         >= 0.  H >= 1 and H <= 1024.
+ *   out       device f32 [H][512], 16-byte aligned.  lse: device f32 [H] or NULL.
+ *   workspace device, >= mla_absorb_decode_fp8_workspace_size(T, H, variant)
+ *             bytes, 256-byte aligned; scratch for the split-T partials.  Calls
+ *             that overlap in time must not share a workspace.
+ *   variant   a kv8_decode_variant.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_EWORKSPACE, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int64_t mla_absorb_decode_fp8_workspace_size(int64_t T, int H, int variant);
+int mla_absorb_decode_fp8(const float* q_lat, const float* q_rope, const uint8_t* kv_codes,
+                          const float* kv_scales, int64_t T, int H, float sm_scale, float* out,
+                          float* lse, void* workspace, int64_t workspace_bytes, int variant,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------
+ * mla_absorb_decode_fp8_batch -- the batched form (KV8 page, CUDA item: the
+ * batched absorbed kernel).  Our reading of "batch": B ragged sequences, one
+ * decode query each, whose rows sit in 64-token pages of one pool.  Token t of
+ * sequence b is cache slot block_table[b][t / 64] * 64 + t % 64.  Per sequence
+ * the arithmetic is that of mla_absorb_decode_fp8.
+ *
+ *   q_lat       device f32 [B][H][512];  q_rope device f32 [B][H][64].
+ *   kv_codes    device uint8 [n_blocks * 64][576];  kv_scales f32 [n_blocks*64][2].
+ *   block_table device int32 [B][max_blocks];  seq_lens device int32 [B].
+ *   block_size  must be 64 (KV8_EUNSUPPORTED otherwise).
+ *   out         device f32 [B][H][512];  lse device f32 [B][H] or NULL.
+ *   workspace   >= mla_absorb_decode_fp8_batch_workspace_size(B, H, max_blocks,
+ *               block_size, variant) bytes, 256-byte aligned.
+ * Device-side checks: a seq_len outside [0, max_blocks*64] is clamped, and a
+ * block-table entry outside [0, n_blocks) makes its page read as empty; either
+ * sets an error word in the workspace that kv8_workspace_error() reports.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_EUNSUPPORTED, KV8_EWORKSPACE, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int64_t mla_absorb_decode_fp8_batch_workspace_size(int B, int H, int max_blocks, int block_size,
+                                                   int variant);
+int mla_absorb_decode_fp8_batch(const float* q_lat, const float* q_rope, const uint8_t* kv_codes,
+                                const float* kv_scales, const int32_t* block_table,
+                                const int32_t* seq_lens, int B, int H, int max_blocks,
+                                int block_size, int64_t n_blocks, float sm_scale, float* out,
+                                float* lse, void* workspace, int64_t workspace_bytes,
+                                int variant, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Split phases of mla_absorb_decode_fp8_batch.  The batched call is exactly
+ * _partials followed by _combine on the same stream and workspace.  _partials
+ * runs the split-T kernel and leaves, per (sequence, split, head), the running
+ * maximum m (log2 units), the sum l of 2^(z*log2e - m) and the unnormalised
+ * context o in the workspace; _combine merges them into out/lse.  Exposed so a
+ * caller can time the phases, or merge partials computed elsewhere (the same
+ * log-sum-exp recombination joins the partials of one sequence split across
+ * devices).  Arguments and errors as for mla_absorb_decode_fp8_batch.
+ * ------------------------------------------------------------------------- */
+int mla_absorb_decode_fp8_batch_partials(const float* q_lat, const float* q_rope,
+                                         const uint8_t* kv_codes, const float* kv_scales,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int B, int H, int max_blocks, int block_size,
+                                         int64_t n_blocks, float sm_scale, void* workspace,
+                                         int64_t workspace_bytes, int variant, void* stream);
+int mla_absorb_decode_fp8_batch_combine(const int32_t* seq_lens, int B, int H, int max_blocks,
+                                        int block_size, float* out, float* lse,
+                                        const void* workspace, int64_t workspace_bytes,
+                                        int variant, void* stream);
+
+/* kv8_workspace_error -- synchronises `stream`, then reports the device-side
+ * error word of the last decode call that used `workspace`: KV8_OK or
+ * KV8_EBOUNDS.  A debugging aid; the decode calls themselves never sync. */
+int kv8_workspace_error(const void* workspace, void* stream);
+
+/* Human-readable text for a kv8_status value (static storage). */
+const char* kv8_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int kv8_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8MLA_H */

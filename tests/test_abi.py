@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library loads, exports every call the header
+declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import fp8_mla_latent_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8mla.h")
+
+EINVAL, EALIGN, EUNSUPPORTED, EWORKSPACE = -1, -2, -3, -6
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_documented_calls():
+    names = declared_functions()
+    for want in ("kv8_quantize_rows", "mla_absorb_decode_fp8", "mla_absorb_decode_fp8_batch",
+                 "mla_absorb_decode_fp8_workspace_size",
+                 "mla_absorb_decode_fp8_batch_workspace_size", "kv8_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = pkg.lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_status_strings_and_version():
+    L = pkg.lib()
+    assert L.kv8_abi_version() >= 100
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert L.kv8_status_string(s)
+    assert L.kv8_status_string(12345) == b"unknown status"
+
+
+def P(x):
+    return ctypes.c_void_p(x)
+
+
+def test_quantize_rejects_bad_arguments_on_host():
+    L = pkg.lib()
+    f = L.kv8_quantize_rows
+    good = 1 << 20  # a 16-byte aligned fake address: never dereferenced because validation fails
+    assert f(P(good), -1, 576, None, P(good), P(good), 10, None) == EINVAL
+    assert f(None, 4, 576, None, P(good), P(good), 10, None) == EINVAL
+    assert f(P(good), 4, 575, None, P(good), P(good), 10, None) == EINVAL
+    assert f(P(good), 11, 576, None, P(good), P(good), 10, None) == EINVAL
+    assert f(P(good + 4), 4, 576, None, P(good), P(good), 10, None) == EALIGN
+    assert f(P(good), 4, 578, None, P(good), P(good), 10, None) == EALIGN
+    assert f(P(good), 4, 576, None, P(good + 8), P(good), 10, None) == EALIGN
+    assert f(P(good), 4, 576, None, P(good), P(good + 4), 10, None) == EALIGN
+    assert f(P(good), 0, 576, None, None, None, 0, None) == 0  # nothing to do
+
+
+def test_decode_rejects_bad_arguments_on_host():
+    L = pkg.lib()
+    g = 1 << 20
+    d = L.mla_absorb_decode_fp8
+    assert d(P(g), P(g), P(g), P(g), -1, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
+    assert d(P(g), P(g), P(g), P(g), 10, 0, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 7, None) == EINVAL
+    assert d(None, P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
+    assert d(P(g + 8), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EALIGN
+    assert d(P(g), P(g), P(g + 1), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EALIGN
+    need = L.mla_absorb_decode_fp8_workspace_size(10, 4, 0)
+    assert need > 0
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), need - 1, 0, None) == EWORKSPACE
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, None, need, 0, None) == EWORKSPACE
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g + 16), need, 0, None) == EALIGN
+    b = L.mla_absorb_decode_fp8_batch
+    args = [P(g)] * 6 + [2, 4, 8, 64, 16, 0.1, P(g), None, P(g), 1 << 30, 0, None]
+    a = list(args)
+    a[9] = 32
+    assert b(*a) == EUNSUPPORTED
+    a = list(args)
+    a[4] = None
+    assert b(*a) == EINVAL
+    a = list(args)
+    a[10] = 0
+    assert b(*a) == EINVAL
+    assert b(*([P(g)] * 6 + [0, 4, 8, 64, 16, 0.1, P(g), None, P(g), 1 << 30, 0, None])) == 0
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_workspace_sizes(variant):
+    L = pkg.lib()
+    for T, H in ((0, 1), (1, 4), (256, 4), (4096, 128), (262144, 128)):
+        n = L.mla_absorb_decode_fp8_workspace_size(T, H, variant)
+        assert n >= 256 and n % 256 == 0
+    assert L.mla_absorb_decode_fp8_workspace_size(-1, 4, variant) < 0
+    assert L.mla_absorb_decode_fp8_batch_workspace_size(32, 128, 512, 64, variant) > 0
+    assert L.mla_absorb_decode_fp8_batch_workspace_size(32, 128, 512, 32, variant) < 0
+    # more tokens never needs a smaller workspace per split partial
+    assert (L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 4096, 64, variant)
+            >= L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 1, 64, variant))

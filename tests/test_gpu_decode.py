@@ -1,0 +1,199 @@
+"""GPU decode parity against the f64 oracle.
+
+Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv
+v2"), PR description (absorbed attention over the e4m3 latent rows, scales
+hoisted out of the dots) and closing note (split-T).  Tolerance: max-abs error
+<= 2e-3 * max|out| per sequence, lse within 2e-3 (both kernels accumulate in
+f32; the tensor-core kernel rounds q and the softmax weights to fp16).
+Caches are filled by the library's quantizer and the oracle reads the same
+codes, so these tests isolate attention.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_mla_latent_gb300 as pkg
+from fp8_mla_latent_gb300 import workloads
+
+from gpu_helpers import check, decode, upload_cache
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {"simt": pkg.KV8_DECODE_SIMT, "tcgen05": pkg.KV8_DECODE_TCGEN05}
+
+
+def tc_ready():
+    try:
+        d = torch.device("cuda:0")
+        q = torch.zeros((16, 512), device=d)
+        r = torch.zeros((16, 64), device=d)
+        c = torch.zeros((1, 576), dtype=torch.uint8, device=d)
+        s = torch.zeros((1, 2), device=d)
+        pkg.mla_absorb_decode_fp8(q, r, c, s, 1, 0.1, variant=pkg.KV8_DECODE_TCGEN05)
+        return True
+    except pkg.Kv8Error as e:
+        if e.status == -3:
+            return False
+        raise
+
+
+@pytest.fixture(params=list(VARIANTS))
+def variant(request):
+    v = VARIANTS[request.param]
+    if v == pkg.KV8_DECODE_TCGEN05 and not tc_ready():
+        pytest.skip("tensor-core decode not built in this library")
+    return v
+
+
+def all_pairs(w, head_block=None):
+    hb = head_block or w.H
+    return [(b, (h, min(h + hb, w.H))) for b in range(w.B) for h in range(0, w.H, hb)]
+
+
+SMALL = [("tiny", 1.0), ("single", 0.25), ("batched", 0.03), ("long", 0.01), ("append", 0.05)]
+
+
+@pytest.mark.parametrize("name,scale", SMALL)
+def test_workloads_small(name, scale, variant):
+    w = workloads.make(name, scale=scale)
+    codes, scales = upload_cache(w)
+    out, lse = decode(w, codes, scales, variant)
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    rng = np.random.default_rng(0)
+    if w.H * int(w.seq_lens.sum()) <= 4_000_000:
+        pairs = all_pairs(w)
+    else:  # every sequence, a random block of 8 heads
+        pairs = [(b, (h, h + 8)) for b in range(w.B)
+                 for h in [int(rng.integers(0, max(1, w.H - 8)))]]
+    check(w, out, lse, c, s, pairs)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 1000])
+@pytest.mark.parametrize("H", [1, 3, 16, 17, 64, 100, 128])
+def test_ragged_lengths_and_head_counts(T, H, variant):
+    if H * T > 128 * 300 and T > 300:
+        pytest.skip("covered by the workload tests")
+    rng = np.random.default_rng(T * 1000 + H)
+    w = workloads.make("tiny", scale=1.0, seed=T + H)
+    x = rng.standard_normal((T, 576)).astype(np.float32) * np.exp(
+        0.5 * rng.standard_normal(576)).astype(np.float32)
+    w.cache_rows = x
+    w.cache_slots = np.arange(T, dtype=np.int64)
+    w.n_slots = ((T + 63) // 64) * 64
+    w.seq_lens = np.array([T], np.int32)
+    w.block_table = np.arange(w.n_slots // 64, dtype=np.int32)[None]
+    w.H = H
+    w.q_lat = rng.standard_normal((1, H, 512)).astype(np.float32)
+    w.q_rope = rng.standard_normal((1, H, 64)).astype(np.float32)
+    codes, scales = upload_cache(w)
+    for contiguous in (True, False):
+        out, lse = decode(w, codes, scales, variant, contiguous=contiguous)
+        check(w, out, lse, codes.cpu().numpy(), scales.cpu().numpy(), all_pairs(w))
+
+
+def test_empty_cache_single(variant):
+    d = torch.device("cuda:0")
+    q = torch.randn((16, 512), device=d)
+    r = torch.randn((16, 64), device=d)
+    c = torch.zeros((1, 576), dtype=torch.uint8, device=d)
+    s = torch.zeros((1, 2), device=d)
+    lse = torch.empty(16, device=d)
+    out = pkg.mla_absorb_decode_fp8(q, r, c, s, 0, 0.1, lse=lse, variant=variant)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_batch_with_empty_and_short_sequences(variant):
+    w = workloads.make("batched", scale=0.01)
+    w.seq_lens = w.seq_lens.copy()
+    w.seq_lens[0] = 0
+    w.seq_lens[1] = 1
+    w.seq_lens[2] = 64
+    codes, scales = upload_cache(w)
+    out, lse = decode(w, codes, scales, variant)
+    check(w, out, lse, codes.cpu().numpy(), scales.cpu().numpy(),
+          [(b, (0, 16)) for b in range(6)])
+
+
+def test_paged_permutation_is_bitwise_identical(variant):
+    """Same tokens in the same logical order: any physical page permutation gives
+    the same bits."""
+    w = workloads.make("long", scale=0.01)
+    codes, scales = upload_cache(w)
+    out_a, lse_a = decode(w, codes, scales, variant)
+    rng = np.random.default_rng(1)
+    nb = w.n_slots // 64
+    perm = rng.permutation(nb).astype(np.int32)
+    c2 = torch.empty_like(codes)
+    s2 = torch.empty_like(scales)
+    p = torch.from_numpy(perm.astype(np.int64)).to(codes.device)
+    c2.view(nb, 64, 576)[p] = codes.view(nb, 64, 576)
+    s2.view(nb, 64, 2)[p] = scales.view(nb, 64, 2)
+    w.block_table = perm[w.block_table]
+    out_b, lse_b = decode(w, c2, s2, variant)
+    assert np.array_equal(out_a.view(np.uint32), out_b.view(np.uint32))
+    assert np.array_equal(lse_a.view(np.uint32), lse_b.view(np.uint32))
+
+
+def test_bad_block_table_and_seq_len_report_ebounds(variant):
+    w = workloads.make("batched", scale=0.01)
+    codes, scales = upload_cache(w)
+    d = torch.device("cuda:0")
+    bt = torch.from_numpy(w.block_table).to(d)
+    bt[0, 0] = 10 ** 6
+    bt[1, 1] = -5
+    sl = torch.from_numpy(w.seq_lens).to(d)
+    sl[2] = w.max_blocks * 64 + 1000
+    ql = torch.from_numpy(w.q_lat).to(d)
+    qr = torch.from_numpy(w.q_rope).to(d)
+    ws = pkg.alloc_workspace(pkg.mla_absorb_decode_fp8_batch_workspace_size(
+        w.B, w.H, w.max_blocks, variant=variant), d)
+    out = pkg.mla_absorb_decode_fp8_batch(ql, qr, codes, scales, bt, sl, w.sm_scale,
+                                          workspace=ws, variant=variant)
+    assert pkg.kv8_workspace_error(ws) == -5
+    assert torch.isfinite(out[3:]).all()
+    # a clean call on the same workspace clears the error word
+    pkg.mla_absorb_decode_fp8_batch(ql, qr, codes, scales, torch.from_numpy(w.block_table).to(d),
+                                    torch.from_numpy(w.seq_lens).to(d), w.sm_scale, workspace=ws,
+                                    variant=variant)
+    assert pkg.kv8_workspace_error(ws) == 0
+
+
+def test_split_phases_equal_the_fused_call(variant):
+    w = workloads.make("append", scale=0.05)
+    codes, scales = upload_cache(w)
+    d = torch.device("cuda:0")
+    ql = torch.from_numpy(w.q_lat).to(d)
+    qr = torch.from_numpy(w.q_rope).to(d)
+    bt = torch.from_numpy(w.block_table).to(d)
+    sl = torch.from_numpy(w.seq_lens).to(d)
+    ws = pkg.alloc_workspace(pkg.mla_absorb_decode_fp8_batch_workspace_size(
+        w.B, w.H, w.max_blocks, variant=variant), d)
+    ref = pkg.mla_absorb_decode_fp8_batch(ql, qr, codes, scales, bt, sl, w.sm_scale,
+                                          workspace=ws, variant=variant).clone()
+    out = torch.empty_like(ref)
+    lse = torch.empty((w.B, w.H), device=d)
+    pkg.mla_absorb_decode_fp8_batch_partials(ql, qr, codes, scales, bt, sl, w.sm_scale, ws,
+                                             variant=variant)
+    pkg.mla_absorb_decode_fp8_batch_combine(sl, w.H, w.max_blocks, out, lse, ws, variant=variant)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+FULL = ["single", "long", "batched", "append"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name, variant):
+    """Full-size workloads in the benchmark's launch configuration; sampled heads."""
+    if variant == pkg.KV8_DECODE_SIMT and name in ("long", "batched"):
+        pytest.skip("the CUDA-core kernel is checked at full size on the smaller workloads")
+    w = workloads.make(name)
+    codes, scales = upload_cache(w)
+    out, lse = decode(w, codes, scales, variant)
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    rng = np.random.default_rng(7)
+    bs = rng.choice(w.B, size=min(w.B, 2), replace=False)
+    pairs = [(int(b), (h, h + 1)) for b in bs for h in rng.choice(w.H, size=2, replace=False)]
+    check(w, out, lse, c, s, pairs)
+    assert np.isfinite(out).all()
