@@ -19,7 +19,7 @@ from . import build as _build
 KV8_DL, KV8_DR, KV8_D, KV8_BLOCK = 512, 64, 576, 64
 KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05 = 0, 1, 2
 STATUS = {0: "KV8_OK", -1: "KV8_EINVAL", -2: "KV8_EALIGN", -3: "KV8_EUNSUPPORTED",
-          -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE"}
+          -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE", -7: "KV8_ETIMEOUT"}
 
 _lock = threading.Lock()
 _lib = None

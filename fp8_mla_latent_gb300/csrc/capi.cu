@@ -20,7 +20,7 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   if (v == kAuto) v = (H >= 16 && tc_available()) ? kTc : kSimt;
   p.variant = v;
   if (v == kTc) {
-    p.hg = H > 64 ? 64 : (int)align_up(H, 16);
+    p.hg = H <= 16 ? 16 : (H <= 32 ? 32 : 64);  // MMA N = heads per CTA
   } else {
     p.hg = 4;
   }
@@ -99,6 +99,7 @@ const char* kv8_status_string(int status) {
     case KV8_ECUDA: return "CUDA error";
     case KV8_EBOUNDS: return "device-side index out of range";
     case KV8_EWORKSPACE: return "workspace missing or too small";
+    case KV8_ETIMEOUT: return "device-side wait timed out";
     default: return "unknown status";
   }
 }
@@ -257,6 +258,7 @@ int kv8_workspace_error(const void* workspace, void* stream) {
   if (cudaMemcpyAsync(&w, workspace, sizeof w, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return KV8_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+  if (w & ERR_TIMEOUT) return KV8_ETIMEOUT;
   return w ? KV8_EBOUNDS : KV8_OK;
 }
 

@@ -9,7 +9,7 @@
 // Lane l owns latent channels [16l, 16l+16) and RoPE channels [512+2l, 512+2l+2),
 // so one token row (576 B) is read by the warp as 32 x 16 B + 32 x 2 B.  Each warp
 // walks tokens t0 + w, t0 + w + 8, ... keeping an online softmax per head in log2
-// units; the 8 warps are merged through shared memory and the split's partial
+// units; the 8 warps are merged in a fixed order through shared memory and the split's partial
 // (m, l, o) goes to the workspace for the combine kernel.
 //
 // This is the kernel for small head counts (and a cross-check of the tensor-core
@@ -119,17 +119,19 @@ decode_simt_kernel(DecodeArgs a) {
     sm_M[threadIdx.x] = M;
   }
   __syncthreads();
+  // fixed-order sum over the warps (no atomics), so results are bitwise reproducible
+  for (int wr = 0; wr < SWARPS; ++wr) {
+    if (warp == wr) {
 #pragma unroll
-  for (int j = 0; j < HG_SIMT; ++j) {
-    const float M = sm_M[j];
-    const float f = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - M);
-    if (f != 0.f) {
+      for (int j = 0; j < HG_SIMT; ++j) {
+        const float f = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - sm_M[j]);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) atomicAdd(&sm_o[j][lane * 16 + k], o[j][k] * f);
-      if (lane == 0) atomicAdd(&sm_l[j], l[j] * f);
+        for (int k = 0; k < 16; ++k) sm_o[j][lane * 16 + k] += o[j][k] * f;
+        if (lane == 0) sm_l[j] += l[j] * f;
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
   const int64_t base = ((int64_t)b * a.plan.n_splits + split) * a.H;
   for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) {
     const int j = i / DL, d = i % DL, h = h0 + j;

@@ -15,6 +15,7 @@ constexpr int NUM_SMS = 152;  // GB300: 2 dies x 76 SMs
 // Device-side error bits written into the workspace header.
 constexpr unsigned ERR_BLOCK_TABLE = 1u;
 constexpr unsigned ERR_SEQ_LEN = 2u;
+constexpr unsigned ERR_TIMEOUT = 4u;  // a bounded wait in a kernel gave up
 
 enum Variant { kAuto = 0, kSimt = 1, kTc = 2 };
 

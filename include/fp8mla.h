@@ -47,7 +47,8 @@ typedef enum {
     KV8_EUNSUPPORTED = -3,  /* a size this build does not handle (e.g. block_size)   */
     KV8_ECUDA = -4,         /* a CUDA launch or runtime call failed                  */
     KV8_EBOUNDS = -5,       /* a device-side index (block table, seq_len) was bad    */
-    KV8_EWORKSPACE = -6     /* workspace missing or smaller than *_workspace_size    */
+    KV8_EWORKSPACE = -6,    /* workspace missing or smaller than *_workspace_size    */
+    KV8_ETIMEOUT = -7       /* a bounded device-side wait gave up (internal error)   */
 } kv8_status;
 
 /* Decode kernel choice.  Both accumulate in f32; the tensor-core kernel rounds
@@ -175,8 +176,10 @@ int mla_absorb_decode_fp8_batch_combine(const int32_t* seq_lens, int B, int H, i
                                         int variant, void* stream);
 
 /* kv8_workspace_error -- synchronises `stream`, then reports the device-side
- * error word of the last decode call that used `workspace`: KV8_OK or
- * KV8_EBOUNDS.  A debugging aid; the decode calls themselves never sync. */
+ * error word of the last decode call that used `workspace`: KV8_OK,
+ * KV8_EBOUNDS (a bad block-table entry or seq_len) or KV8_ETIMEOUT (a kernel
+ * gave up a wait after its bound and returned without a result).  A debugging
+ * aid; the decode calls themselves never sync. */
 int kv8_workspace_error(const void* workspace, void* stream);
 
 /* Human-readable text for a kv8_status value (static storage). */

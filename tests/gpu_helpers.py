@@ -39,9 +39,11 @@ def decode(w, codes, scales, variant, lse=True, contiguous=None):
     if contiguous:
         T = int(w.seq_lens[0])
         l = torch.empty((w.H,), dtype=torch.float32, device=d) if lse else None
+        ws = pkg.alloc_workspace(pkg.mla_absorb_decode_fp8_workspace_size(T, w.H, variant), d)
         out = pkg.mla_absorb_decode_fp8(ql[0], qr[0], codes, scales, T, w.sm_scale, lse=l,
-                                        variant=variant)
+                                        workspace=ws, variant=variant)
         torch.cuda.synchronize()
+        assert pkg.kv8_workspace_error(ws) == 0
         return out[None].cpu().numpy(), (l[None].cpu().numpy() if lse else None)
     bt = torch.from_numpy(w.block_table).to(d)
     sl = torch.from_numpy(w.seq_lens).to(d)

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol():
 def test_status_strings_and_version():
     L = pkg.lib()
     assert L.kv8_abi_version() >= 100
-    for s in (0, -1, -2, -3, -4, -5, -6):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
         assert L.kv8_status_string(s)
     assert L.kv8_status_string(12345) == b"unknown status"
 
