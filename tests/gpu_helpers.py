@@ -9,8 +9,13 @@ import torch
 import fp8_mla_latent_gb300 as pkg
 import oracle
 
-TOL = 2e-3       # max-abs error <= TOL * max|out| per sequence (f32 accumulation class)
+# max-abs error <= TOL * max|out| per sequence against the f64 oracle on the same codes:
+#   CUDA-core kernel (f32 operands and accumulation): 2e-3;
+#   tensor-core kernel (16-bit MMA operands: q and the softmax weights rounded to fp16,
+#   f32 accumulation): 1e-2, the class the decode tolerance sets for 16-bit operands.
+TOLS = {1: 2e-3, 2: 1e-2}
 LSE_TOL = 2e-3   # natural-log units
+WORST = {}       # variant -> worst observed err / max|out|, reported by the tests
 
 
 def dev():
@@ -65,8 +70,9 @@ def oracle_heads(w, codes_np, scales_np, b, heads):
                                 slots=slots, heads=(h0, h1 - h0))
 
 
-def check(w, out, lse, codes_np, scales_np, pairs):
-    """pairs: list of (b, (h0, h1)) blocks to compare; returns the worst ratio err/(TOL*max)."""
+def check(w, out, lse, codes_np, scales_np, pairs, variant=1):
+    """pairs: list of (b, (h0, h1)) blocks to compare; returns the worst err / max|out|."""
+    TOL = TOLS[variant]
     worst = 0.0
     for b, (h0, h1) in pairs:
         ref, ref_lse = oracle_heads(w, codes_np, scales_np, b, (h0, h1))
@@ -78,8 +84,9 @@ def check(w, out, lse, codes_np, scales_np, pairs):
             continue
         assert np.isfinite(got).all(), f"non-finite output b={b}"
         assert err <= TOL * scale, f"b={b} h={h0}:{h1} err {err:.3e} > {TOL} * {scale:.3e}"
-        worst = max(worst, err / (TOL * scale))
+        worst = max(worst, err / scale)
         if lse is not None:
             lerr = np.abs(lse[b, h0:h1] - ref_lse).max()
             assert lerr <= LSE_TOL * max(1.0, np.abs(ref_lse).max()), f"lse err {lerr}"
+    WORST[variant] = max(WORST.get(variant, 0.0), worst)
     return worst
