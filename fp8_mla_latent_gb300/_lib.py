@@ -19,7 +19,8 @@ from . import build as _build
 KV8_DL, KV8_DR, KV8_D, KV8_BLOCK = 512, 64, 576, 64
 KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05 = 0, 1, 2
 STATUS = {0: "KV8_OK", -1: "KV8_EINVAL", -2: "KV8_EALIGN", -3: "KV8_EUNSUPPORTED",
-          -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE", -7: "KV8_ETIMEOUT"}
+          -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE", -7: "KV8_ETIMEOUT",
+          -8: "KV8_ESCRATCH"}
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +53,9 @@ def lib() -> ctypes.CDLL:
                                                                i64, f32, P, i64, i32, P]),
                 "mla_absorb_decode_fp8_batch_combine": (i32, [P, i32, i32, i32, i32, P, P, P, i64,
                                                               i32, P]),
+                "mla_absorb_decode_fp8_batch_noalloc": (i32, [P, P, P, P, P, P, i32, i32, i32, i32,
+                                                              i64, f32, P, P, i32, P]),
+                "kv8_noalloc_error": (i32, [P]),
                 "kv8_workspace_error": (i32, [P, P]),
                 "kv8_status_string": (ctypes.c_char_p, [i32]),
                 "kv8_abi_version": (i32, []),
@@ -226,3 +230,22 @@ def mla_absorb_decode_fp8_batch_combine(seq_lens, H, max_blocks, out, lse, works
 
 def kv8_workspace_error(workspace, stream=None) -> int:
     return int(lib().kv8_workspace_error(_ptr(workspace), _stream(stream)))
+
+
+def mla_absorb_decode_fp8_batch_noalloc(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
+                                        sm_scale, out=None, lse=None, variant=KV8_DECODE_AUTO,
+                                        block_size=KV8_BLOCK, stream=None):
+    """The batched decode without a caller workspace (for callers that cannot
+    allocate device memory): partials go to the library's static device scratch."""
+    _need(q_lat, "q_lat", torch.float32, 3)
+    _need(q_rope, "q_rope", torch.float32, 3)
+    B, H = q_lat.shape[:2]
+    if out is None:
+        out = torch.empty((B, H, KV8_DL), dtype=torch.float32, device=q_lat.device)
+    st = lib().mla_absorb_decode_fp8_batch_noalloc(
+        _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
+        _ptr(seq_lens), B, H, block_table.shape[1], int(block_size),
+        int(kv_codes.shape[0] // block_size), float(sm_scale), _ptr(out), _ptr(lse), int(variant),
+        _stream(stream))
+    _check("mla_absorb_decode_fp8_batch_noalloc", st)
+    return out

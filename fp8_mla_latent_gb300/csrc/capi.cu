@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/fp8mla.h"
 #include "kv8_internal.h"
@@ -100,6 +101,7 @@ const char* kv8_status_string(int status) {
     case KV8_EBOUNDS: return "device-side index out of range";
     case KV8_EWORKSPACE: return "workspace missing or too small";
     case KV8_ETIMEOUT: return "device-side wait timed out";
+    case KV8_ESCRATCH: return "problem needs more scratch than the static no-alloc buffer";
     default: return "unknown status";
   }
 }
@@ -260,6 +262,71 @@ int kv8_workspace_error(const void* workspace, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
   if (w & ERR_TIMEOUT) return KV8_ETIMEOUT;
   return w ? KV8_EBOUNDS : KV8_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation decode.  For callers that cannot allocate device memory (a host
+// runtime that owns every buffer and passes only inputs and outputs, or a loop
+// with a fixed memory budget): the split-T partials live in one scratch array
+// declared here, in device memory, for the life of the process.  In host code
+// the array's name is only a stand-in for the symbol, never a device address:
+// its address is looked up once per device with cudaGetSymbolAddress.
+
+namespace {
+
+constexpr int64_t kNoallocBytes = KV8_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (looked up on first use).
+int noalloc_scratch(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KV8_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KV8_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return KV8_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return KV8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_absorb_decode_fp8_batch_noalloc(const float* q_lat, const float* q_rope,
+                                        const uint8_t* kv_codes, const float* kv_scales,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int B, int H, int max_blocks, int block_size,
+                                        int64_t n_blocks, float sm_scale, float* out,
+                                        float* lse, int variant, void* stream) {
+  DecodeArgs a;
+  int st = batch_args(a, q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, B, H,
+                      max_blocks, block_size, n_blocks, sm_scale, out, lse, variant, true, true);
+  if (st != KV8_OK || B == 0) return st;
+  if (a.plan.ws_bytes > kNoallocBytes) return KV8_ESCRATCH;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != KV8_OK) return st;
+  // run_decode clears the error word before the split kernel; the partials are
+  // written before they are read, so nothing else needs zeroing.
+  return run_decode(a, scratch, kNoallocBytes, static_cast<cudaStream_t>(stream));
+}
+
+int kv8_noalloc_error(void* stream) {
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != KV8_OK) return st;
+  return kv8_workspace_error(scratch, stream);
 }
 
 }  // extern "C"

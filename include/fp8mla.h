@@ -48,7 +48,8 @@ typedef enum {
     KV8_ECUDA = -4,         /* a CUDA launch or runtime call failed                  */
     KV8_EBOUNDS = -5,       /* a device-side index (block table, seq_len) was bad    */
     KV8_EWORKSPACE = -6,    /* workspace missing or smaller than *_workspace_size    */
-    KV8_ETIMEOUT = -7       /* a bounded device-side wait gave up (internal error)   */
+    KV8_ETIMEOUT = -7,      /* a bounded device-side wait gave up (internal error)   */
+    KV8_ESCRATCH = -8       /* problem too large for the library's static scratch    */
 } kv8_status;
 
 /* Decode kernel choice.  Both accumulate in f32.  Tolerance classes, as max-abs
@@ -178,6 +179,44 @@ int mla_absorb_decode_fp8_batch_combine(const int32_t* seq_lens, int B, int H, i
                                         int block_size, float* out, float* lse,
                                         const void* workspace, int64_t workspace_bytes,
                                         int variant, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * mla_absorb_decode_fp8_batch_noalloc -- mla_absorb_decode_fp8_batch for
+ * callers that cannot allocate device memory: code that runs where no
+ * allocator may be called (a host runtime or plugin that owns every device
+ * buffer and hands out only inputs and outputs, a hot loop whose memory budget
+ * is fixed up front) and so has no way to provide a workspace.  The paper has no
+ * counterpart; this is a convenience of this library.
+ *
+ * Same arguments, arithmetic and result as mla_absorb_decode_fp8_batch, minus
+ * the workspace: the split-T partials go to one scratch array that the library
+ * declares statically in device memory, KV8_NOALLOC_SCRATCH_BYTES (32 MiB) on
+ * every GPU that loads the library, held until the process exits.  The call
+ * allocates nothing and calls no allocating routine.
+ * - Size limit: a problem whose workspace
+ *   (mla_absorb_decode_fp8_batch_workspace_size) exceeds the scratch size is
+ *   rejected with KV8_ESCRATCH before anything is launched.
+ * - First call on a device: it looks up the scratch array's device address,
+ *   with that device current, and caches it; make that first call before any
+ *   stream capture on the device.
+ * - Sharing: every call on a device uses the same scratch, which keeps the last
+ *   call's contents.  Calls that can overlap on the GPU (different streams, or
+ *   different host threads, without ordering between them) race on it and must
+ *   not be issued that way; calls on one stream are ordered and safe.  The
+ *   device-side error word is cleared by each call and can be read with
+ *   kv8_noalloc_error().
+ * Errors: as mla_absorb_decode_fp8_batch, plus KV8_ESCRATCH.
+ * ------------------------------------------------------------------------- */
+#define KV8_NOALLOC_SCRATCH_BYTES (32ll << 20)
+int mla_absorb_decode_fp8_batch_noalloc(const float* q_lat, const float* q_rope,
+                                        const uint8_t* kv_codes, const float* kv_scales,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int B, int H, int max_blocks, int block_size,
+                                        int64_t n_blocks, float sm_scale, float* out,
+                                        float* lse, int variant, void* stream);
+/* Synchronises `stream` and reports the error word of the last no-alloc call on
+ * the current device, like kv8_workspace_error(). */
+int kv8_noalloc_error(void* stream);
 
 /* kv8_workspace_error -- synchronises `stream`, then reports the device-side
  * error word of the last decode call that used `workspace`: KV8_OK,
