@@ -145,7 +145,7 @@ def run_ours(args, rank, world, local_rank):
     variant = {"auto": pkg.KV8_DECODE_AUTO, "simt": pkg.KV8_DECODE_SIMT,
                "tcgen05": pkg.KV8_DECODE_TCGEN05}[args.variant]
 
-    w = workloads.make(args.workload)
+    w = workloads.make(args.workload, scale=args.scale)
     codes = torch.zeros((w.n_slots, 576), dtype=torch.uint8, device=dev)
     scales = torch.zeros((w.n_slots, 2), dtype=torch.float32, device=dev)
     pkg.kv8_quantize_rows(torch.from_numpy(w.cache_rows).to(dev), codes, scales,
@@ -295,7 +295,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f32 accum",
         "data": "synthetic (seeded; shapes and value mix of the workload, see DESIGN.md)",
         "token_heads_per_s": tok_heads / (ms_step * 1e-3),
-        "config": {"workload": args.workload, "B": w.B, "H": w.H,
+        "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H,
                    "T_total": w.total_tokens, "kv_lora": 512, "qk_rope": 64,
                    "variant": {1: "simt", 2: "tcgen05"}[plan_variant],
                    "l2": "flushed between steps (256 MB write) and KV > L2",
@@ -382,7 +382,7 @@ def run_reference(args, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; same workload as our arm)",
-        "config": {"workload": args.workload, "B": w.B, "H": w.H, "T_total": w.total_tokens},
+        "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H, "T_total": w.total_tokens},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
                          "sample": cb["sample"] + f"; {args.steps} steps"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -400,6 +400,8 @@ def main():
     ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="shrink token counts (profiling captures only; the bench line is scale 1)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -26,7 +26,7 @@
 //   warps 1-4   softmax: thread <-> TMEM lane <-> token row of the tile; tile
 //               max / sum per head by warp transposed reductions, lazy rescaling
 //               of O (only when a head's max grows by more than 2^8).
-//   warps 5-12  converters: 16-byte global loads of e4m3 rows (two chunks ahead
+//   warps 5-12  converters: 16-byte global loads of e4m3 rows (six chunks ahead
 //               in registers; the bulk-copy engine prefetches tiles into L2),
 //               exact cvt to fp16, swizzled 16-byte stores into a 6-slot ring.
 // MMA issue order is S(0), S(1), V(0), S(2), V(1), ...: the scores of tile i+1
@@ -45,6 +45,8 @@ constexpr int RING = 6;                      // fp16 Lc chunk slots (even: pairs
 constexpr int RC_SLOTS = 2;
 constexpr int CHUNK = TILE * 64 * 2;         // 16 KB: 128 rows x 64 fp16
 constexpr int NCONV = 8;
+constexpr int CONV_DEPTH = 6;               // chunks of e4m3 loads in flight per converter
+constexpr int L2_AHEAD = 3;                 // tiles prefetched into L2 ahead of the converters
 constexpr int NSOFT = 4;
 constexpr int WARP_SOFT = 1;
 constexpr int WARP_CONV = WARP_SOFT + NSOFT;
@@ -562,7 +564,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       x0 = p0 ? ldg16(p0 + dim0) : make_uint4(0u, 0u, 0u, 0u);
       x1 = p1 ? ldg16(p1 + dim0) : make_uint4(0u, 0u, 0u, 0u);
     };
-    uint4 R[3][2];
+    // CONV_DEPTH chunks of loads stay in flight per thread (8 KB per chunk per CTA)
+    uint4 R[CONV_DEPTH][2];
     uint32_t k = 0;
     bool ok = true;
     auto convert_store = [&](uint32_t dst, int r, const uint4& x) {
@@ -574,8 +577,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       sts128(dst + sw128(r, 2 * sub), make_uint4(h[0], h[1], h[2], h[3]));
       sts128(dst + sw128(r, 2 * sub + 1), make_uint4(h[4], h[5], h[6], h[7]));
     };
-    auto step = [&](int j, uint4 (&cur)[2], uint4 (&ahead)[2]) -> bool {
-      if (j + 2 < total) load(j + 2, ahead[0], ahead[1]);
+    // convert chunk j (its codes are in cur), publish it, then refill cur with chunk j + CONV_DEPTH
+    auto step = [&](int j, uint4 (&cur)[2]) -> bool {
       const ChunkInfo ci = chunk_info(j, n_tiles);
       uint64_t* full;
       uint32_t dst;
@@ -598,9 +601,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(full);
-      // L2 prefetch of the tile two ahead, once per tile, by the bulk-copy engine
-      if (ct == 0 && !ci.v && ci.c == 0 && ci.tile + 2 < n_tiles) {
-        const int64_t tb = t0 + (int64_t)(ci.tile + 2) * TILE;
+      if (j + CONV_DEPTH < total) load(j + CONV_DEPTH, cur[0], cur[1]);
+      // L2 prefetch of the tile L2_AHEAD tiles ahead, once per tile, by the bulk-copy engine
+      if (ct == 0 && !ci.v && ci.c == 0 && ci.tile + L2_AHEAD < n_tiles) {
+        const int64_t tb = t0 + (int64_t)(ci.tile + L2_AHEAD) * TILE;
         for (int pg = 0; pg < TILE / PAGE; ++pg) {
           const int64_t tk = tb + pg * PAGE;
           if (tk >= t_end) break;
@@ -611,12 +615,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       }
       return true;
     };
-    load(0, R[0][0], R[0][1]);
-    if (total > 1) load(1, R[1][0], R[1][1]);
-    for (int j = 0; j < total && ok; j += 3) {
-      ok = step(j, R[0], R[2]);
-      if (ok && j + 1 < total) ok = step(j + 1, R[1], R[0]);
-      if (ok && j + 2 < total) ok = step(j + 2, R[2], R[1]);
+    // the first tiles' lines: ask the bulk-copy engine for them before the loads below
+    if (ct == 0) {
+      for (int tl = 0; tl < L2_AHEAD && tl < n_tiles; ++tl) {
+        for (int pg = 0; pg < TILE / PAGE; ++pg) {
+          const int64_t tk = t0 + (int64_t)tl * TILE + pg * PAGE;
+          if (tk >= t_end) break;
+          const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
+          const int64_t slot = slot_of(a, b, tk);
+          if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < CONV_DEPTH; ++d)
+      if (d < total) load(d, R[d][0], R[d][1]);
+    for (int j0 = 0; j0 < total && ok; j0 += CONV_DEPTH) {
+#pragma unroll
+      for (int d = 0; d < CONV_DEPTH; ++d)
+        if (ok && j0 + d < total) ok = step(j0 + d, R[d]);
     }
     if (!ok) {
       *abort_flag = 1;
