@@ -26,17 +26,13 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
     p.hg = 4;
   }
   p.n_hg = (H + p.hg - 1) / p.hg;
-  const int64_t tiles = max_len > 0 ? (max_len + TILE - 1) / TILE : 1;
+  (void)max_len;
   // One wave: the tensor-core kernel holds a whole SM per CTA, the SIMT kernel
-  // runs about four CTAs per SM.
-  const int64_t target = (int64_t)NUM_SMS * (v == kTc ? 1 : 4);
-  const int64_t jobs = (int64_t)B * p.n_hg * tiles;
-  int64_t st = (jobs + target - 1) / target;
-  if (st < 1) st = 1;
-  if (st > tiles) st = tiles;
-  p.split_tiles = (int)st;
-  p.n_splits = (int)((tiles + st - 1) / st);
-  const int64_t parts = (int64_t)B * p.n_splits * H;
+  // runs about four CTAs per SM.  Cutting every (sequence, head group) into
+  // items of ceil(jobs / target) tiles gives at most target + B * n_hg items.
+  p.target = NUM_SMS * (v == kTc ? 1 : 4);
+  p.max_items = p.target + B * p.n_hg;
+  const int64_t parts = (int64_t)p.max_items * p.hg;
   int64_t off = 256;  // header: error word
   p.off_m = off;
   off = align_up(off + parts * 4, 256);

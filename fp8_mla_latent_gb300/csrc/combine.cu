@@ -1,4 +1,6 @@
 // combine.cu -- merge of the split-T partials (flash-decoding log-sum-exp merge).
+// The partials of (sequence, head) are those of the work items of its head
+// group, found from the sequence lengths exactly as the split kernel cut them.
 //
 // KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"),
 // closing note: split-T kernels remove the T caps of the CUDA path.  With the
@@ -13,22 +15,30 @@ namespace {
 
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   const int h = blockIdx.x, b = blockIdx.y;
-  const int64_t T = seq_len_of(a, b);
-  const int64_t split_len = (int64_t)a.plan.split_tiles * TILE;
-  const int ns = (int)((T + split_len - 1) / split_len);
-  const int64_t base = (int64_t)b * a.plan.n_splits * a.H + h;  // + s * H
+  __shared__ long long s_first, s_count;
+  if (threadIdx.x < 32) {
+    int64_t f, c;
+    item_range(a, b, h / a.plan.hg, f, c);
+    if (threadIdx.x == 0) {
+      s_first = f;
+      s_count = c;
+    }
+  }
+  __syncthreads();
+  const int64_t first = s_first, ns = s_count;
+  const int hl = h % a.plan.hg;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_m[base + (int64_t)s * a.H]);
+  for (int64_t s = 0; s < ns; ++s) M = fmaxf(M, a.ws_m[(first + s) * a.plan.hg + hl]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float ms = a.ws_m[base + (int64_t)s * a.H];
+    for (int64_t s = 0; s < ns; ++s) {
+      const int64_t part = (first + s) * a.plan.hg + hl;
+      const float ms = a.ws_m[part];
       if (ms == -INFINITY) continue;
       const float w = exp2f(ms - M);
-      L += w * a.ws_l[base + (int64_t)s * a.H];
-      const float4 o = reinterpret_cast<const float4*>(
-          a.ws_o + (base + (int64_t)s * a.H) * DL)[threadIdx.x];
+      L += w * a.ws_l[part];
+      const float4 o = reinterpret_cast<const float4*>(a.ws_o + part * DL)[threadIdx.x];
       acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
     }
   }

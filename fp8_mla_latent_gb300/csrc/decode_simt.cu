@@ -5,7 +5,8 @@
 // dequantize inline with the per-row scale hoisted out of each dot; closing
 // note: split-T kernels for long caches.
 //
-// Grid (split, head group, sequence); 8 warps per CTA, HG_SIMT heads per CTA.
+// One CTA per work item (sequence, head group of HG_SIMT heads, token range);
+// 8 warps per CTA.
 // Lane l owns latent channels [16l, 16l+16) and RoPE channels [512+2l, 512+2l+2),
 // so one token row (576 B) is read by the warp as 32 x 16 B + 32 x 2 B.  Each warp
 // walks tokens t0 + w, t0 + w + 8, ... keeping an online softmax per head in log2
@@ -25,13 +26,21 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(SWARPS * 32)
 decode_simt_kernel(DecodeArgs a) {
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t T = seq_len_of(a, b);
-  const int64_t split_len = (int64_t)a.plan.split_tiles * TILE;
-  const int64_t t0 = (int64_t)split * split_len;
-  if (t0 >= T) return;  // this split is empty; the combine kernel skips it
-  const int64_t t1 = (t0 + split_len < T) ? t0 + split_len : T;
+  __shared__ WorkItem s_it;
+  __shared__ int s_ok;
+  if (warp == 0) {
+    WorkItem it;
+    const bool ok = find_item(a, blockIdx.x, it);
+    if (lane == 0) {
+      s_it = it;
+      s_ok = ok ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;  // past the last work item of this call
+  const int b = s_it.b, g = s_it.g;
+  const int64_t t0 = s_it.t0, t1 = s_it.t1;
   const int h0 = g * HG_SIMT;
 
   // query slices, pre-multiplied by sm_scale * log2(e) so scores come out in log2 units
@@ -132,22 +141,21 @@ decode_simt_kernel(DecodeArgs a) {
     }
     __syncthreads();
   }
-  const int64_t base = ((int64_t)b * a.plan.n_splits + split) * a.H;
+  const int64_t base = (int64_t)blockIdx.x * HG_SIMT;  // this item's partials
   for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) {
-    const int j = i / DL, d = i % DL, h = h0 + j;
-    if (h < a.H) a.ws_o[(base + h) * DL + d] = sm_o[j][d];
+    const int j = i / DL, d = i % DL;
+    if (h0 + j < a.H) a.ws_o[(base + j) * DL + d] = sm_o[j][d];
   }
   if (threadIdx.x < HG_SIMT && h0 + threadIdx.x < a.H) {
-    a.ws_m[base + h0 + threadIdx.x] = sm_M[threadIdx.x];
-    a.ws_l[base + h0 + threadIdx.x] = sm_l[threadIdx.x];
+    a.ws_m[base + threadIdx.x] = sm_M[threadIdx.x];
+    a.ws_l[base + threadIdx.x] = sm_l[threadIdx.x];
   }
 }
 
 }  // namespace
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s) {
-  dim3 grid(a.plan.n_splits, a.plan.n_hg, a.B);
-  decode_simt_kernel<<<grid, SWARPS * 32, 0, s>>>(a);
+  decode_simt_kernel<<<a.plan.max_items, SWARPS * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 

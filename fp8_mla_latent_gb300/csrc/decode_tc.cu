@@ -9,7 +9,8 @@
 //   z_t = sm * ( sLc_t <q_lat, dec(Lc_t)> + sRc_t <q_rope, dec(Rc_t)> )
 //   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)
 //
-// One CTA = one (split of T, group of N heads, sequence); N in {16, 32, 64}.
+// One CTA = one work item (sequence, group of N heads, range of tiles); N in
+// {16, 32, 64}.
 // The two contractions of a 128-token tile run on the tensor cores with fp16
 // operands and f32 accumulators in TMEM; the per-row scales stay outside the MMA:
 //   S^T[t][h] = K_t . Q_h      M = 128 tokens, N heads, K = 512 (S_L) and 64 (S_R)
@@ -176,13 +177,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  const int split = blockIdx.x, g_head = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t T = seq_len_of(a, b);
-  const int64_t split_len = (int64_t)a.plan.split_tiles * TILE;
-  const int64_t t0 = (int64_t)split * split_len;
-  if (t0 >= T) return;  // empty split: the combine kernel skips it
-  const int64_t t_end = (t0 + split_len < T) ? t0 + split_len : T;
+  __shared__ WorkItem s_it;
+  __shared__ int s_ok;
+  if (warp == 0) {
+    WorkItem it;
+    const bool ok = find_item(a, blockIdx.x, it);
+    if (lane == 0) {
+      s_it = it;
+      s_ok = ok ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;  // past the last work item of this call
+  const int g_head = s_it.g, b = s_it.b;
+  const int64_t t0 = s_it.t0, t_end = s_it.t1;
   const int n_tiles = (int)((t_end - t0 + TILE - 1) / TILE);
   const int total_chunks = PERIOD * n_tiles;
   const int h0 = g_head * N;
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
         if (group_sync(1, n_tiles)) {
           // epilogue: unnormalised partial o = acc * s_ref, with (m, l) per head
           tc_fence_after();
-          const int64_t base = ((int64_t)b * a.plan.n_splits + split) * a.H + h0;
+          const int64_t base = (int64_t)blockIdx.x * N;  // this item's partials
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -660,8 +669,7 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.plan.n_splits, a.plan.n_hg, a.B);
-  decode_tc_kernel<N><<<grid, NTHREADS, smem, s>>>(a);
+  decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 

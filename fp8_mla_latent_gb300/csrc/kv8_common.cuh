@@ -57,4 +57,94 @@ __device__ __forceinline__ int64_t seq_len_of(const DecodeArgs& a, int b) {
   return T;
 }
 
+// ---------------------------------------------------------------------------
+// Work items of a decode call.  The tokens of every (sequence, head group) are
+// cut into items of `st` tiles, st = ceil(total tiles x head groups / target),
+// so the items of a ragged batch spread evenly over one wave of CTAs.  Items are
+// numbered by sequence, then head group, then position; every kernel of a call
+// derives the same numbering from the sequence lengths, on the device.
+
+struct WorkItem {
+  int b, g;        // sequence, head group
+  int64_t t0, t1;  // tokens [t0, t1) of sequence b
+};
+
+__device__ __forceinline__ int64_t tiles_of(const DecodeArgs& a, int b) {
+  return (seq_len_of(a, b) + TILE - 1) / TILE;
+}
+
+// Warp-wide (all 32 lanes): tiles per item for this call.
+__device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a) {
+  const int lane = threadIdx.x & 31;
+  int64_t total = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    int64_t t = (b0 + lane < a.B) ? tiles_of(a, b0 + lane) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    total += t;
+  }
+  const int64_t jobs = total * a.plan.n_hg;
+  const int64_t st = (jobs + a.plan.target - 1) / a.plan.target;
+  return st < 1 ? 1 : st;
+}
+
+// Warp-wide: walks the sequences 32 at a time with the inclusive scan of their
+// item counts and calls f(b, first item of b, items per head group, st) in every
+// lane for the sequence holding item k (k >= 0) or for sequence want_b (k < 0).
+// Returns false if no sequence matched.
+template <typename F>
+__device__ __forceinline__ bool scan_items(const DecodeArgs& a, int64_t k, int want_b, F&& f) {
+  const int lane = threadIdx.x & 31;
+  const int64_t st = item_tiles(a);
+  int64_t base = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int64_t tiles = (b < a.B) ? tiles_of(a, b) : 0;
+    const int64_t ns = (tiles + st - 1) / st;
+    const int64_t cnt = ns * a.plan.n_hg;
+    int64_t inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const int64_t first = base + inc - cnt;
+    const bool mine = (b < a.B) && (k >= 0 ? (k >= first && k < first + cnt) : (b == want_b));
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      f(__shfl_sync(0xffffffffu, b, src), __shfl_sync(0xffffffffu, first, src),
+        __shfl_sync(0xffffffffu, ns, src), st);
+      return true;
+    }
+    base += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  return false;
+}
+
+// Warp-wide: the work item with index k; false if k is past the last item.
+__device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it) {
+  return scan_items(a, k, -1, [&](int b, int64_t first, int64_t ns, int64_t st) {
+    const int64_t r = k - first;
+    const int64_t s = r % ns;
+    it.b = b;
+    it.g = (int)(r / ns);
+    it.t0 = s * st * TILE;
+    const int64_t T = seq_len_of(a, b);
+    const int64_t e = (s + 1) * st * TILE;
+    it.t1 = e < T ? e : T;
+  });
+}
+
+// Warp-wide: first item and item count of (sequence b, head group g).
+__device__ __forceinline__ void item_range(const DecodeArgs& a, int b, int g, int64_t& first,
+                                           int64_t& count) {
+  first = 0;
+  count = 0;
+  scan_items(a, -1, b, [&](int, int64_t f0, int64_t ns, int64_t) {
+    first = f0 + (int64_t)g * ns;
+    count = ns;
+  });
+}
+
 }  // namespace kv8

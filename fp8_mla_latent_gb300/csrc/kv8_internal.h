@@ -23,8 +23,8 @@ struct SplitPlan {
   int variant;      // resolved: kSimt or kTc
   int hg;           // heads per CTA (head group)
   int n_hg;         // head groups
-  int split_tiles;  // tiles of TILE tokens per split
-  int n_splits;     // splits of the longest sequence
+  int target;       // CTAs the work is spread over (one wave of the split kernel)
+  int max_items;    // upper bound on work items: the split kernel's grid size
   int64_t ws_bytes; // workspace bytes needed
   // byte offsets inside the workspace
   int64_t off_m, off_l, off_o;
@@ -48,9 +48,9 @@ struct DecodeArgs {
   float* out;                  // [B][H][512]
   float* lse;                  // [B][H] or nullptr
   unsigned* err;               // workspace header word
-  float* ws_m;                 // [B][n_splits][H]   running max, log2 units
-  float* ws_l;                 // [B][n_splits][H]   sum of exp2(z - m)
-  float* ws_o;                 // [B][n_splits][H][512] unnormalised context
+  float* ws_m;                 // [max_items][hg]   running max, log2 units
+  float* ws_l;                 // [max_items][hg]   sum of exp2(z - m)
+  float* ws_o;                 // [max_items][hg][512] unnormalised context
   SplitPlan plan;
 };
 
