@@ -23,7 +23,8 @@
 // converted twice per tile (once for each contraction) but never held whole.
 //
 // Warp roles (13 warps):
-//   warp 0      one thread issues every tcgen05.mma; the warp owns TMEM.
+//   warp 0      issues every tcgen05.mma (lane 0 alone, or for N = 16 the whole
+//               warp with one elected lane); the warp owns TMEM.
 //   warps 1-8   softmax, two groups of four warps; a thread owns one token row
 //               (its TMEM lane) and half of the heads: tile max per head by a
 //               transposed warp reduction, running denominators per thread, lazy
@@ -294,45 +295,67 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
 
   if (warp == 0) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // Narrow head groups (light softmax) issue from the whole converged warp with
+    // elect.sync; wider ones from lane 0 alone, which leaves more issue slots on
+    // this SM sub-partition to the softmax warps that share it (measured both
+    // ways on the workloads of each width).
+    constexpr bool WARP_ISSUE = (N <= 16);
+    if (WARP_ISSUE || lane == 0) {
       const uint32_t idS = idesc_f16(128, N, false, false);
       const uint32_t idV = idesc_f16(128, N, true, false);
-      auto wait_full = [&](int j) -> bool {
-        if (!mbar_wait(&bars[B_FULL + (j % RING)], (j / RING) & 1, abort_flag, WAIT_NS))
-          return false;
-        tc_fence_after();
-        return true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(bar, parity, abort_flag, WAIT_NS);
+        if constexpr (WARP_ISSUE) return __all_sync(0xffffffffu, ok);
+        return ok;
       };
+      auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+        if constexpr (WARP_ISSUE) mma_f16_warp(d, ad, bd, id, acc);
+        else mma_f16(d, ad, bd, id, acc);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (WARP_ISSUE) mma_commit_warp(bar);
+        else mma_commit(bar);
+      };
+      auto wait_full = [&](int j) -> bool {
+        const bool ok = wait(&bars[B_FULL + (j % RING)], (j / RING) & 1);
+        tc_fence_after();
+        return ok;
+      };
+      // Within a tile the loops run straight through; a failed wait only marks
+      // the tile bad (the abort flag then makes every later wait return at once).
       auto issue_S = [&](int i) -> bool {
         const int buf = i & 1;
-        if (!mbar_wait(&bars[B_S_EMPTY + buf], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS))
-          return false;
+        if (!wait(&bars[B_S_EMPTY + buf], ((i >> 1) & 1) ^ 1)) return false;
         tc_fence_after();
         const uint32_t dL = tmem + buf * 2 * N, dR = dL + N;
         const int base = s_base(i);
+        bool good = true;
         for (int c = 0; c < 9; ++c) {
           const int j = base + c;
-          if (!wait_full(j)) return false;
+          good = wait_full(j) && good;
           const uint32_t ab = ring_base + (j % RING) * CHUNK, bb = q_base + c * N * 128;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(c < 8 ? dL : dR, smem_desc(ab + kk * 32, 16, 1024, SW128),
-                    smem_desc(bb + kk * 32, 16, 1024, SW128), idS, (c == 8 ? kk : (c | kk)) != 0);
-          mma_commit(&bars[B_EMPTY + (j % RING)]);
+            mma(c < 8 ? dL : dR, smem_desc(ab + kk * 32, 16, 1024, SW128),
+                smem_desc(bb + kk * 32, 16, 1024, SW128), idS, (c == 8 ? kk : (c | kk)) != 0);
+          commit(&bars[B_EMPTY + (j % RING)]);
         }
         // the pad chunk carries no data: hand its slot straight back
-        if (!wait_full(base + 9)) return false;
-        mbar_arrive(&bars[B_EMPTY + ((base + 9) % RING)]);
-        mma_commit(&bars[B_S_FULL + buf]);
+        good = wait_full(base + 9) && good;
+        if (!good) return false;
+        if (!WARP_ISSUE || lane == 0) mbar_arrive(&bars[B_EMPTY + ((base + 9) % RING)]);
+        commit(&bars[B_S_FULL + buf]);
         return true;
       };
       auto issue_V = [&](int i) -> bool {
-        if (!mbar_wait(&bars[B_P_FULL], i & 1, abort_flag, WAIT_NS)) return false;
+        if (!wait(&bars[B_P_FULL], i & 1)) return false;
         tc_fence_after();
         const int base = v_base(i, n_tiles);
+        bool good = true;
         for (int m = 0; m < 4; ++m) {
           const int j = base + 2 * m;  // slot j % RING is even, j + 1 is the next slot
-          if (!wait_full(j) || !wait_full(j + 1)) return false;
+          good = wait_full(j) && good;
+          good = wait_full(j + 1) && good;
           const uint32_t ab = ring_base + (j % RING) * CHUNK;
           const uint32_t d = tmem + 4 * N + m * N;
 #pragma unroll
@@ -341,25 +364,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
             const uint64_t ad = smem_desc(ab + kk * 2048, CHUNK, 1024, SW128);
             const uint64_t bd =
                 smem_desc(p_base + (kk >> 2) * N * 128 + (kk & 3) * 32, 16, 1024, SW128);
-            mma_f16(d, ad, bd, idV, (i > 0 || kk > 0) ? 1u : 0u);
+            mma(d, ad, bd, idV, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars[B_EMPTY + (j % RING)]);
-          mma_commit(&bars[B_EMPTY + ((j + 1) % RING)]);
+          commit(&bars[B_EMPTY + (j % RING)]);
+          commit(&bars[B_EMPTY + ((j + 1) % RING)]);
         }
-        mma_commit(&bars[B_O_DONE]);
+        if (!good) return false;
+        commit(&bars[B_O_DONE]);
         return true;
       };
       bool ok = issue_S(0);
       for (int i = 1; ok && i < n_tiles; ++i) ok = issue_S(i) && issue_V(i - 1);
       if (ok) ok = issue_V(n_tiles - 1);
-      if (!ok) {
+      if (!ok && lane == 0) {
         *abort_flag = 1;
         atomicOr(a.err, ERR_TIMEOUT);
       }
-      // drain: every MMA issued above completes before TMEM is released
+      // drain: every MMA issued above completes before TMEM is released (this
+      // wait ignores the abort flag; it is still bounded in time)
       const int zero = 0;
-      mma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+      commit(&bars[B_DRAIN]);
+      (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
     }
     __syncwarp();
   } else if (warp < WARP_CONV) {

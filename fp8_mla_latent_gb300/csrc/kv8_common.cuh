@@ -59,8 +59,11 @@ __device__ __forceinline__ int64_t seq_len_of(const DecodeArgs& a, int b) {
 
 // ---------------------------------------------------------------------------
 // Work items of a decode call.  The tokens of every (sequence, head group) are
-// cut into items of `st` tiles, st = ceil(total tiles x head groups / target),
-// so the items of a ragged batch spread evenly over one wave of CTAs.  Items are
+// cut into items of `st` tiles: st is the smallest item length whose items all
+// fit in one wave of `target` CTAs (so no CTA waits for a second wave behind a
+// long item), and never below ceil(total tiles x head groups / target).  When
+// there are more (sequence, head group) pairs than one wave holds, the items are
+// ceil(total / target) tiles long and spread over several waves.  Items are
 // numbered by sequence, then head group, then position; every kernel of a call
 // derives the same numbering from the sequence lengths, on the device.
 
@@ -73,19 +76,49 @@ __device__ __forceinline__ int64_t tiles_of(const DecodeArgs& a, int b) {
   return (seq_len_of(a, b) + TILE - 1) / TILE;
 }
 
+// Warp-wide (all 32 lanes): number of items if every sequence is cut into
+// pieces of st tiles, times the head groups.
+__device__ __forceinline__ int64_t count_items(const DecodeArgs& a, int64_t st) {
+  const int lane = threadIdx.x & 31;
+  int64_t n = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int64_t t = (b0 + lane < a.B) ? tiles_of(a, b0 + lane) : 0;
+    int64_t c = (t + st - 1) / st;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    n += c;
+  }
+  return n * a.plan.n_hg;
+}
+
 // Warp-wide (all 32 lanes): tiles per item for this call.
 __device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a) {
   const int lane = threadIdx.x & 31;
-  int64_t total = 0;
+  int64_t total = 0, tmax = 0;
   for (int b0 = 0; b0 < a.B; b0 += 32) {
     int64_t t = (b0 + lane < a.B) ? tiles_of(a, b0 + lane) : 0;
+    int64_t m = t;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      t += __shfl_xor_sync(0xffffffffu, t, o);
+      const int64_t mo = __shfl_xor_sync(0xffffffffu, m, o);
+      m = mo > m ? mo : m;
+    }
     total += t;
+    tmax = m > tmax ? m : tmax;
   }
   const int64_t jobs = total * a.plan.n_hg;
-  const int64_t st = (jobs + a.plan.target - 1) / a.plan.target;
-  return st < 1 ? 1 : st;
+  int64_t lo = (jobs + a.plan.target - 1) / a.plan.target;
+  if (lo < 1) lo = 1;
+  if (tmax <= lo || count_items(a, lo) <= a.plan.target) return lo;
+  if (count_items(a, tmax) > a.plan.target) return lo;  // more pairs than one wave holds
+  int64_t hi = tmax;  // invariant: count(lo) > target >= count(hi); count falls as st grows
+  while (lo + 1 < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (count_items(a, mid) <= a.plan.target) hi = mid;
+    else lo = mid;
+  }
+  return hi;
 }
 
 // Warp-wide: walks the sequences 32 at a time with the inclusive scan of their
