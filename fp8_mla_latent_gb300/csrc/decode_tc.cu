@@ -10,36 +10,48 @@
 //   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)
 //
 // One CTA = one work item (sequence, group of N heads, range of tiles); N in
-// {16, 32, 64}.
-// The two contractions of a 128-token tile run on the tensor cores with fp16
-// operands and f32 accumulators in TMEM; the per-row scales stay outside the MMA:
-//   S^T[t][h] = K_t . Q_h      M = 128 tokens, N heads, K = 512 (S_L) and 64 (S_R)
+// {16, 32, 64}.  Both contractions of a 128-token tile run on the tensor cores
+// with f32 accumulators in TMEM; the per-row scales stay outside the MMA:
+//   S^T[t][h] = K_t . Q_h      kind::f16, M = 128 tokens, N heads, K = 512 (S_L)
+//                              and 64 (S_R); K converted from e4m3 to fp16 (exact),
+//                              Q in fp16 with a per-head power-of-two scale
 //   z[t][h]   = c_h (sLc_t S_L + sRc_t S_R)                  (softmax warps)
-//   P'[h][t]  = 2^(z - m_h) * sLc_t / s_ref                   (fp16, K-major in smem)
-//   O^T[d][h] += sum_t V[t][d] P'[h][t]   M = 128 latent rows (x4), N heads, K = 128 tokens
-// The e4m3 codes convert exactly to fp16.  One fp16 chunk of 128 tokens x 64
-// channels (128-byte swizzle, K-major) feeds the score MMA as A, and two such
-// chunks side by side feed the context MMA as an MN-major A operand, so Lc is
-// converted twice per tile (once for each contraction) but never held whole.
+//   P''[h][t] = 2^(z - m_h) (sLc_t / s_ref) P_TOP            (two e4m3 terms hi + lo)
+//   O^T[d][h] += sum_t V[t][d] P''[h][t]   kind::f8f6f4, M = 128 latent rows (x4),
+//                              N heads, K = 128 tokens; V^T is the e4m3 cache tile
+//                              itself (MN-major), loaded by TMA, never converted
+// The fp16 score operand: one chunk of 128 tokens x 64 channels (128-byte
+// swizzle, K-major).  The e4m3 context operand: one d-block of 128 tokens x 128
+// channels (the TMA box, 128-byte swizzle), read as V^T.
 //
-// Warp roles (13 warps):
-//   warp 0      issues every tcgen05.mma (lane 0 alone, or for N = 16 the whole
-//               warp with one elected lane); the warp owns TMEM.
-//   warps 1-8   softmax, two groups of four warps; a thread owns one token row
-//               (its TMEM lane) and half of the heads: tile max per head by a
-//               transposed warp reduction, running denominators per thread, lazy
-//               rescaling of O (only when a head's max grows by more than 2^8).
-//   warps 9-12  converters: warp w converts every 4th 16 KB chunk, alternating
-//               between ring slots w and w+4 (e4m3 -> fp16 by the hardware cvt,
-//               swizzled 16-byte stores), with the loads of its next chunk in
-//               flight while it waits; the bulk-copy engine prefetches tiles into
-//               L2 ahead of them.
-// Chunk stream (converters and MMA in the same order): S(0), S(1), V(0), S(2),
-// V(1), ..., V(n-1).  S(i) = Lc chunks 0..7, the Rc chunk and one empty pad
-// chunk (so every V chunk pair lands on an even slot); V(i) = Lc chunks 0..7.
-// The scores of tile i+1 run on the tensor cores while the softmax of tile i
-// runs on the CUDA cores.  Every wait is bounded (2 s): on a timeout the CTA
-// flags the workspace error word, drains its MMAs, frees TMEM and exits.
+// Warp roles (14 warps):
+//   warp 0       issues the score MMAs of every tile (lane 0 alone, or for N = 16
+//                the whole warp with one elected lane); the warp owns TMEM.
+//   warp 13      loads each tile's four e4m3 d-blocks by TMA (the next tile's
+//                block as soon as this tile's MMAs on it are done), zeroes rows
+//                that hold no data, and issues the context MMAs as soon as the
+//                tile's P'' is written.
+//   warps 1-8    softmax, two groups of four warps; a thread owns one token row
+//                (its TMEM lane) and half of the heads: tile max per head by a
+//                transposed warp reduction, running denominators per thread, lazy
+//                rescaling of O (only the heads whose max grew by more than 2^1),
+//                P'' split into e4m3 hi + lo in f16 arithmetic.
+//   warps 9-12   score converters: the chunks Lc 0..7, Rc of every tile, in order,
+//                into a 4-slot fp16 ring; warp w takes every fourth chunk (16-byte
+//                loads, the next chunk's loads in flight while it waits for its
+//                slot, hardware cvt, swizzled 16-byte stores).  The bulk-copy
+//                engine prefetches tiles into L2 three tiles ahead.
+// The ring has one consumer taking its chunks in order, so the parity waits on
+// a slot are exact.  The scores of tile i+1 run on the tensor cores while the
+// softmax of tile i runs on the CUDA cores.  Every wait is bounded (2 s): on a
+// timeout the CTA flags the workspace error word, drains its MMAs and its TMA
+// loads, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "kv8_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -48,19 +60,24 @@ namespace {
 
 using namespace ptx;
 
-constexpr int RING = 8;                      // fp16 chunk slots, two per converter warp
 constexpr int CHUNK = TILE * 64 * 2;         // 16 KB: 128 rows x 64 fp16
-constexpr int S_CHUNKS = 10;                 // Lc 0..7, Rc, pad
-constexpr int V_CHUNKS = 8;
-constexpr int PERIOD = S_CHUNKS + V_CHUNKS;
-constexpr int NCONV = 4;
+constexpr int VBLK = TILE * 128;             // 16 KB: 128 rows x 128 e4m3 (one d-block of V)
+constexpr int S_RING = 4;                    // score-operand chunk slots
+constexpr int S_PER_TILE = 9;                // Lc channel blocks 0..7, then Rc
 constexpr int NSOFT = 8;
+constexpr int NCONV = 4;
 constexpr int WARP_SOFT = 1;
-constexpr int WARP_CONV = WARP_SOFT + NSOFT;
-constexpr int NTHREADS = (WARP_CONV + NCONV) * 32;
+constexpr int WARP_CONV = WARP_SOFT + NSOFT;  // 9..12
+constexpr int WARP_VMMA = WARP_CONV + NCONV;  // 13: V tile loads and context MMAs
+constexpr int NTHREADS = (WARP_VMMA + 1) * 32;
 constexpr int L2_AHEAD = 3;                  // tiles prefetched into L2 ahead of the converters
-constexpr float TAU = 8.0f;                  // rescale O only if a max grows by > 2^8
-constexpr float TAU_S_POW = 64.0f;           // ... or the scale reference by > 2^6
+// Lazy rescaling thresholds.  The e4m3 weights P'' = 2^(z - m) (sLc / s_ref)
+// P_TOP are at most 2^TAU * TAU_S_POW * P_TOP = 256 <= 448, and with this
+// little headroom the largest weights of a tile sit near the top of the e4m3
+// range, where the two-term split keeps about 8 significant bits.
+constexpr float TAU = 1.0f;                  // rescale O if a head's max grows by > 2^1
+constexpr float TAU_S_POW = 2.0f;            // ... or the scale reference by > 2
+constexpr float P_TOP = 64.0f;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bound on any single wait
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -71,7 +88,8 @@ struct Lay {
   static constexpr int NH = N / 2;                         // heads per softmax group
   static constexpr int Q = 0;                              // 9 chunks [N x 64] fp16
   static constexpr int RINGO = align1k(Q + 9 * N * 128);
-  static constexpr int P = RINGO + RING * CHUNK;           // 2 chunks [N x 64 tokens]
+  static constexpr int VT = RINGO + S_RING * CHUNK;         // e4m3 V tile: 4 d-blocks
+  static constexpr int P = VT + 4 * VBLK;                   // e4m3 P'' hi, lo: [N x 128 tokens] each
   static constexpr int BAR = P + 2 * N * 128;              // 32 mbarriers
   static constexpr int FLAGS = BAR + 32 * 8;               // tmem base, abort, corr flags
   static constexpr int CS = FLAGS + 32;                    // score constant per head
@@ -86,8 +104,8 @@ struct Lay {
 };
 
 // barrier indices
-constexpr int B_FULL = 0, B_EMPTY = 8, B_S_FULL = 16, B_S_EMPTY = 18, B_P_FULL = 20,
-              B_O_DONE = 21, B_G = 22 /* [group][2] */, B_DRAIN = 26;
+constexpr int B_SF = 0, B_SE = 4, B_VT = 8, B_VD = 12, B_S_FULL = 16, B_S_EMPTY = 18, B_P_FULL = 20,
+              B_O_DONE = 21, B_G = 22 /* [group][2] */, B_DRAIN = 26 /* [2] */;
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   uint4 v;
@@ -103,32 +121,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+__device__ __forceinline__ void sts8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Offset of 16-byte unit u of row r in a 128-byte-swizzled K-major tile.
 __device__ __forceinline__ uint32_t sw128(int r, int u) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
-}
-
-// Position of flat chunk j in the stream S(0), S(1), V(0), S(2), V(1), ..., V(n-1).
-struct ChunkInfo {
-  int tile, c;  // c: 0..7 Lc channel block, 8 Rc, 9 pad
-  bool v;
-};
-__device__ __forceinline__ ChunkInfo chunk_info(int j, int n_tiles) {
-  if (j < S_CHUNKS) return {0, j, false};
-  const int jj = j - S_CHUNKS, pair = jj / PERIOD, r = jj % PERIOD;
-  if (pair < n_tiles - 1) {
-    if (r < S_CHUNKS) return {pair + 1, r, false};
-    return {pair, r - S_CHUNKS, true};
-  }
-  return {n_tiles - 1, r, true};
-}
-__device__ __forceinline__ int s_base(int i) { return i == 0 ? 0 : S_CHUNKS + PERIOD * (i - 1); }
-__device__ __forceinline__ int v_base(int i, int n) {
-  return i < n - 1 ? 2 * S_CHUNKS + PERIOD * i : S_CHUNKS + PERIOD * (n - 1);
 }
 
 // Transposed warp reduction of NV <= 32 values per lane: afterwards lane holds
@@ -171,7 +170,8 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[NV], int
 }
 
 template <int N>
-__global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using L = Lay<N>;
   constexpr int NH = L::NH;
   constexpr int LOG2_NH = NH == 8 ? 3 : (NH == 16 ? 4 : 5);
@@ -194,7 +194,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
   const int g_head = s_it.g, b = s_it.b;
   const int64_t t0 = s_it.t0, t_end = s_it.t1;
   const int n_tiles = (int)((t_end - t0 + TILE - 1) / TILE);
-  const int total_chunks = PERIOD * n_tiles;
   const int h0 = g_head * N;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
@@ -211,9 +210,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
 
   // ------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
-    for (int i = 0; i < RING; ++i) {
-      mbar_init(&bars[B_FULL + i], 1);
-      mbar_init(&bars[B_EMPTY + i], 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[B_SF + i], 1);
+      mbar_init(&bars[B_SE + i], 1);
+      mbar_init(&bars[B_VT + i], 1);
+      mbar_init(&bars[B_VD + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_S_FULL + i], 1);
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
     mbar_init(&bars[B_O_DONE], 1);
     for (int i = 0; i < 4; ++i) mbar_init(&bars[B_G + i], NSOFT / 2);
     mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[B_DRAIN + 1], 1);
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) corr_flag[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -289,20 +291,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t ring_base = smem_u32(sm + L::RINGO);
+  const uint32_t sring = smem_u32(sm + L::RINGO);
+  const uint32_t vtile = smem_u32(sm + L::VT);
   const uint32_t p_base = smem_u32(sm + L::P);
   const uint32_t q_base = smem_u32(sm + L::Q);
 
   if (warp == 0) {
-    // ---------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------- score MMAs
     // Narrow head groups (light softmax) issue from the whole converged warp with
-    // elect.sync; wider ones from lane 0 alone, which leaves more issue slots on
-    // this SM sub-partition to the softmax warps that share it (measured both
-    // ways on the workloads of each width).
+    // elect.sync; wider ones from lane 0 alone, which leaves more issue slots to
+    // the softmax warps that share the SM sub-partition (measured both ways on
+    // the workloads of each width).
     constexpr bool WARP_ISSUE = (N <= 16);
     if (WARP_ISSUE || lane == 0) {
       const uint32_t idS = idesc_f16(128, N, false, false);
-      const uint32_t idV = idesc_f16(128, N, true, false);
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait(bar, parity, abort_flag, WAIT_NS);
         if constexpr (WARP_ISSUE) return __all_sync(0xffffffffu, ok);
@@ -316,66 +318,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
         if constexpr (WARP_ISSUE) mma_commit_warp(bar);
         else mma_commit(bar);
       };
-      auto wait_full = [&](int j) -> bool {
-        const bool ok = wait(&bars[B_FULL + (j % RING)], (j / RING) & 1);
-        tc_fence_after();
-        return ok;
-      };
-      // Within a tile the loops run straight through; a failed wait only marks
-      // the tile bad (the abort flag then makes every later wait return at once).
-      auto issue_S = [&](int i) -> bool {
+      // The ring has this one consumer taking its chunks in order, so a parity
+      // wait on a slot is never more than one phase ahead of the slot.  Within a
+      // tile the loop runs straight through; a failed wait only marks the tile
+      // bad (the abort flag then makes every later wait return at once).
+      bool ok = true;
+      for (int i = 0; ok && i < n_tiles; ++i) {
         const int buf = i & 1;
-        if (!wait(&bars[B_S_EMPTY + buf], ((i >> 1) & 1) ^ 1)) return false;
+        if (!wait(&bars[B_S_EMPTY + buf], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dL = tmem + buf * 2 * N, dR = dL + N;
-        const int base = s_base(i);
-        bool good = true;
-        for (int c = 0; c < 9; ++c) {
-          const int j = base + c;
-          good = wait_full(j) && good;
-          const uint32_t ab = ring_base + (j % RING) * CHUNK, bb = q_base + c * N * 128;
+        for (int c = 0; c < S_PER_TILE; ++c) {
+          const int sc = i * S_PER_TILE + c, slot = sc % S_RING;
+          ok = wait(&bars[B_SF + slot], (sc / S_RING) & 1) && ok;
+          tc_fence_after();
+          const uint32_t ab = sring + slot * CHUNK, bb = q_base + c * N * 128;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma(c < 8 ? dL : dR, smem_desc(ab + kk * 32, 16, 1024, SW128),
                 smem_desc(bb + kk * 32, 16, 1024, SW128), idS, (c == 8 ? kk : (c | kk)) != 0);
-          commit(&bars[B_EMPTY + (j % RING)]);
+          commit(&bars[B_SE + slot]);
         }
-        // the pad chunk carries no data: hand its slot straight back
-        good = wait_full(base + 9) && good;
-        if (!good) return false;
-        if (!WARP_ISSUE || lane == 0) mbar_arrive(&bars[B_EMPTY + ((base + 9) % RING)]);
-        commit(&bars[B_S_FULL + buf]);
-        return true;
-      };
-      auto issue_V = [&](int i) -> bool {
-        if (!wait(&bars[B_P_FULL], i & 1)) return false;
-        tc_fence_after();
-        const int base = v_base(i, n_tiles);
-        bool good = true;
-        for (int m = 0; m < 4; ++m) {
-          const int j = base + 2 * m;  // slot j % RING is even, j + 1 is the next slot
-          good = wait_full(j) && good;
-          good = wait_full(j + 1) && good;
-          const uint32_t ab = ring_base + (j % RING) * CHUNK;
-          const uint32_t d = tmem + 4 * N + m * N;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // A = V^T: MN-major, 64-channel atoms CHUNK bytes apart, 8-token groups 1 KB apart
-            const uint64_t ad = smem_desc(ab + kk * 2048, CHUNK, 1024, SW128);
-            const uint64_t bd =
-                smem_desc(p_base + (kk >> 2) * N * 128 + (kk & 3) * 32, 16, 1024, SW128);
-            mma(d, ad, bd, idV, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          commit(&bars[B_EMPTY + (j % RING)]);
-          commit(&bars[B_EMPTY + ((j + 1) % RING)]);
-        }
-        if (!good) return false;
-        commit(&bars[B_O_DONE]);
-        return true;
-      };
-      bool ok = issue_S(0);
-      for (int i = 1; ok && i < n_tiles; ++i) ok = issue_S(i) && issue_V(i - 1);
-      if (ok) ok = issue_V(n_tiles - 1);
+        if (ok) commit(&bars[B_S_FULL + buf]);
+      }
       if (!ok && lane == 0) {
         *abort_flag = 1;
         atomicOr(a.err, ERR_TIMEOUT);
@@ -385,6 +350,97 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       const int zero = 0;
       commit(&bars[B_DRAIN]);
       (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+    }
+    __syncwarp();
+  } else if (warp == WARP_VMMA) {
+    // ---------------------------------------------------------- context MMAs
+    // The e4m3 Lc bytes of a tile come straight from the cache by TMA (128-byte
+    // swizzle), one [128 tokens x 128 channels] d-block per barrier; rows past
+    // the data are zeroed here.  O^T[d][h] += V^T P''^T with A = V^T (MN-major
+    // e4m3) and B = P'' in two e4m3 terms (hi + lo), K = 32 tokens per MMA.  The
+    // next tile's d-block m is requested as soon as this tile's MMAs on it are
+    // done.  The whole warp walks the loop; one elected lane issues.
+    const uint32_t idV = idesc_f16(128, N, true, false);  // e4m3 encodes as format 0
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_NS));
+    };
+    int64_t s0 = -1, s1 = -1;
+    int nv = 0;
+    auto tile_rows = [&](int i) {
+      const int64_t tb = t0 + (int64_t)i * TILE;
+      const int64_t n = t_end - tb;
+      nv = n < TILE ? (int)n : TILE;
+      s0 = slot_of(a, b, tb);
+      s1 = nv > PAGE ? slot_of(a, b, tb + PAGE) : -1;
+    };
+    auto load_block = [&](int m) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[B_VT + m], (s0 >= 0 ? 8192u : 0u) + (s1 >= 0 ? 8192u : 0u));
+        const uint32_t dst = vtile + m * VBLK;
+        if (s0 >= 0) tma_load_2d(dst, &tmap, 128 * m, (int)s0, &bars[B_VT + m]);
+        if (s1 >= 0) tma_load_2d(dst + 8192, &tmap, 128 * m, (int)s1, &bars[B_VT + m]);
+      }
+      __syncwarp();
+    };
+    auto zero_rows = [&](int m, int r0, int r1) {  // rows [r0, r1) of d-block m
+      const uint32_t base = vtile + m * VBLK;
+      for (int u = r0 * 8 + lane; u < r1 * 8; u += 32) sts128(base + u * 16, make_uint4(0u, 0u, 0u, 0u));
+    };
+    bool ok = true;
+    int requested = 1;  // tiles whose four d-blocks have been requested
+    tile_rows(0);
+    for (int m = 0; m < 4; ++m) load_block(m);
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      if (!wait(&bars[B_P_FULL], i & 1)) { ok = false; break; }
+      tc_fence_after();
+      for (int m = 0; m < 4; ++m) {
+        ok = wait(&bars[B_VT + m], i & 1) && ok;
+        if (s0 < 0 || s1 < 0 || nv < TILE) {
+          // rows with no data (past the end, or a page the block table does not map)
+          if (s0 < 0) zero_rows(m, 0, nv < PAGE ? nv : PAGE);
+          if (s1 < 0 && nv > PAGE) zero_rows(m, PAGE, nv);
+          if (nv < TILE) zero_rows(m, nv, TILE);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        const uint32_t vb = vtile + m * VBLK;
+        const uint32_t d = tmem + 4 * N + m * N;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // A = V^T: 128 channels (one swizzle atom) x 32 tokens, 8-token groups 1 KB apart
+          const uint64_t ad = smem_desc(vb + kk * 4096, VBLK, 1024, SW128);
+#pragma unroll
+          for (int term = 0; term < 2; ++term) {
+            const uint64_t bd = smem_desc(p_base + term * N * 128 + kk * 32, 16, 1024, SW128);
+            mma_f8_warp(d, ad, bd, idV, (i > 0 || kk > 0 || term > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit_warp(&bars[B_VD + m]);
+      }
+      if (!ok) break;
+      mma_commit_warp(&bars[B_O_DONE]);
+      if (i + 1 < n_tiles) {
+        tile_rows(i + 1);
+        for (int m = 0; m < 4; ++m) {
+          ok = wait(&bars[B_VD + m], i & 1) && ok;
+          load_block(m);
+        }
+        ++requested;
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(a.err, ERR_TIMEOUT);
+    }
+    const int zero = 0;
+    mma_commit_warp(&bars[B_DRAIN + 1]);
+    (void)mbar_wait(&bars[B_DRAIN + 1], 0, &zero, WAIT_NS);
+    // after an abort the last tile's loads may still be in flight: let them land
+    // (a completed phase passes at once; this wait ignores the abort flag)
+    if (!ok) {
+      for (int m = 0; m < 4; ++m)
+        (void)mbar_wait(&bars[B_VT + m], (requested - 1) & 1, &zero, WAIT_NS);
     }
     __syncwarp();
   } else if (warp < WARP_CONV) {
@@ -401,14 +457,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
     for (int h = 0; h < NH; ++h) lpart[h] = 0.f;
     float sref = 0.f;
     bool ok = true;
-    auto group_sync = [&](int k, int i) -> bool {
+    // group barriers k = 0, 1: each counts its own phases
+    int gph[2] = {0, 0};
+    auto group_sync = [&](int k) -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_G + 2 * grp + k]);
-      return mbar_wait_warp(&bars[B_G + 2 * grp + k], i & 1, abort_flag, WAIT_NS);
+      return mbar_wait_warp(&bars[B_G + 2 * grp + k], (gph[k]++) & 1, abort_flag, WAIT_NS);
     };
-    // P'[h][t] element address (K-major [N x 64] chunks, token chunk = row >> 6)
-    const uint32_t prow = p_base + (row >> 6) * N * 128;
-    const int tcol = row & 63;
+    // byte of P''[h][t] (K-major [N x 128 tokens], 128-byte swizzle): row h,
+    // 16-byte unit t >> 4, byte t & 15; the lo term follows the hi term
+    auto p_addr = [&](int h) -> uint32_t {
+      return p_base + (uint32_t)((h >> 3) * 1024 + (h & 7) * 128 + (((row >> 4) ^ (h & 7)) << 4) +
+                                 (row & 15));
+    };
+    const float4* cs4 = reinterpret_cast<const float4*>(cs + hb);
+    const float4* mu4 = reinterpret_cast<const float4*>(mu_s + hb);
+    const float4* al4 = reinterpret_cast<const float4*>(alpha_s + hb);
     for (int i = 0; i < n_tiles && ok; ++i) {
       const int64_t tok = t0 + (int64_t)i * TILE + row;
       float sL = 0.f, sR = 0.f;
@@ -435,17 +499,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
         tmem_ld8(tmem + lane_addr + buf * 2 * N + hb + c, rl);
         tmem_ld8(tmem + lane_addr + buf * 2 * N + N + hb + c, rr);
         tmem_wait_ld();
+        const float4 c0 = cs4[c / 4], c1 = cs4[c / 4 + 1];
+        const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          z[c + j] = valid ? cs[hb + c + j] * (sL * __uint_as_float(rl[j]) +
-                                               sR * __uint_as_float(rr[j]))
+          z[c + j] = valid ? cc[j] * (sL * __uint_as_float(rl[j]) + sR * __uint_as_float(rr[j]))
                            : -INFINITY;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_S_EMPTY + buf]);
 
-      // tile max per head (and of sLc) over the group's four warps
+      // Tile max per head (and of sLc) over the group's four warps.  The running
+      // max of a head moves (and its O columns are rescaled) only if the tile max
+      // exceeds it by more than 2^TAU, the scale reference only if a scale
+      // exceeds it TAU_S_POW times.
+      bool corr = false;
       {
         const float mx = warp_transpose_reduce<NH, true>(z, lane);
         if ((lane & ((32 >> LOG2_NH) - 1)) == 0)
@@ -454,38 +523,60 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
         if (lane == 0) rs[grp * 4 + wq] = smax;
-      }
-      if (!group_sync(0, i)) { ok = false; break; }
-      const float smax = fmaxf(fmaxf(rs[grp * 4 + 0], rs[grp * 4 + 1]),
-                               fmaxf(rs[grp * 4 + 2], rs[grp * 4 + 3]));
-      const float sref_new = (smax > sref * TAU_S_POW) ? smax : sref;
-      const float beta = (sref_new == sref) ? 1.f : (sref > 0.f ? sref / sref_new : 0.f);
-      if (st == 0) corr_flag[grp * 2 + ((i + 1) & 1)] = 0;  // flag of the next tile
-      if (st < NH) {
-        const int hh = hb + st;
-        const float tmax = fmaxf(fmaxf(rmax[hh], rmax[N + hh]), fmaxf(rmax[2 * N + hh], rmax[3 * N + hh]));
-        float mu = mu_s[hh];
-        const float mn = fmaxf(mu, tmax);
-        float alpha = 1.f;
-        if (mn > mu + TAU) {
-          alpha = (mu == -INFINITY) ? 0.f : ex2_approx(mu - mn);
-          mu = mn;
+        if (st == 0) corr_flag[grp * 2 + buf] = 0;
+        if (!group_sync(0)) { ok = false; break; }
+        const float gmax = fmaxf(fmaxf(rs[grp * 4 + 0], rs[grp * 4 + 1]),
+                                 fmaxf(rs[grp * 4 + 2], rs[grp * 4 + 3]));
+        const float sref_new = (gmax > sref * TAU_S_POW) ? gmax : sref;
+        const float beta = (sref_new == sref) ? 1.f : (sref > 0.f ? sref / sref_new : 0.f);
+        if (st < NH) {
+          const int hh = hb + st;
+          const float tmax =
+              fmaxf(fmaxf(rmax[hh], rmax[N + hh]), fmaxf(rmax[2 * N + hh], rmax[3 * N + hh]));
+          float mu = mu_s[hh];
+          const float mn = fmaxf(mu, tmax);
+          float alpha = 1.f;
+          if (mn > mu + TAU) {
+            alpha = (mu == -INFINITY) ? 0.f : ex2_approx(mu - mn);
+            mu = mn;
+          }
+          mu_s[hh] = mu;
+          alpha_s[hh] = alpha;
+          fcol[hh] = alpha * beta;
+          if (i > 0 && alpha * beta != 1.f) corr_flag[grp * 2 + buf] = 1;
         }
-        mu_s[hh] = mu;
-        alpha_s[hh] = alpha;
-        fcol[hh] = alpha * beta;
-        if (i > 0 && alpha * beta != 1.f) corr_flag[grp * 2 + (i & 1)] = 1;
+        sref = sref_new;
+        if (!group_sync(1)) { ok = false; break; }
+        corr = corr_flag[grp * 2 + buf] != 0;
       }
-      sref = sref_new;
-      if (!group_sync(1, i)) { ok = false; break; }
 
-      // probabilities; running denominators; fp16 P' = p * sLc / s_ref
+      // probabilities; running denominators; P' = p * sLc / s_ref
       const float w = valid ? sL * (sref > 0.f ? 1.0f / sref : 0.f) : 0.f;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float p = (z[h] == -INFINITY) ? 0.f : ex2_approx(z[h] - mu_s[hb + h]);
-        lpart[h] = lpart[h] * alpha_s[hb + h] + p;
-        z[h] = p * w;
+      for (int h = 0; h < NH; h += 4) {
+        const float4 m4 = mu4[h / 4];
+        const float4 a4 = al4[h / 4];
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p = (z[h + j] == -INFINITY) ? 0.f : ex2_approx(z[h + j] - mm[j]);
+          lpart[h + j] = lpart[h + j] * aa[j] + p;
+          z[h + j] = p * w;
+        }
+      }
+      // e4m3 weights P'' = P' * P_TOP as hi + lo on the same scale, computed in
+      // f16 (the residual of the hi term is exact there); bytes packed by head
+      uint32_t phi[NH / 4], plo[NH / 4];
+#pragma unroll
+      for (int h = 0; h < NH; h += 4) {
+        const __half2 x01 = __floats2half2_rn(z[h] * P_TOP, z[h + 1] * P_TOP);
+        const __half2 x23 = __floats2half2_rn(z[h + 2] * P_TOP, z[h + 3] * P_TOP);
+        const uint16_t h01 = f16x2_to_e4m3x2(x01), h23 = f16x2_to_e4m3x2(x23);
+        const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
+        const uint16_t l01 = f16x2_to_e4m3x2(__hsub2(x01, *reinterpret_cast<const __half2*>(&d01)));
+        const uint16_t l23 = f16x2_to_e4m3x2(__hsub2(x23, *reinterpret_cast<const __half2*>(&d23)));
+        phi[h / 4] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+        plo[h / 4] = (uint32_t)l01 | ((uint32_t)l23 << 16);
       }
       if (i > 0) {
         if (!mbar_wait_warp(&bars[B_O_DONE], (i - 1) & 1, abort_flag, WAIT_NS)) {
@@ -493,19 +584,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
           break;
         }
         tc_fence_after();
-        if (corr_flag[grp * 2 + (i & 1)]) {
+        if (corr) {
+          // rescale the O columns of the heads whose factor moved, 8 heads at a
+          // time, the four d-blocks' loads in flight together
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
+          for (int c = 0; c < NH; c += 8) {
+            const float4 f0 = *reinterpret_cast<const float4*>(fcol + hb + c);
+            const float4 f1 = *reinterpret_cast<const float4*>(fcol + hb + c + 4);
+            const float ff[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            bool moved = false;
 #pragma unroll
-            for (int c = 0; c < NH; c += 8) {
-              uint32_t r[8];
-              const uint32_t ad = tmem + lane_addr + 4 * N + m * N + hb + c;
-              tmem_ld8(ad, r);
-              tmem_wait_ld();
+            for (int j = 0; j < 8; ++j) moved |= (ff[j] != 1.f);
+            if (!moved) continue;  // the same for every thread of the group
+            uint32_t r[4][8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                r[j] = __float_as_uint(__uint_as_float(r[j]) * fcol[hb + c + j]);
-              tmem_st8(ad, r);
+            for (int m = 0; m < 4; ++m) tmem_ld8(tmem + lane_addr + 4 * N + m * N + hb + c, r[m]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) r[m][j] = __float_as_uint(__uint_as_float(r[m][j]) * ff[j]);
+              tmem_st8(tmem + lane_addr + 4 * N + m * N + hb + c, r[m]);
             }
           }
           tmem_wait_st();
@@ -513,8 +612,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       }
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const int hr = hb + h;
-        sts16(prow + sw128(hr, tcol >> 3) + (tcol & 7) * 2, __half_as_ushort(__float2half_rn(z[h])));
+        const uint32_t ad = p_addr(hb + h);
+        sts8(ad, phi[h / 4] >> (8 * (h & 3)));
+        sts8(ad + N * 128, plo[h / 4] >> (8 * (h & 3)));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -531,13 +631,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
         if ((lane & ((32 >> LOG2_NH) - 1)) == 0)
           rmax[wq * N + hb + (lane >> (5 - LOG2_NH))] = ls;
       }
-      if (group_sync(0, n_tiles)) {
+      if (group_sync(0)) {
         if (st < NH) {
           const int hh = hb + st;
           lfin[hh] = (rmax[hh] + rmax[N + hh]) + (rmax[2 * N + hh] + rmax[3 * N + hh]);
         }
-        if (group_sync(1, n_tiles)) {
-          // epilogue: unnormalised partial o = acc * s_ref, with (m, l) per head
+        if (group_sync(1)) {
+          // epilogue: unnormalised partial o = acc * s_ref / P_TOP, with (m, l) per head
+          const float oscale = sref * (1.0f / P_TOP);
           tc_fence_after();
           const int64_t base = (int64_t)blockIdx.x * N;  // this item's partials
 #pragma unroll 1
@@ -551,7 +652,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
               for (int j = 0; j < 8; ++j) {
                 const int h = hb + c + j;
                 if (h0 + h < a.H)
-                  a.ws_o[(base + h) * DL + m * 128 + row] = __uint_as_float(r[j]) * sref;
+                  a.ws_o[(base + h) * DL + m * 128 + row] = __uint_as_float(r[j]) * oscale;
               }
             }
           }
@@ -575,11 +676,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
     }
   } else {
     // ---------------------------------------------------------- converters
-    // Warp cw converts chunks j = cw, cw + 4, ... into ring slot j % 8.  Lane l
-    // handles rows 8i + (l >> 2) (i = 0..15) and 16-byte piece (l & 3) of the
-    // chunk's 64 bytes per row; rows 0..63 are the tile's first page, 64..127 its
-    // second.
+    // The converters fill the score ring with the fp16 chunks of every tile in
+    // order (Lc blocks 0..7, then Rc); converter w takes every NCONV-th chunk.
+    // Lane l handles rows 8i + (l >> 2) (i = 0..15) and 16-byte piece (l & 3) of
+    // the chunk's 64 bytes per row; rows 0..63 are the tile's first page,
+    // 64..127 its second.
+    constexpr bool score_side = true;
     const int cw = warp - WARP_CONV;
+    constexpr int nconv = NCONV;
+    constexpr int per_tile = S_PER_TILE;
+    constexpr int ring = S_RING;
+    const uint32_t ring_base = sring;
+    uint64_t* full = &bars[B_SF];
+    uint64_t* empty = &bars[B_SE];
+    const int total = per_tile * n_tiles;
     const int rin = lane >> 2, sub = lane & 3;
     int ctile[2] = {-1, -1};
     const uint8_t* cpg[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
@@ -603,14 +713,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       ctile[0] = tile; cpg[0][0] = q[0]; cpg[0][1] = q[1]; cvalid[0] = (int)nv;
       p0 = q[0]; p1 = q[1]; nvalid = (int)nv;
     };
+    auto prefetch_tile = [&](int tile) {
+      const int64_t tb = t0 + (int64_t)tile * TILE;
+      for (int pg = 0; pg < 2; ++pg) {
+        const int64_t tk = tb + pg * PAGE;
+        if (tk >= t_end) break;
+        const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
+        const int64_t slot = slot_of(a, b, tk);
+        if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
+      }
+    };
     uint4 dat[16];
     auto load = [&](int j) {
-      const ChunkInfo ci = chunk_info(j, n_tiles);
-      if (ci.c == 9) return;  // pad chunk
+      const int tile = j / per_tile, c = j % per_tile;
       const uint8_t *p0, *p1;
       int nv;
-      pages_of(ci.tile, p0, p1, nv);
-      const int off = ci.c * 64 + sub * 16;  // c == 8 is the Rc block: channels 512..575
+      pages_of(tile, p0, p1, nv);
+      const int off = c * 64 + sub * 16;  // c == 8 is the Rc block: channels 512..575
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = 8 * i + rin;
@@ -620,56 +739,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
       }
     };
     bool ok = true;
-    if (cw == 0 && lane == 0) {
+    if (score_side && cw == 0 && lane == 0) {
       // the first tiles' lines: ask the bulk-copy engine for them up front
-      for (int tl = 0; tl < L2_AHEAD && tl < n_tiles; ++tl) {
-        for (int pg = 0; pg < 2; ++pg) {
-          const int64_t tk = t0 + (int64_t)tl * TILE + pg * PAGE;
-          if (tk >= t_end) break;
-          const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
-          const int64_t slot = slot_of(a, b, tk);
-          if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
-        }
-      }
+      for (int tl = 0; tl < L2_AHEAD && tl < n_tiles; ++tl) prefetch_tile(tl);
     }
-    if (cw < total_chunks) load(cw);
-    for (int j = cw; j < total_chunks && ok; j += NCONV) {
-      const ChunkInfo ci = chunk_info(j, n_tiles);
-      const int slot = j % RING;
+    if (cw < total) load(cw);
+    for (int j = cw; j < total && ok; j += nconv) {
+      const int slot = j % ring;
       const uint32_t slot_addr = ring_base + slot * CHUNK;
-      if (!mbar_wait_warp(&bars[B_EMPTY + slot], ((j / RING) & 1) ^ 1, abort_flag, WAIT_NS)) {
+      if (!mbar_wait_warp(&empty[slot], ((j / ring) & 1) ^ 1, abort_flag, WAIT_NS)) {
         ok = false;
         break;
       }
-      if (ci.c != 9) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = 8 * i + rin;
-          const uint4 x = dat[i];
-          uint32_t h[8];
-          h[0] = e4m3x2_to_f16x2((uint16_t)(x.x & 0xFFFFu)); h[1] = e4m3x2_to_f16x2((uint16_t)(x.x >> 16));
-          h[2] = e4m3x2_to_f16x2((uint16_t)(x.y & 0xFFFFu)); h[3] = e4m3x2_to_f16x2((uint16_t)(x.y >> 16));
-          h[4] = e4m3x2_to_f16x2((uint16_t)(x.z & 0xFFFFu)); h[5] = e4m3x2_to_f16x2((uint16_t)(x.z >> 16));
-          h[6] = e4m3x2_to_f16x2((uint16_t)(x.w & 0xFFFFu)); h[7] = e4m3x2_to_f16x2((uint16_t)(x.w >> 16));
-          sts128(slot_addr + sw128(r, 2 * sub), make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(slot_addr + sw128(r, 2 * sub + 1), make_uint4(h[4], h[5], h[6], h[7]));
-        }
-        fence_proxy_async_smem();
+      for (int i = 0; i < 16; ++i) {
+        const int r = 8 * i + rin;
+        const uint4 x = dat[i];
+        uint32_t h[8];
+        h[0] = e4m3x2_to_f16x2((uint16_t)(x.x & 0xFFFFu)); h[1] = e4m3x2_to_f16x2((uint16_t)(x.x >> 16));
+        h[2] = e4m3x2_to_f16x2((uint16_t)(x.y & 0xFFFFu)); h[3] = e4m3x2_to_f16x2((uint16_t)(x.y >> 16));
+        h[4] = e4m3x2_to_f16x2((uint16_t)(x.z & 0xFFFFu)); h[5] = e4m3x2_to_f16x2((uint16_t)(x.z >> 16));
+        h[6] = e4m3x2_to_f16x2((uint16_t)(x.w & 0xFFFFu)); h[7] = e4m3x2_to_f16x2((uint16_t)(x.w >> 16));
+        sts128(slot_addr + sw128(r, 2 * sub), make_uint4(h[0], h[1], h[2], h[3]));
+        sts128(slot_addr + sw128(r, 2 * sub + 1), make_uint4(h[4], h[5], h[6], h[7]));
       }
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_FULL + slot]);
-      if (j + NCONV < total_chunks) load(j + NCONV);
-      // L2 prefetch of the tile L2_AHEAD tiles ahead, by whoever converts its S(i) chunk 0
-      if (lane == 0 && !ci.v && ci.c == 0 && ci.tile + L2_AHEAD < n_tiles) {
-        const int64_t tb = t0 + (int64_t)(ci.tile + L2_AHEAD) * TILE;
-        for (int pg = 0; pg < 2; ++pg) {
-          const int64_t tk = tb + pg * PAGE;
-          if (tk >= t_end) break;
-          const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
-          const int64_t slot = slot_of(a, b, tk);
-          if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
-        }
-      }
+      if (lane == 0) mbar_arrive(&full[slot]);
+      if (j + nconv < total) load(j + nconv);
+      // L2 prefetch of the tile L2_AHEAD tiles ahead, when its score chunk 0 is converted
+      const int tile = j / per_tile;
+      if (score_side && lane == 0 && j % per_tile == 0 && tile + L2_AHEAD < n_tiles)
+        prefetch_tile(tile + L2_AHEAD);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -684,6 +785,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_tc_kernel(const DecodeArgs
   if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
+// Tensor map of the e4m3 cache for the V tile loads: rows of 576 bytes, boxes
+// of 64 rows (one page) x 128 bytes (one d-block), 128-byte swizzle.  Rows past
+// the end of the map read as zeros.
+cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
+  if (rows < 1 || a.codes == nullptr) {
+    // no cache rows: no tile is ever loaded, the map is never read
+    memset(map, 0, sizeof(*map));
+    return cudaSuccess;
+  }
+  if (rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D};
+  const cuuint32_t box[2] = {128, PAGE};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.codes), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int N>
 cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
   const int smem = Lay<N>::TOTAL + 1024;
@@ -694,7 +828,10 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, smem, s>>>(a);
+  CUtensorMap map;
+  const cudaError_t e = make_cache_map(a, &map);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, smem, s>>>(a, map);
   return cudaGetLastError();
 }
 

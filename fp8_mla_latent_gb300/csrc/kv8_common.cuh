@@ -33,6 +33,14 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float e0, float e1) {
   return r;
 }
 
+// f16x2 -> two e4m3 bytes (the low half lands in the low byte), round to
+// nearest even, finite results saturate at +-448.
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(__half2 v) {
+  uint16_t r;
+  asm("{ cvt.rn.satfinite.e4m3x2.f16x2 %0, %1; }" : "=h"(r) : "r"(*reinterpret_cast<const uint32_t*>(&v)));
+  return r;
+}
+
 // Page-table lookup: cache slot of token t of sequence b, or -1 if the block
 // table entry is out of range (the error word records it).
 __device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int64_t t) {

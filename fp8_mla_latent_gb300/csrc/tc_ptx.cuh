@@ -190,6 +190,40 @@ __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
       : "memory");
 }
 
+// kind::f8f6f4 MMA (A and B e4m3; the instruction descriptor encodes e4m3 as
+// format 0 for both, so idesc_f16 builds it too), issued by a whole converged
+// warp through elect.sync.  K = 32 per instruction.
+__device__ __forceinline__ void mma_f8_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// Arrive on `bar` and raise its expected transaction count by `bytes`.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 2-D tiled bulk tensor load global -> shared; completes `bytes` of tx on `bar`.
+// x (innermost, in elements of the map) must keep x * element size a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2^x on the SFU (max relative error ~2^-22; results below 2^-126 flush to 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

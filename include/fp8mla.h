@@ -55,11 +55,13 @@ typedef enum {
 /* Decode kernel choice.  Both accumulate in f32.  Tolerance classes, as max-abs
  * error against the exact attention of the stored cache:
  *   SIMT     f32 operands:                      <= 2e-3 * max|out|
- *   TCGEN05  16-bit MMA operands (the query and the softmax weights rounded to
- *            fp16; the cache's e4m3 values convert to fp16 exactly):
+ *   TCGEN05  reduced-precision MMA operands: the query rounded to fp16 for the
+ *            scores (the cache's e4m3 values convert to fp16 exactly), and the
+ *            softmax weights as two e4m3 terms (about 8 significant bits) for the
+ *            context, which reads the e4m3 cache values as they are:
  *                                               <= 1e-2 * max|out|
- * (the tensor-core kernel measures about 2e-3 on outlier-heavy caches and
- * below 1e-3 on plain ones; its error is dominated by the fp16 query).         */
+ * (the tensor-core kernel's error is dominated by the fp16 query; see the test
+ * report for the measured worst case).                                         */
 typedef enum {
     KV8_DECODE_AUTO = 0,     /* tcgen05 when H >= 16, else SIMT                   */
     KV8_DECODE_SIMT = 1,     /* CUDA-core split-T kernel, any H >= 1              */

@@ -11,8 +11,8 @@ import oracle
 
 # max-abs error <= TOL * max|out| per sequence against the f64 oracle on the same codes:
 #   CUDA-core kernel (f32 operands and accumulation): 2e-3;
-#   tensor-core kernel (16-bit MMA operands: q and the softmax weights rounded to fp16,
-#   f32 accumulation): 1e-2, the class the decode tolerance sets for 16-bit operands.
+#   tensor-core kernel (reduced-precision MMA operands: q rounded to fp16 for the scores,
+#   the softmax weights as two e4m3 terms for the context; f32 accumulation): 1e-2.
 TOLS = {1: 2e-3, 2: 1e-2}
 LSE_TOL = 2e-3   # natural-log units
 WORST = {}       # variant -> worst observed err / max|out|, reported by the tests
@@ -48,7 +48,8 @@ def decode(w, codes, scales, variant, lse=True, contiguous=None):
         out = pkg.mla_absorb_decode_fp8(ql[0], qr[0], codes, scales, T, w.sm_scale, lse=l,
                                         workspace=ws, variant=variant)
         torch.cuda.synchronize()
-        assert pkg.kv8_workspace_error(ws) == 0
+        err = pkg.kv8_workspace_error(ws)
+        assert err == 0, f"workspace error status {err}"
         return out[None].cpu().numpy(), (l[None].cpu().numpy() if lse else None)
     bt = torch.from_numpy(w.block_table).to(d)
     sl = torch.from_numpy(w.seq_lens).to(d)
@@ -58,7 +59,8 @@ def decode(w, codes, scales, variant, lse=True, contiguous=None):
     out = pkg.mla_absorb_decode_fp8_batch(ql, qr, codes, scales, bt, sl, w.sm_scale, lse=l,
                                           workspace=ws, variant=variant)
     torch.cuda.synchronize()
-    assert pkg.kv8_workspace_error(ws) == 0
+    err = pkg.kv8_workspace_error(ws)
+    assert err == 0, f"workspace error status {err}"
     return out.cpu().numpy(), (l.cpu().numpy() if lse else None)
 
 
