@@ -103,9 +103,18 @@ struct Lay {
   static constexpr int TMEM_COLS = (8 * N <= 128) ? 128 : (8 * N <= 256 ? 256 : 512);
 };
 
-// barrier indices
-constexpr int B_SF = 0, B_SE = 4, B_VT = 8, B_VD = 12, B_S_FULL = 16, B_S_EMPTY = 18, B_P_FULL = 20,
-              B_O_DONE = 21, B_G = 22 /* [group][2] */, B_DRAIN = 26 /* [2] */;
+// barrier indices (the layout follows the ring size; 32 barriers are allocated)
+constexpr int B_SF = 0;                      // [S_RING] score chunk converted
+constexpr int B_SE = B_SF + S_RING;          // [S_RING] score chunk consumed
+constexpr int B_VT = B_SE + S_RING;          // [4] e4m3 d-block loaded (TMA transactions)
+constexpr int B_VD = B_VT + 4;               // [4] context MMAs on a d-block done
+constexpr int B_S_FULL = B_VD + 4;           // [2] scores of a tile in TMEM
+constexpr int B_S_EMPTY = B_S_FULL + 2;      // [2] scores read by the softmax
+constexpr int B_P_FULL = B_S_EMPTY + 2;      // P'' of a tile written
+constexpr int B_O_DONE = B_P_FULL + 1;       // context MMAs of a tile done
+constexpr int B_G = B_O_DONE + 1;            // [group][2] softmax group barriers
+constexpr int B_DRAIN = B_G + 4;             // [2] issuers' final drains
+static_assert(B_DRAIN + 2 <= 32, "barrier layout exceeds the 32 barriers allocated");
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   uint4 v;
@@ -210,9 +219,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < S_RING; ++i) {
       mbar_init(&bars[B_SF + i], 1);
       mbar_init(&bars[B_SE + i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[B_VT + i], 1);
       mbar_init(&bars[B_VD + i], 1);
     }
