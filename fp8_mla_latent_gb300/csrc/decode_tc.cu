@@ -503,6 +503,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
+      // u = sLc S_L + sRc S_R; the score in log2 units is z = c_h u with c_h >= 0,
+      // so the tile max is taken on u and c_h is applied inside the exponent
       float z[NH];
 #pragma unroll
       for (int c = 0; c < NH; c += 8) {
@@ -510,11 +512,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld8(tmem + lane_addr + buf * 2 * N + hb + c, rl);
         tmem_ld8(tmem + lane_addr + buf * 2 * N + N + hb + c, rr);
         tmem_wait_ld();
-        const float4 c0 = cs4[c / 4], c1 = cs4[c / 4 + 1];
-        const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          z[c + j] = valid ? cc[j] * (sL * __uint_as_float(rl[j]) + sR * __uint_as_float(rr[j]))
+          z[c + j] = valid ? fmaf(sR, __uint_as_float(rr[j]), sL * __uint_as_float(rl[j]))
                            : -INFINITY;
       }
       tc_fence_before();
@@ -542,8 +542,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float beta = (sref_new == sref) ? 1.f : (sref > 0.f ? sref / sref_new : 0.f);
         if (st < NH) {
           const int hh = hb + st;
-          const float tmax =
+          const float umax =
               fmaxf(fmaxf(rmax[hh], rmax[N + hh]), fmaxf(rmax[2 * N + hh], rmax[3 * N + hh]));
+          const float tmax = (cs[hh] > 0.f) ? cs[hh] * umax : -INFINITY;
           float mu = mu_s[hh];
           const float mn = fmaxf(mu, tmax);
           float alpha = 1.f;
@@ -561,27 +562,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         corr = corr_flag[grp * 2 + buf] != 0;
       }
 
-      // probabilities; running denominators; P' = p * sLc / s_ref
-      const float w = valid ? sL * (sref > 0.f ? 1.0f / sref : 0.f) : 0.f;
+      // probabilities; running denominators; P'' = p * (sLc / s_ref) * P_TOP
+      // (a running max still at -inf is floored so that an empty row gives 2^-inf = 0)
+      const float w = valid ? sL * (sref > 0.f ? P_TOP / sref : 0.f) : 0.f;
 #pragma unroll
       for (int h = 0; h < NH; h += 4) {
         const float4 m4 = mu4[h / 4];
         const float4 a4 = al4[h / 4];
+        const float4 c4 = cs4[h / 4];
         const float mm[4] = {m4.x, m4.y, m4.z, m4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float p = (z[h + j] == -INFINITY) ? 0.f : ex2_approx(z[h + j] - mm[j]);
-          lpart[h + j] = lpart[h + j] * aa[j] + p;
+          const float p = ex2_approx(fmaf(cc[j], z[h + j], -fmaxf(mm[j], -3.0e38f)));
+          lpart[h + j] = fmaf(lpart[h + j], aa[j], p);
           z[h + j] = p * w;
         }
       }
-      // e4m3 weights P'' = P' * P_TOP as hi + lo on the same scale, computed in
+      // e4m3 weights P'' as hi + lo on the same scale, computed in
       // f16 (the residual of the hi term is exact there); bytes packed by head
       uint32_t phi[NH / 4], plo[NH / 4];
 #pragma unroll
       for (int h = 0; h < NH; h += 4) {
-        const __half2 x01 = __floats2half2_rn(z[h] * P_TOP, z[h + 1] * P_TOP);
-        const __half2 x23 = __floats2half2_rn(z[h + 2] * P_TOP, z[h + 3] * P_TOP);
+        const __half2 x01 = __floats2half2_rn(z[h], z[h + 1]);
+        const __half2 x23 = __floats2half2_rn(z[h + 2], z[h + 3]);
         const uint16_t h01 = f16x2_to_e4m3x2(x01), h23 = f16x2_to_e4m3x2(x23);
         const uint32_t d01 = e4m3x2_to_f16x2(h01), d23 = e4m3x2_to_f16x2(h23);
         const uint16_t l01 = f16x2_to_e4m3x2(__hsub2(x01, *reinterpret_cast<const __half2*>(&d01)));
