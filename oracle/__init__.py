@@ -75,6 +75,9 @@ def lib():
                 "orc_attention_batch_f32": (None, [P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P,
                                                    i32]),
                 "orc_max_threads": (i32, []),
+                "orc_rmsnorm_row": (None, [P, P, f32, P]),
+                "orc_rope_pairs": (None, [P, P, P, P]),
+                "orc_produce_rows": (None, [P, i64, i64, P, f32, P, P, P, i64, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -120,6 +123,48 @@ def list_mismatches_nearest(bits):
     first = ctypes.c_uint32(0)
     n = lib().orc_e4m3_list_mismatches_nearest(_p(bits), bits.size, ctypes.byref(first))
     return int(n), int(first.value)
+
+
+# ---------------------------------------------------------------- fused producer
+def rmsnorm_row(x, weight, eps: float) -> np.ndarray:
+    """RMS norm of the 512 Lc values of one row (fixed f32 order; see kv8_oracle.h)."""
+    x = _c(x, np.float32)
+    w = _c(weight, np.float32)
+    y = np.empty(DL, np.float32)
+    lib().orc_rmsnorm_row(_p(x), _p(w), float(eps), _p(y))
+    return y
+
+
+def rope_pairs(x, cos_row, sin_row) -> np.ndarray:
+    """Rotation of the 32 Rc pairs (x[2j], x[2j+1]) by tabulated cos/sin."""
+    x = _c(x, np.float32)
+    y = np.empty(DR, np.float32)
+    lib().orc_rope_pairs(_p(x), _p(_c(cos_row, np.float32)), _p(_c(sin_row, np.float32)), _p(y))
+    return y
+
+
+def produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, dst_slot=None,
+                 n_slots=None, codes=None, scales=None):
+    """Fused producer: RMS norm (Lc) + rotary pairs (Rc) + quantize, into cache slots."""
+    src = np.asarray(src, dtype=np.float32)
+    assert src.ndim == 2 and src.shape[1] >= D and src.strides[1] == 4
+    n = src.shape[0]
+    stride = src.strides[0] // 4
+    rope_cos = _c(rope_cos, np.float32)
+    rope_sin = _c(rope_sin, np.float32)
+    assert rope_cos.shape == rope_sin.shape and rope_cos.shape[1] == DR // 2
+    if n_slots is None:
+        n_slots = n if dst_slot is None else int(np.max(dst_slot)) + 1 if n else 0
+    if codes is None:
+        codes = np.zeros((n_slots, D), np.uint8)
+    if scales is None:
+        scales = np.zeros((n_slots, 2), np.float32)
+    slots = None if dst_slot is None else _c(dst_slot, np.int64)
+    lib().orc_produce_rows(src.ctypes.data_as(ctypes.c_void_p), n, stride,
+                           _p(_c(norm_weight, np.float32)), float(eps),
+                           _p(_c(positions, np.int64)), _p(rope_cos), _p(rope_sin),
+                           rope_cos.shape[0], _p(slots), _p(codes), _p(scales))
+    return codes, scales
 
 
 # ---------------------------------------------------------------- quantizer

@@ -218,6 +218,69 @@ void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Fused producer.  KV8 page, PR description, attention_rows item: the producer
+ * quantizes "the fresh normed/roped row".  The page names the steps but not
+ * their formulas; the readings (RMS norm with a weight over Lc, rotation of the
+ * pairs (2j, 2j+1) of Rc by tabulated angles) and the fixed f32 order are in
+ * kv8_oracle.h.  Each f32 operation goes through a volatile, so it is rounded
+ * once, in the order written.                                                  */
+void orc_rmsnorm_row(const float* x, const float* weight, float eps, float* y) {
+    float p[32];
+    for (int l = 0; l < 32; ++l) {
+        volatile float acc = 0.0f;
+        for (int k = 0; k < 16; ++k) {
+            volatile float sq = x[16 * l + k] * x[16 * l + k];
+            acc = acc + sq;
+        }
+        p[l] = acc;
+    }
+    for (int o = 16; o >= 1; o >>= 1) {
+        float q[32];
+        for (int l = 0; l < 32; ++l) {
+            volatile float t = p[l] + p[l ^ o];
+            q[l] = t;
+        }
+        for (int l = 0; l < 32; ++l) p[l] = q[l];
+    }
+    volatile float ms = p[0] * (1.0f / 512.0f);   /* exact: a power of two */
+    volatile float t = ms + eps;
+    volatile float r = sqrtf(t);
+    volatile float inv = 1.0f / r;
+    for (int i = 0; i < ORC_DL; ++i) {
+        volatile float a = x[i] * inv;
+        volatile float b = a * weight[i];
+        y[i] = b;
+    }
+}
+
+void orc_rope_pairs(const float* x, const float* cos_row, const float* sin_row, float* y) {
+    for (int j = 0; j < ORC_DR / 2; ++j) {
+        const float x0 = x[2 * j], x1 = x[2 * j + 1], c = cos_row[j], s = sin_row[j];
+        volatile float a = x0 * c, b = x1 * s, d = x0 * s, e = x1 * c;
+        volatile float y0 = a - b, y1 = d + e;
+        y[2 * j] = y0;
+        y[2 * j + 1] = y1;
+    }
+}
+
+void orc_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                      const float* norm_weight, float eps, const int64_t* positions,
+                      const float* rope_cos, const float* rope_sin, int64_t max_pos,
+                      const int64_t* dst_slot, uint8_t* codes, float* scales) {
+    float y[ORC_D];
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t pos = positions[r];
+        if (pos < 0 || pos >= max_pos) continue;
+        const float* x = src + r * src_row_stride;
+        orc_rmsnorm_row(x, norm_weight, eps, y);
+        orc_rope_pairs(x + ORC_DL, rope_cos + pos * (ORC_DR / 2), rope_sin + pos * (ORC_DR / 2),
+                       y + ORC_DL);
+        const int64_t slot = dst_slot ? dst_slot[r] : r;
+        orc_quantize_row(y, codes + slot * ORC_D, scales + slot * 2);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Absorbed decode attention.  KV8 page, PR description, opening paragraph:
  * "the latent is both key and value in the absorbed attention"; attention_rows
  * item: the absorb "score/context loops LUT-dequant inline with the scale

@@ -48,6 +48,26 @@ void orc_quantize_row(const float* x, uint8_t* codes, float* scales);
 void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
                        const int64_t* dst_slot, uint8_t* codes, float* scales);
 
+/* ---- fused producer (KV8 page, PR description, attention_rows item: the
+ * producer quantizes "the fresh normed/roped row" instead of an f32 copy) ----
+ * Our reading of the steps the page names but does not spell out:
+ *   Lc: RMS norm with a weight, y_i = (x_i * inv) * w_i, inv = 1 / sqrt(ss/512 + eps);
+ *   Rc: rotary embedding of the 32 pairs (x[2j], x[2j+1]) by the angle whose
+ *       cosine and sine the caller tabulates per position (rope_cos/sin[pos][32]):
+ *       y0 = x0*c - x1*s,  y1 = x0*s + x1*c;
+ *   then the per-row quantizer above, into dst_slot[r].
+ * Every f32 operation is rounded once (no FMA).  The sum of squares ss has a
+ * fixed order, the one a 32-lane warp reduction takes: 32 partial sums p_l of
+ * x[16l .. 16l+15] in index order, then for o = 16, 8, 4, 2, 1 every p_l becomes
+ * p_l + p_(l xor o); ss = p_0.  Rows whose position is outside [0, max_pos) are
+ * skipped (their slots are left as they were).                                  */
+void orc_rmsnorm_row(const float* x, const float* weight, float eps, float* y);
+void orc_rope_pairs(const float* x, const float* cos_row, const float* sin_row, float* y);
+void orc_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                      const float* norm_weight, float eps, const int64_t* positions,
+                      const float* rope_cos, const float* rope_sin, int64_t max_pos,
+                      const int64_t* dst_slot, uint8_t* codes, float* scales);
+
 /* ---- absorbed decode attention (KV8 page, attention_rows item) ----
  * One query (all H heads) against the rows of one sequence.  slot_of_token[t]
  * gives the cache slot of token t (NULL means slot == t).
