@@ -7,7 +7,7 @@ kv_lora 512 + qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token,
 One step = one decode query per sequence over its whole cache (the "append"
 workload also quantizes 65536 fresh rows into the cache inside the step).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce]
                     [--variant auto|simt|tcgen05] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  `value` = KV GB/s over all ranks (KV bytes the
@@ -312,6 +312,115 @@ def run_ours(args, rank, world, local_rank):
     return res, w
 
 
+PRODUCE_METRIC = "fp8-latent fused producer (RMS norm + rotary + e4m3 quantize + paged write): GB/s"
+PRODUCE_ROW_BYTES = 2304 + 8 + 8 + 576 + 8   # f32 row, position, slot in; codes, scales out
+
+
+def run_produce(args, rank, world, local_rank):
+    """The fused producer step of the append workload: 65536 raw rows -> cache slots."""
+    import torch
+    import fp8_mla_latent_gb300 as pkg
+    from fp8_mla_latent_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    n = max(1, int(65536 * args.scale))
+    p = workloads.producer_inputs(n)
+    rows = torch.from_numpy(p.rows).to(dev)
+    weight = torch.from_numpy(p.weight).to(dev)
+    pos = torch.from_numpy(p.positions).to(dev)
+    cos = torch.from_numpy(p.rope_cos).to(dev)
+    sin = torch.from_numpy(p.rope_sin).to(dev)
+    slots = torch.from_numpy(p.slots).to(dev)
+    codes = torch.zeros((p.n_slots, 576), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((p.n_slots, 2), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def once():
+        pkg.kv8_produce_rows(rows, weight, p.eps, pos, cos, sin, codes, scales, dst_slot=slots,
+                             err_word=err)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        once()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        once()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+    ms = float(np.mean(times))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    nbytes = n * PRODUCE_ROW_BYTES
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    # end to end: raw rows from pinned host memory, error word back
+    host_rows = torch.from_numpy(p.rows).pin_memory()
+    host_err = torch.zeros(1, dtype=torch.int32).pin_memory()
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rows.copy_(host_rows, non_blocking=True)
+        once()
+        host_err.copy_(err, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.mean(e2e))
+    peaks = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    res = {
+        "metric": PRODUCE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 in, e4m3 + f32 scales out",
+        "data": "synthetic (seeded; append-workload value mix, see DESIGN.md)",
+        "rows_per_s": world * n / (ms * 1e-3),
+        "config": {"workload": "produce", "rows": n, "max_pos": int(p.rope_cos.shape[0]),
+                   "l2": "flushed between steps (256 MB write); rows > L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "produce_rows", "ms_per_launch": ms,
+                     "peak_note": f"{peaks['src']} copy",
+                     "algorithmic": {"bytes": nbytes, "per_unit": f"{PRODUCE_ROW_BYTES} B per row"}},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": n * 2304, "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks if clocks else {"note": "timed region shorter than the 50 ms sampling period"},
+    }
+    return res, p
+
+
+def produce_cpu_baseline(p, budget_s=8.0):
+    import oracle
+    n = p.rows.shape[0]
+    t0 = time.time()
+    done = 0
+    while time.time() - t0 < budget_s and done < 4 * n:
+        oracle.produce_rows(p.rows, p.weight, p.eps, p.positions, p.rope_cos, p.rope_sin,
+                            dst_slot=p.slots, n_slots=p.n_slots)
+        done += n
+    dt = time.time() - t0
+    return {"value": done * PRODUCE_ROW_BYTES / dt / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{done} rows of the producer workload, plain C, {dt:.2f} s wall"}
+
+
 def tc_built(pkg, dev):
     import torch
     try:
@@ -365,6 +474,22 @@ def oracle_sample(w, budget_s, codes=None, scales=None):
 def run_reference(args, world):
     from fp8_mla_latent_gb300 import workloads
     import oracle
+    if args.workload == "produce":
+        p = workloads.producer_inputs(max(1, int(65536 * args.scale)))
+        for _ in range(args.warmup):
+            produce_cpu_baseline(p, 0.1)
+        vals = [produce_cpu_baseline(p, 1.0) for _ in range(args.steps)]
+        value = float(np.mean([v["value"] for v in vals]))
+        return {
+            "impl": "reference", "metric": PRODUCE_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": p.rows.shape[0] * PRODUCE_ROW_BYTES / (value * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; same rows as our arm)",
+            "config": {"workload": "produce", "rows": int(p.rows.shape[0])},
+            "cpu_baseline": dict(vals[-1], value=value),
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     w = workloads.make(args.workload)
     cache = None
     for _ in range(args.warmup):
@@ -420,14 +545,21 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    r = run_ours(args, rank, world, local_rank)
-    if rank == 0:
-        res, w = r
-        if not args.no_cpu_baseline:
-            cb, _ = oracle_sample(w, 8.0)
-            cb.pop("seconds", None)
-            res["cpu_baseline"] = cb
-        print(json.dumps(res), flush=True)
+    if args.workload == "produce":
+        res, p = run_produce(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = produce_cpu_baseline(p)
+            print(json.dumps(res), flush=True)
+    else:
+        r = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            res, w = r
+            if not args.no_cpu_baseline:
+                cb, _ = oracle_sample(w, 8.0)
+                cb.pop("seconds", None)
+                res["cpu_baseline"] = cb
+            print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -44,6 +44,8 @@ def lib() -> ctypes.CDLL:
             P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
             sig = {
                 "kv8_quantize_rows": (i32, [P, i64, i64, P, P, P, i64, P]),
+                "kv8_produce_rows": (i32, [P, i64, i64, P, ctypes.c_float, P, P, P, i64, P, P, P,
+                                           i64, P, P]),
                 "mla_absorb_decode_fp8_workspace_size": (i64, [i64, i32, i32]),
                 "mla_absorb_decode_fp8": (i32, [P, P, P, P, i64, i32, f32, P, P, P, i64, i32, P]),
                 "mla_absorb_decode_fp8_batch_workspace_size": (i64, [i32, i32, i32, i32, i32]),
@@ -116,6 +118,38 @@ def kv8_quantize_rows(src, kv_codes, kv_scales, dst_slot=None, stream=None):
                                  _ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0],
                                  _stream(stream))
     _check("kv8_quantize_rows", st)
+
+
+def kv8_produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, kv_codes, kv_scales,
+                     dst_slot=None, err_word=None, stream=None):
+    """Fused producer: RMS norm (Lc) + rotary pairs (Rc) + quantize raw rows src [n, >=576]."""
+    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and src.is_cuda
+            and src.dim() == 2 and src.stride(1) == 1):
+        raise ValueError("src must be a CUDA float32 [n, >=576] tensor with unit column stride")
+    _need(norm_weight, "norm_weight", torch.float32, 1)
+    _need(positions, "positions", torch.int64, 1)
+    _need(rope_cos, "rope_cos", torch.float32, 2)
+    _need(rope_sin, "rope_sin", torch.float32, 2)
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    if norm_weight.numel() != KV8_DL:
+        raise ValueError("norm_weight must have 512 entries")
+    if positions.numel() != src.shape[0]:
+        raise ValueError("positions must have one entry per source row")
+    if rope_cos.shape != rope_sin.shape or rope_cos.shape[1] != KV8_DR // 2:
+        raise ValueError("rope_cos and rope_sin must both be [max_pos, 32]")
+    if dst_slot is not None:
+        _need(dst_slot, "dst_slot", torch.int64, 1)
+        if dst_slot.numel() != src.shape[0]:
+            raise ValueError("dst_slot must have one entry per source row")
+    if err_word is not None and not (err_word.is_cuda and err_word.dtype == torch.int32):
+        raise ValueError("err_word must be a CUDA int32 tensor")
+    st = lib().kv8_produce_rows(_ptr(src), src.shape[0], src.stride(0), _ptr(norm_weight),
+                                float(eps), _ptr(positions), _ptr(rope_cos), _ptr(rope_sin),
+                                rope_cos.shape[0], _ptr(dst_slot), _ptr(kv_codes),
+                                _ptr(kv_scales), kv_codes.shape[0], _ptr(err_word),
+                                _stream(stream))
+    _check("kv8_produce_rows", st)
 
 
 # ----------------------------------------------------------------- decode

@@ -118,6 +118,29 @@ int kv8_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
   return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
 }
 
+int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                     const float* norm_weight, float eps, const int64_t* positions,
+                     const float* rope_cos, const float* rope_sin, int64_t max_pos,
+                     const int64_t* dst_slot, uint8_t* kv_codes, float* kv_scales,
+                     int64_t n_slots, unsigned* err_word, void* stream) {
+  if (n_rows < 0 || n_slots < 0 || max_pos < 1) return KV8_EINVAL;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return KV8_EINVAL;  // also rejects NaN
+  if (n_rows == 0) return KV8_OK;
+  if (src == nullptr || norm_weight == nullptr || positions == nullptr || rope_cos == nullptr ||
+      rope_sin == nullptr || kv_codes == nullptr || kv_scales == nullptr)
+    return KV8_EINVAL;
+  if (src_row_stride < KV8_D) return KV8_EINVAL;
+  if (dst_slot == nullptr && n_rows > n_slots) return KV8_EINVAL;
+  if (!aligned(src, 16) || (src_row_stride % 4) != 0 || !aligned(norm_weight, 16) ||
+      !aligned(positions, 8) || !aligned(rope_cos, 4) || !aligned(rope_sin, 4) ||
+      !aligned(kv_codes, 16) || !aligned(kv_scales, 8) || !aligned(err_word, 4))
+    return KV8_EALIGN;
+  cudaError_t e = launch_produce(src, n_rows, src_row_stride, norm_weight, eps, positions,
+                                 rope_cos, rope_sin, max_pos, dst_slot, kv_codes, kv_scales,
+                                 n_slots, err_word, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
+}
+
 int64_t mla_absorb_decode_fp8_workspace_size(int64_t T, int H, int variant) {
   if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant)) return -1;
   return plan_decode(1, H, T, variant).ws_bytes;

@@ -60,5 +60,10 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_quantize(const float* src, int64_t n_rows, int64_t stride,
                             const int64_t* dst_slot, uint8_t* codes, float* scales,
                             int64_t n_slots, cudaStream_t s);
+cudaError_t launch_produce(const float* src, int64_t n_rows, int64_t stride, const float* weight,
+                           float eps, const int64_t* positions, const float* rope_cos,
+                           const float* rope_sin, int64_t max_pos, const int64_t* dst_slot,
+                           uint8_t* codes, float* scales, int64_t n_slots, unsigned* err,
+                           cudaStream_t s);
 
 }  // namespace kv8

@@ -169,3 +169,35 @@ def make(name: str, scale: float = 1.0, seed: int | None = None) -> Workload:
                         np.ascontiguousarray(q[..., DL:]))
 
     raise ValueError(f"unknown workload {name!r}; choose from {WORKLOADS}")
+
+
+@dataclasses.dataclass
+class ProducerInputs:
+    """Raw rows for the fused producer, with its tables (all seeded inputs)."""
+    rows: np.ndarray        # f32 [n, 576]: pre-norm Lc, pre-rotation Rc
+    weight: np.ndarray      # f32 [512] norm weight
+    eps: float
+    positions: np.ndarray   # int64 [n]
+    rope_cos: np.ndarray    # f32 [max_pos, 32]
+    rope_sin: np.ndarray    # f32 [max_pos, 32]
+    slots: np.ndarray       # int64 [n]: distinct cache slots
+    n_slots: int
+
+
+def producer_inputs(n: int, max_pos: int = 16384, seed: int = 4, base: float = 10000.0,
+                    eps: float = 1e-6) -> ProducerInputs:
+    """Rows of the append workload's value mix (Student-t nu=3, 1% zero rows, 1%
+    subnormal-amax rows, 0.1% NaN entries) before normalisation and rotation; a
+    norm weight around 1; positions uniform in [0, max_pos); the rotation tables
+    cos/sin(pos * base^(-j/32)) for the 32 pairs, computed in float64 and
+    rounded to f32 (the caller's rope cache); slots a random injective map into a
+    pool twice the size."""
+    rng = np.random.default_rng(seed)
+    rows = _append_rows(rng, n)
+    weight = (1.0 + 0.1 * rng.standard_normal(DL)).astype(np.float32)
+    positions = rng.integers(0, max_pos, n).astype(np.int64)
+    ang = np.outer(np.arange(max_pos, dtype=np.float64), base ** (-np.arange(DR // 2) / (DR // 2)))
+    n_slots = 2 * n
+    slots = rng.permutation(n_slots)[:n].astype(np.int64)
+    return ProducerInputs(rows, weight, eps, positions, np.cos(ang).astype(np.float32),
+                          np.sin(ang).astype(np.float32), slots, n_slots)

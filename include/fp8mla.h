@@ -101,6 +101,42 @@ int kv8_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
                       int64_t n_slots, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kv8_produce_rows -- KV8 page, PR description, attention_rows item: the
+ * producer quantizes "the fresh normed/roped row" instead of an f32 copy.  The
+ * fused form of that producer: from the raw latent rows to cache codes in one
+ * pass.  The page names the steps; the formulas are our reading.  For each row r
+ * with position pos = positions[r]:
+ *   Lc (floats 0..511):   ss  = sum of x_i^2 in a fixed order (32 partial sums
+ *                         of x[16l..16l+15] in index order, then for o = 16, 8,
+ *                         4, 2, 1 every partial p_l becomes p_l + p_(l xor o));
+ *                         inv = 1 / sqrt(ss / 512 + eps);  y_i = (x_i * inv) * w_i
+ *   Rc (floats 512..575): for pair j = 0..31, (x0, x1) = (x[512+2j], x[512+2j+1]),
+ *                         c = rope_cos[pos][j], s = rope_sin[pos][j]:
+ *                         y0 = x0*c - x1*s,  y1 = x0*s + x1*c
+ *   then y is quantized exactly as by kv8_quantize_rows into slot dst_slot[r].
+ * Every f32 operation is rounded once (no FMA), so the codes are bit-identical
+ * to the oracle's for every input.
+ *
+ *   src            device f32 [n_rows][src_row_stride]; 16-byte aligned,
+ *                  src_row_stride (in floats) >= 576 and a multiple of 4.
+ *   norm_weight    device f32 [512], 16-byte aligned.
+ *   eps            finite, >= 0.
+ *   positions      device int64 [n_rows].  A row whose position is outside
+ *                  [0, max_pos) is skipped (writes nothing) and, when err_word
+ *                  is not NULL, sets bit 0 of *err_word (atomic OR; the caller
+ *                  clears it).
+ *   rope_cos/sin   device f32 [max_pos][32], 4-byte aligned.
+ *   dst_slot, kv_codes, kv_scales, n_slots: as for kv8_quantize_rows.
+ *   err_word       device uint32 or NULL.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
+                     const float* norm_weight, float eps, const int64_t* positions,
+                     const float* rope_cos, const float* rope_sin, int64_t max_pos,
+                     const int64_t* dst_slot, uint8_t* kv_codes, float* kv_scales,
+                     int64_t n_slots, unsigned* err_word, void* stream);
+
+/* ---------------------------------------------------------------------------
  * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph ("the
  * latent is both key and value in the absorbed attention"), attention_rows item
  * (score and context loops dequantize inline "with the scale hoisted out of the

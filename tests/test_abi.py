@@ -23,7 +23,8 @@ def declared_functions():
 
 def test_header_declares_the_documented_calls():
     names = declared_functions()
-    for want in ("kv8_quantize_rows", "mla_absorb_decode_fp8", "mla_absorb_decode_fp8_batch",
+    for want in ("kv8_quantize_rows", "kv8_produce_rows", "mla_absorb_decode_fp8",
+                 "mla_absorb_decode_fp8_batch",
                  "mla_absorb_decode_fp8_workspace_size",
                  "mla_absorb_decode_fp8_batch_workspace_size", "kv8_status_string"):
         assert want in names
@@ -64,6 +65,36 @@ def test_quantize_rejects_bad_arguments_on_host():
     assert f(P(good), 4, 576, None, P(good + 8), P(good), 10, None) == EALIGN
     assert f(P(good), 4, 576, None, P(good), P(good + 4), 10, None) == EALIGN
     assert f(P(good), 0, 576, None, None, None, 0, None) == 0  # nothing to do
+
+
+def test_produce_rejects_bad_arguments_on_host():
+    L = pkg.lib()
+    f = L.kv8_produce_rows
+    g = 1 << 20
+    base = [P(g), 4, 576, P(g), 1e-6, P(g), P(g), P(g), 16, None, P(g), P(g), 10, None, None]
+
+    def call(**kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return f(*a)
+    assert call(a1=-1) == EINVAL
+    assert call(a8=0) == EINVAL                      # max_pos < 1
+    assert call(a4=-1.0) == EINVAL                   # negative eps
+    assert call(a4=float("nan")) == EINVAL
+    assert call(a0=None) == EINVAL
+    assert call(a3=None) == EINVAL                   # norm weight
+    assert call(a5=None) == EINVAL                   # positions
+    assert call(a6=None) == EINVAL
+    assert call(a2=575) == EINVAL
+    assert call(a1=11) == EINVAL                     # identity slots past n_slots
+    assert call(a0=P(g + 4)) == EALIGN
+    assert call(a2=578) == EALIGN
+    assert call(a3=P(g + 4)) == EALIGN
+    assert call(a5=P(g + 4)) == EALIGN
+    assert call(a10=P(g + 8)) == EALIGN
+    assert call(a13=P(g + 2)) == EALIGN
+    assert call(a1=0, a0=None, a3=None) == 0         # nothing to do
 
 
 def test_decode_rejects_bad_arguments_on_host():
