@@ -167,6 +167,22 @@ def produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, dst_slot=
     return codes, scales
 
 
+# ---------------------------------------------------------------- W_UV epilogue
+def bf16_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32, exactly (the upper half of an f32)."""
+    bits = np.asarray(bits, np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def wuv_project(o, w_uv_bits) -> np.ndarray:
+    """Per-head projection of the latent context (the step after the attention in the
+    absorbed form): y[b][h][v] = sum_d o[b][h][d] * W_UV[h][d][v], in float64, with the
+    bf16 weights taken exactly.  o: [B, H, 512]; w_uv_bits: uint16 [H, 512, V]."""
+    o = np.asarray(o, np.float64)
+    w = bf16_to_f32(w_uv_bits).astype(np.float64)
+    return np.einsum("bhd,hdv->bhv", o, w)
+
+
 # ---------------------------------------------------------------- quantizer
 def quantize_rows(src, dst_slot=None, n_slots=None, codes=None, scales=None):
     """Quantize f32 rows [n, >=576] into (codes [n_slots, 576] u8, scales [n_slots, 2] f32)."""
