@@ -7,7 +7,7 @@ kv_lora 512 + qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token,
 One step = one decode query per sequence over its whole cache (the "append"
 workload also quantizes 65536 fresh rows into the cache inside the step).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce|wuv]
                     [--variant auto|simt|tcgen05] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  `value` = KV GB/s over all ranks (KV bytes the
@@ -407,6 +407,56 @@ def run_produce(args, rank, world, local_rank):
     return res, p
 
 
+WUV_METRIC = "fp8-latent MLA decode W_UV epilogue (per-head value projection): GB/s"
+
+
+def run_wuv(args, rank, world, local_rank):
+    """The W_UV epilogue after the long workload's decode: B=2 sequences, H=128, V=128."""
+    import torch
+    import fp8_mla_latent_gb300 as pkg
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    B, H, V = 2, 128, 128
+    rng = np.random.default_rng(9)
+    o = torch.from_numpy(rng.standard_normal((B, H, 512)).astype(np.float32)).to(dev)
+    w = torch.from_numpy((rng.standard_normal((H, 512, V)) / np.sqrt(512)).astype(np.float32))
+    w = w.to(torch.bfloat16).to(dev)
+    y = torch.empty((B, H, V), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        pkg.mla_wuv_epilogue(o, w, y)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkg.mla_wuv_epilogue(o, w, y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    nbytes = H * 512 * V * 2 + B * H * 512 * 4 + B * H * V * 4
+    peaks = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": WUV_METRIC, "value": world * achieved, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 accum",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "wuv", "B": B, "H": H, "V": V, "l2": "flushed between steps"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "wuv",
+                     "ms_per_launch": ms, "peak_note": f"{peaks['src']} copy",
+                     "algorithmic": {"bytes": nbytes, "per_unit": "H*512*V bf16 weights + B*H*(512+V) f32"}},
+        "gpu_launches": args.steps,
+        "clocks": {"note": "timed region shorter than the 50 ms sampling period"},
+    }
+
+
 def produce_cpu_baseline(p, budget_s=8.0):
     import oracle
     n = p.rows.shape[0]
@@ -545,7 +595,11 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    if args.workload == "produce":
+    if args.workload == "wuv":
+        res = run_wuv(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    elif args.workload == "produce":
         res, p = run_produce(args, rank, world, local_rank)
         if rank == 0:
             if not args.no_cpu_baseline:

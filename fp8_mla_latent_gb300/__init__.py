@@ -11,7 +11,7 @@ from ._lib import (KV8_BLOCK, KV8_D, KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECOD
                    mla_absorb_decode_fp8_batch, mla_absorb_decode_fp8_batch_combine,
                    mla_absorb_decode_fp8_batch_noalloc, mla_absorb_decode_fp8_batch_partials,
                    mla_absorb_decode_fp8_batch_workspace_size,
-                   mla_absorb_decode_fp8_workspace_size)
+                   mla_absorb_decode_fp8_workspace_size, mla_wuv_epilogue)
 
 __all__ = [
     "KV8_BLOCK", "KV8_D", "KV8_DECODE_AUTO", "KV8_DECODE_SIMT", "KV8_DECODE_TCGEN05", "KV8_DL",
@@ -20,4 +20,5 @@ __all__ = [
     "mla_absorb_decode_fp8_batch_combine", "mla_absorb_decode_fp8_batch_noalloc",
     "mla_absorb_decode_fp8_batch_partials",
     "mla_absorb_decode_fp8_batch_workspace_size", "mla_absorb_decode_fp8_workspace_size",
+    "mla_wuv_epilogue",
 ]

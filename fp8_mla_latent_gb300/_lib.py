@@ -46,6 +46,7 @@ def lib() -> ctypes.CDLL:
                 "kv8_quantize_rows": (i32, [P, i64, i64, P, P, P, i64, P]),
                 "kv8_produce_rows": (i32, [P, i64, i64, P, ctypes.c_float, P, P, P, i64, P, P, P,
                                            i64, P, P]),
+                "mla_wuv_epilogue": (i32, [P, P, i32, i32, i32, P, P]),
                 "mla_absorb_decode_fp8_workspace_size": (i64, [i64, i32, i32]),
                 "mla_absorb_decode_fp8": (i32, [P, P, P, P, i64, i32, f32, P, P, P, i64, i32, P]),
                 "mla_absorb_decode_fp8_batch_workspace_size": (i64, [i32, i32, i32, i32, i32]),
@@ -150,6 +151,25 @@ def kv8_produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, kv_co
                                 _ptr(kv_scales), kv_codes.shape[0], _ptr(err_word),
                                 _stream(stream))
     _check("kv8_produce_rows", st)
+
+
+def mla_wuv_epilogue(o, w_uv, y=None, stream=None):
+    """Per-head value projection y[b,h,:] = o[b,h,:] @ W_UV[h]; o f32 [B,H,512], w_uv bf16 [H,512,V]."""
+    _need(o, "o", torch.float32, 3)
+    if not (isinstance(w_uv, torch.Tensor) and w_uv.is_cuda and w_uv.dim() == 3
+            and w_uv.dtype in (torch.bfloat16, torch.int16, torch.uint16)
+            and w_uv.is_contiguous()):
+        raise ValueError("w_uv must be a contiguous CUDA bfloat16 [H, 512, V] tensor")
+    B, H, dl = o.shape
+    if dl != KV8_DL or w_uv.shape[0] != H or w_uv.shape[1] != KV8_DL:
+        raise ValueError("shapes must be o [B, H, 512] and w_uv [H, 512, V]")
+    V = w_uv.shape[2]
+    if y is None:
+        y = torch.empty((B, H, V), dtype=torch.float32, device=o.device)
+    _need(y, "y", torch.float32, 3)
+    st = lib().mla_wuv_epilogue(_ptr(o), _ptr(w_uv), B, H, V, _ptr(y), _stream(stream))
+    _check("mla_wuv_epilogue", st)
+    return y
 
 
 # ----------------------------------------------------------------- decode

@@ -141,6 +141,16 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
   return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
 }
 
+int mla_wuv_epilogue(const float* o, const uint16_t* w_uv, int B, int H, int V, float* y,
+                     void* stream) {
+  if (B < 0 || H < 1 || H > 1024 || V < 1 || V > 4096) return KV8_EINVAL;
+  if (B == 0) return KV8_OK;
+  if (o == nullptr || w_uv == nullptr || y == nullptr) return KV8_EINVAL;
+  if (!aligned(o, 4) || !aligned(w_uv, 2) || !aligned(y, 4)) return KV8_EALIGN;
+  cudaError_t e = launch_wuv(o, w_uv, B, H, V, y, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
+}
+
 int64_t mla_absorb_decode_fp8_workspace_size(int64_t T, int H, int variant) {
   if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant)) return -1;
   return plan_decode(1, H, T, variant).ws_bytes;

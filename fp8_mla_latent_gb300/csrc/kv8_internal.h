@@ -65,5 +65,7 @@ cudaError_t launch_produce(const float* src, int64_t n_rows, int64_t stride, con
                            const float* rope_sin, int64_t max_pos, const int64_t* dst_slot,
                            uint8_t* codes, float* scales, int64_t n_slots, unsigned* err,
                            cudaStream_t s);
+cudaError_t launch_wuv(const float* o, const uint16_t* w, int B, int H, int V, float* y,
+                       cudaStream_t s);
 
 }  // namespace kv8

@@ -137,6 +137,25 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
                      int64_t n_slots, unsigned* err_word, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * mla_wuv_epilogue -- the step after the absorbed attention (KV8 page, PR
+ * description: "the latent is both key and value in the absorbed attention", so
+ * the attention's output is a latent context per head): the per-head value
+ * projection
+ *   y[b][h][v] = sum_{d<512} o[b][h][d] * W_UV[h][d][v]      (f32 accumulation)
+ *
+ *   o        device f32 [B][H][512] (e.g. the decode call's out), 4-byte aligned.
+ *   w_uv     device bf16 bit patterns [H][512][V], 2-byte aligned.
+ *   B, H, V  B >= 0, 1 <= H <= 1024, 1 <= V <= 4096.
+ *   y        device f32 [B][H][V].
+ * Tolerance: f32 sums of 512 products in a fixed order (partial sums over
+ * interleaved latent rows, then added in row-group order):
+ * max-abs error <= 1e-5 * max|y| against float64.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int mla_wuv_epilogue(const float* o, const uint16_t* w_uv, int B, int H, int V, float* y,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph ("the
  * latent is both key and value in the absorbed attention"), attention_rows item
  * (score and context loops dequantize inline "with the scale hoisted out of the

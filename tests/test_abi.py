@@ -97,6 +97,19 @@ def test_produce_rejects_bad_arguments_on_host():
     assert call(a1=0, a0=None, a3=None) == 0         # nothing to do
 
 
+def test_wuv_rejects_bad_arguments_on_host():
+    f = pkg.lib().mla_wuv_epilogue
+    g = 1 << 20
+    assert f(P(g), P(g), -1, 4, 128, P(g), None) == EINVAL
+    assert f(P(g), P(g), 2, 0, 128, P(g), None) == EINVAL
+    assert f(P(g), P(g), 2, 4, 0, P(g), None) == EINVAL
+    assert f(P(g), P(g), 2, 4, 5000, P(g), None) == EINVAL
+    assert f(None, P(g), 2, 4, 128, P(g), None) == EINVAL
+    assert f(P(g + 2), P(g), 2, 4, 128, P(g), None) == EALIGN
+    assert f(P(g), P(g + 1), 2, 4, 128, P(g), None) == EALIGN
+    assert f(None, None, 0, 4, 128, None, None) == 0
+
+
 def test_decode_rejects_bad_arguments_on_host():
     L = pkg.lib()
     g = 1 << 20
