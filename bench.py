@@ -59,6 +59,8 @@ def source_hash(files):
 
 KERNEL_SOURCES = {
     "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "produce_rows": ["fp8_mla_latent_gb300/csrc/quantize.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "wuv": ["fp8_mla_latent_gb300/csrc/wuv.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "decode_simt": ["fp8_mla_latent_gb300/csrc/decode_simt.cu",
                     "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
 }
@@ -395,7 +397,8 @@ def run_produce(args, rank, world, local_rank):
                    "l2": "flushed between steps (256 MB write); rows > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic_for("produce_rows", "produce") if n == 65536 else None,
                      "kernel": "produce_rows", "ms_per_launch": ms,
                      "peak_note": f"{peaks['src']} copy",
                      "algorithmic": {"bytes": nbytes, "per_unit": f"{PRODUCE_ROW_BYTES} B per row"}},
@@ -449,7 +452,8 @@ def run_wuv(args, rank, world, local_rank):
         "data": "synthetic (seeded)",
         "config": {"workload": "wuv", "B": B, "H": H, "V": V, "l2": "flushed between steps"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "wuv",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("wuv", "wuv"),
+                     "kernel": "wuv",
                      "ms_per_launch": ms, "peak_note": f"{peaks['src']} copy",
                      "algorithmic": {"bytes": nbytes, "per_unit": "H*512*V bf16 weights + B*H*(512+V) f32"}},
         "gpu_launches": args.steps,

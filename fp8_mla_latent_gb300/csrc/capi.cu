@@ -33,7 +33,9 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   p.target = NUM_SMS * (v == kTc ? 1 : 4);
   p.max_items = p.target + B * p.n_hg;
   const int64_t parts = (int64_t)p.max_items * p.hg;
-  int64_t off = 256;  // header: error word
+  p.off_seg = 64;  // header: error word, then the item table of the split
+  p.hdr_bytes = align_up(p.off_seg + (int64_t)B * p.n_hg * 16, 256);
+  int64_t off = p.hdr_bytes;
   p.off_m = off;
   off = align_up(off + parts * 4, 256);
   p.off_l = off;
@@ -57,6 +59,7 @@ int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes
   if (!aligned(workspace, 256)) return KV8_EALIGN;
   char* ws = static_cast<char*>(const_cast<void*>(workspace));
   a.err = reinterpret_cast<unsigned*>(ws);
+  a.seg = reinterpret_cast<int64_t*>(ws + a.plan.off_seg);
   a.ws_m = reinterpret_cast<float*>(ws + a.plan.off_m);
   a.ws_l = reinterpret_cast<float*>(ws + a.plan.off_l);
   a.ws_o = reinterpret_cast<float*>(ws + a.plan.off_o);
@@ -64,7 +67,7 @@ int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes
 }
 
 int run_partials(DecodeArgs& a, cudaStream_t s) {
-  if (cudaMemsetAsync(a.err, 0, sizeof(unsigned), s) != cudaSuccess) return KV8_ECUDA;
+  if (cudaMemsetAsync(a.err, 0, a.plan.hdr_bytes, s) != cudaSuccess) return KV8_ECUDA;
   cudaError_t e = (a.plan.variant == kTc) ? launch_decode_tc(a, s) : launch_decode_simt(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? KV8_EUNSUPPORTED : KV8_ECUDA;
   return KV8_OK;

@@ -1,6 +1,6 @@
 // combine.cu -- merge of the split-T partials (flash-decoding log-sum-exp merge).
 // The partials of (sequence, head) are those of the work items of its head
-// group, found from the sequence lengths exactly as the split kernel cut them.
+// group, whose range the split kernel recorded in the workspace's item table.
 //
 // KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"),
 // closing note: split-T kernels remove the T caps of the CUDA path.  With the
@@ -37,13 +37,10 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
   __shared__ float red[8];
   __shared__ float4 half1[128];
   __shared__ float wsh[WCHUNK];
-  if (threadIdx.x < 32) {
-    int64_t f, c;
-    item_range(a, b, h / a.plan.hg, f, c);
-    if (threadIdx.x == 0) {
-      s_first = f;
-      s_count = c;
-    }
+  if (threadIdx.x == 0) {
+    const int64_t* e = a.seg + ((int64_t)b * a.plan.n_hg + h / a.plan.hg) * 2;
+    s_first = e[0];
+    s_count = e[1];
   }
   __syncthreads();
   const int64_t first = s_first, ns = s_count;

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) {
     WorkItem it;
     const bool ok = find_item(a, blockIdx.x, it);
+    if (lane == 0 && ok) record_segment(a, blockIdx.x, it);
     if (lane == 0) {
       s_it = it;
       s_ok = ok ? 1 : 0;

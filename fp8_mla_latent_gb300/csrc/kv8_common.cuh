@@ -78,7 +78,17 @@ __device__ __forceinline__ int64_t seq_len_of(const DecodeArgs& a, int b) {
 struct WorkItem {
   int b, g;        // sequence, head group
   int64_t t0, t1;  // tokens [t0, t1) of sequence b
+  int64_t first, count;  // items of (b, g): [first, first + count)
 };
+
+// The CTA of the first item of (b, g) records that segment for the merge.
+__device__ __forceinline__ void record_segment(const DecodeArgs& a, int64_t k, const WorkItem& it) {
+  if (k == it.first) {
+    int64_t* e = a.seg + ((int64_t)it.b * a.plan.n_hg + it.g) * 2;
+    e[0] = it.first;
+    e[1] = it.count;
+  }
+}
 
 __device__ __forceinline__ int64_t tiles_of(const DecodeArgs& a, int b) {
   return (seq_len_of(a, b) + TILE - 1) / TILE;
@@ -174,17 +184,8 @@ __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkIt
     const int64_t T = seq_len_of(a, b);
     const int64_t e = (s + 1) * st * TILE;
     it.t1 = e < T ? e : T;
-  });
-}
-
-// Warp-wide: first item and item count of (sequence b, head group g).
-__device__ __forceinline__ void item_range(const DecodeArgs& a, int b, int g, int64_t& first,
-                                           int64_t& count) {
-  first = 0;
-  count = 0;
-  scan_items(a, -1, b, [&](int, int64_t f0, int64_t ns, int64_t) {
-    first = f0 + (int64_t)g * ns;
-    count = ns;
+    it.first = first + (int64_t)it.g * ns;
+    it.count = ns;
   });
 }
 

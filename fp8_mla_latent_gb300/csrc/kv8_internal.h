@@ -26,8 +26,9 @@ struct SplitPlan {
   int target;       // CTAs the work is spread over (one wave of the split kernel)
   int max_items;    // upper bound on work items: the split kernel's grid size
   int64_t ws_bytes; // workspace bytes needed
-  // byte offsets inside the workspace
-  int64_t off_m, off_l, off_o;
+  // byte offsets inside the workspace; the header (error word, then the item
+  // table) is cleared by every split launch
+  int64_t hdr_bytes, off_seg, off_m, off_l, off_o;
 };
 
 // Deterministic in its arguments (no device query), so the workspace-size call
@@ -48,6 +49,7 @@ struct DecodeArgs {
   float* out;                  // [B][H][512]
   float* lse;                  // [B][H] or nullptr
   unsigned* err;               // workspace header word
+  int64_t* seg;                // [B][n_hg][2]: first work item and item count (0 if none)
   float* ws_m;                 // [max_items][hg]   running max, log2 units
   float* ws_l;                 // [max_items][hg]   sum of exp2(z - m)
   float* ws_o;                 // [max_items][hg][512] unnormalised context
