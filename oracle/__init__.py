@@ -183,6 +183,21 @@ def wuv_project(o, w_uv_bits) -> np.ndarray:
     return np.einsum("bhd,hdv->bhv", o, w)
 
 
+# ---------------------------------------------------------------- prefill projection
+def prefill_project(codes, scales, w_ukv_bits, slots=None) -> np.ndarray:
+    """Non-absorbed path: the cached latent of T tokens, dequantized (dec(code) * sLc, as
+    stored), times the up-projection W_UKV (bf16 [512, N], taken exactly), in float64:
+    Y[t][n] = sLc_t * sum_d dec(Lc_t[d]) * W[d][n].  slots[t] is token t's cache slot
+    (None: slot t)."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.float32)
+    idx = np.arange(codes.shape[0]) if slots is None else np.asarray(slots, np.int64)
+    lut = decode_table().astype(np.float64)
+    lc = lut[codes[idx, :DL]] * scales[idx, 0].astype(np.float64)[:, None]
+    w = bf16_to_f32(w_ukv_bits).astype(np.float64)
+    return lc @ w
+
+
 # ---------------------------------------------------------------- quantizer
 def quantize_rows(src, dst_slot=None, n_slots=None, codes=None, scales=None):
     """Quantize f32 rows [n, >=576] into (codes [n_slots, 576] u8, scales [n_slots, 2] f32)."""
