@@ -198,6 +198,16 @@ def prefill_project(codes, scales, w_ukv_bits, slots=None) -> np.ndarray:
     return lc @ w
 
 
+def prefill_rope(codes, scales, slots=None) -> np.ndarray:
+    """Rope keys of the non-absorbed path: the cached Rc of each token dequantized,
+    dec(Rc_t[j]) * sRc_t, the exact product (float64) rounded once to float32."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.float32)
+    idx = np.arange(codes.shape[0]) if slots is None else np.asarray(slots, np.int64)
+    lut = decode_table().astype(np.float64)
+    return (lut[codes[idx, DL:]] * scales[idx, 1].astype(np.float64)[:, None]).astype(np.float32)
+
+
 # ---------------------------------------------------------------- quantizer
 def quantize_rows(src, dst_slot=None, n_slots=None, codes=None, scales=None):
     """Quantize f32 rows [n, >=576] into (codes [n_slots, 576] u8, scales [n_slots, 2] f32)."""

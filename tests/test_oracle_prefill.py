@@ -56,3 +56,39 @@ def test_rope_part_and_scale_of_rc_are_not_used():
     c2[:, 512:] = 0x33
     s2[:, 1] = 7.0
     assert np.array_equal(oracle.prefill_project(c2, s2, wb), y)
+
+
+def test_rope_keys_round_trip_within_half_an_e4m3_step():
+    """Quantize then dequantize: every rope channel comes back within half a step of
+    the e4m3 grid scaled by the row's Rc scale (3 mantissa bits: relative 2^-4 for
+    normals, 2^-10 * sRc below the normal range).  Lc is 1000x larger than Rc in these
+    rows, so using the Lc scale, or the Lc columns, fails the bound."""
+    rng = np.random.default_rng(7)
+    n = 40
+    rows = rng.standard_normal((n, 576)).astype(np.float32)
+    rows[:, :512] *= 1000.0
+    rows[3, 512:] = 0.0            # all-zero rope segment
+    codes, scales = oracle.quantize_rows(rows)
+    k = oracle.prefill_rope(codes, scales)
+    assert k.dtype == np.float32 and k.shape == (n, 64)
+    x = rows[:, 512:].astype(np.float64)
+    sR = scales[:, 1].astype(np.float64)[:, None]
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, sR * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(np.abs(k - x) <= bound)
+    assert np.all(k[3] == 0)
+    # the channel holding the amax decodes to 448 * sRc (code 0x7E, or 0xFE)
+    j = np.argmax(np.abs(x), axis=1)
+    for t in range(n):
+        if t == 3:
+            continue
+        assert abs(k[t, j[t]]) == np.float32(448.0 * np.float64(scales[t, 1]))
+
+
+def test_rope_keys_follow_the_slot_map():
+    rng = np.random.default_rng(8)
+    codes, scales = cache(rng, 10)
+    slots = np.array([9, 2, 2, 0])
+    k = oracle.prefill_rope(codes, scales, slots)
+    full = oracle.prefill_rope(codes, scales)
+    assert np.array_equal(k, full[slots])
+    assert not np.array_equal(full[9], full[2])
