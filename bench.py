@@ -7,7 +7,7 @@ kv_lora 512 + qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token,
 One step = one decode query per sequence over its whole cache (the "append"
 workload also quantizes 65536 fresh rows into the cache inside the step).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce|wuv]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce|wuv|prefill]
                     [--variant auto|simt|tcgen05] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  `value` = KV GB/s over all ranks (KV bytes the
@@ -61,6 +61,8 @@ KERNEL_SOURCES = {
     "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "produce_rows": ["fp8_mla_latent_gb300/csrc/quantize.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "wuv": ["fp8_mla_latent_gb300/csrc/wuv.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "prefill": ["fp8_mla_latent_gb300/csrc/prefill.cu", "fp8_mla_latent_gb300/csrc/tc_ptx.cuh",
+                "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "decode_simt": ["fp8_mla_latent_gb300/csrc/decode_simt.cu",
                     "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
 }
@@ -461,6 +463,157 @@ def run_wuv(args, rank, world, local_rank):
     }
 
 
+PREFILL_METRIC = "fp8-latent non-absorbed prefill projection (cached latent x kv_b, rope keys): TFLOP/s"
+
+
+def prefill_bytes(T, N):
+    """Algorithmic bytes of one launch: the cached rows read once, W read once, Y and
+    the rope keys written once."""
+    return T * ROW_BYTES + 512 * N * 2 + T * N * 2 + T * 64 * 4
+
+
+def run_prefill(args, rank, world, local_rank):
+    """The projection of one 4096-token prompt chunk: Y = dequantized Lc x W_UKV
+    (bf16 [512, 32768]) plus the dequantized rope keys."""
+    import torch
+    import fp8_mla_latent_gb300 as pkg
+    from fp8_mla_latent_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T = max(128, int(4096 * args.scale))
+    p = workloads.prefill_inputs(T)
+    N = p.w_ukv.shape[1]
+    codes = torch.zeros((p.n_slots, 576), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((p.n_slots, 2), dtype=torch.float32, device=dev)
+    slots = torch.from_numpy(p.slots).to(dev)
+    pkg.kv8_quantize_rows(torch.from_numpy(p.rows).to(dev), codes, scales, dst_slot=slots)
+    w = torch.from_numpy(p.w_ukv).to(torch.bfloat16).to(dev)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    k_rope = torch.empty((T, 64), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def once():
+        pkg.kv8_prefill_project(codes, scales, w, slots=slots, y=y, k_rope=k_rope, err_word=err)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        once()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        once()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+    assert err.item() == 0, f"prefill error word {err.item()}"
+    ms = float(np.mean(times))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = 2.0 * T * 512 * N
+    tflops = flops / (ms * 1e-3) / 1e12
+    # end to end: the chunk's cache rows and slot map from pinned host memory, Y and
+    # the rope keys back to pinned host memory
+    h_codes = codes.cpu().pin_memory()
+    h_scales = scales.cpu().pin_memory()
+    h_slots = slots.cpu().pin_memory()
+    h_y = torch.empty((T, N), dtype=torch.bfloat16).pin_memory()
+    h_k = torch.empty((T, 64), dtype=torch.float32).pin_memory()
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        codes.copy_(h_codes, non_blocking=True)
+        scales.copy_(h_scales, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        once()
+        h_y.copy_(y, non_blocking=True)
+        h_k.copy_(k_rope, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.mean(e2e))
+    peaks = load_peaks()
+    nbytes = prefill_bytes(T, N)
+    res = {
+        "metric": PREFILL_METRIC, "value": world * tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 operands (e4m3 codes exact), f32 accum, bf16 out",
+        "data": "synthetic (seeded; Gaussian rows with log-normal channel gains, N(0,1/512) weights)",
+        "tokens_per_s": world * T / (ms * 1e-3),
+        "config": {"workload": "prefill", "T": T, "N": N, "heads": 128, "qk_nope": 128, "v_head": 128,
+                   "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                     "traffic": traffic_for("prefill", "prefill") if T == 4096 else None,
+                     "kernel": "prefill", "ms_per_launch": ms,
+                     "peak_note": f"{peaks['src']} cuBLAS bf16 burst",
+                     "algorithmic": {"flops": flops, "per_unit": "2 x 512 x N flops per token",
+                                     "bytes": nbytes, "hbm_gbs": nbytes / (ms * 1e-3) / 1e9}},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": T * ROW_BYTES + T * 8 + 1024 * ROW_BYTES,
+                "d2h_bytes_per_step": T * N * 2 + T * 64 * 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks if clocks else {"note": "timed region shorter than the 50 ms sampling period"},
+    }
+    return res, p
+
+
+def prefill_cpu_baseline(p, budget_s=8.0):
+    """The float64 oracle on a bounded sample: the first n tokens of the chunk, all
+    N columns, n grown until about budget_s of wall time."""
+    import oracle
+    T = p.rows.shape[0]
+    codes, scales = oracle.quantize_rows(p.rows, dst_slot=p.slots, n_slots=p.n_slots)
+    wb = oracle_bf16_bits(p.w_ukv)
+    n, dt = 16, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.prefill_project(codes, scales, wb, slots=p.slots[:n])
+        oracle.prefill_rope(codes, scales, p.slots[:n])
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or n >= T:
+            break
+        n = min(T, n * 4)
+    N = wb.shape[1]
+    value = 2.0 * n * 512 * N / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} of {T} tokens x {N} columns, float64 numpy, {dt:.2f} s wall"}
+
+
+def oracle_bf16_bits(w):
+    """The bf16 bit patterns of the weights, rounded as the GPU arm rounds them."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
 def produce_cpu_baseline(p, budget_s=8.0):
     import oracle
     n = p.rows.shape[0]
@@ -528,6 +681,22 @@ def oracle_sample(w, budget_s, codes=None, scales=None):
 def run_reference(args, world):
     from fp8_mla_latent_gb300 import workloads
     import oracle
+    if args.workload == "prefill":
+        p = workloads.prefill_inputs(max(128, int(4096 * args.scale)))
+        prefill_cpu_baseline(p, 0.5)
+        vals = [prefill_cpu_baseline(p, 2.0) for _ in range(args.steps)]
+        value = float(np.mean([v["value"] for v in vals]))
+        T, N = p.rows.shape[0], p.w_ukv.shape[1]
+        return {
+            "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 2.0 * T * 512 * N / (value * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; same inputs as our arm)",
+            "config": {"workload": "prefill", "T": T, "N": N},
+            "cpu_baseline": dict(vals[-1], value=value),
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     if args.workload == "produce":
         p = workloads.producer_inputs(max(1, int(65536 * args.scale)))
         for _ in range(args.warmup):
@@ -602,6 +771,12 @@ def main():
     if args.workload == "wuv":
         res = run_wuv(args, rank, world, local_rank)
         if rank == 0:
+            print(json.dumps(res), flush=True)
+    elif args.workload == "prefill":
+        res, p = run_prefill(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = prefill_cpu_baseline(p)
             print(json.dumps(res), flush=True)
     elif args.workload == "produce":
         res, p = run_produce(args, rank, world, local_rank)

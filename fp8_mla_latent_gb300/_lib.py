@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
                 "kv8_produce_rows": (i32, [P, i64, i64, P, ctypes.c_float, P, P, P, i64, P, P, P,
                                            i64, P, P]),
                 "mla_wuv_epilogue": (i32, [P, P, i32, i32, i32, P, P]),
+                "kv8_selftest_wait_timeout": (i32, [P, i64, i64, P]),
+                "kv8_prefill_project": (i32, [P, P, i64, P, i64, P, i32, P, P, P, P]),
                 "mla_absorb_decode_fp8_workspace_size": (i64, [i64, i32, i32]),
                 "mla_absorb_decode_fp8": (i32, [P, P, P, P, i64, i32, f32, P, P, P, i64, i32, P]),
                 "mla_absorb_decode_fp8_batch_workspace_size": (i64, [i32, i32, i32, i32, i32]),
@@ -151,6 +153,45 @@ def kv8_produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, kv_co
                                 _ptr(kv_scales), kv_codes.shape[0], _ptr(err_word),
                                 _stream(stream))
     _check("kv8_produce_rows", st)
+
+
+def kv8_prefill_project(kv_codes, kv_scales, w_ukv, T=None, slots=None, y=None, k_rope=None,
+                        err_word=None, stream=None):
+    """Y [T, N] bf16 = dequantized cached latent (slots or 0..T-1) @ W_UKV (bf16 [512, N]);
+    k_rope (optional f32 [T, 64]) receives the dequantized rope keys."""
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    if not (isinstance(w_ukv, torch.Tensor) and w_ukv.is_cuda and w_ukv.dim() == 2
+            and w_ukv.dtype == torch.bfloat16 and w_ukv.is_contiguous() and w_ukv.shape[0] == KV8_DL):
+        raise ValueError("w_ukv must be a contiguous CUDA bfloat16 [512, N] tensor")
+    if slots is not None:
+        _need(slots, "slots", torch.int64, 1)
+        T = slots.numel()
+    elif T is None:
+        T = kv_codes.shape[0]
+    N = w_ukv.shape[1]
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=kv_codes.device)
+    if not (y.dtype == torch.bfloat16 and y.is_cuda and y.is_contiguous() and tuple(y.shape) == (T, N)):
+        raise ValueError("y must be a contiguous CUDA bfloat16 [T, N] tensor")
+    if k_rope is not None and not (k_rope.dtype == torch.float32 and k_rope.is_cuda
+                                   and k_rope.is_contiguous() and tuple(k_rope.shape) == (T, KV8_DR)):
+        raise ValueError("k_rope must be a contiguous CUDA float32 [T, 64] tensor")
+    if err_word is not None and not (err_word.is_cuda and err_word.dtype == torch.int32):
+        raise ValueError("err_word must be a CUDA int32 tensor")
+    st = lib().kv8_prefill_project(_ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0], _ptr(slots),
+                                   int(T), _ptr(w_ukv), int(N), _ptr(y), _ptr(k_rope),
+                                   _ptr(err_word), _stream(stream))
+    _check("kv8_prefill_project", st)
+    return y
+
+
+def kv8_selftest_wait_timeout(workspace, limit_us: int, stream=None):
+    """Run the bounded-wait failure check; afterwards kv8_workspace_error(workspace) is -7."""
+    _need(workspace, "workspace", torch.uint8, 1)
+    st = lib().kv8_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_us),
+                                         _stream(stream))
+    _check("kv8_selftest_wait_timeout", st)
 
 
 def mla_wuv_epilogue(o, w_uv, y=None, stream=None):

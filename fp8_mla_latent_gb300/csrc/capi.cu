@@ -144,6 +144,35 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
   return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
 }
 
+int kv8_prefill_project(const uint8_t* kv_codes, const float* kv_scales, int64_t n_slots,
+                        const int64_t* slots, int64_t T, const uint16_t* w_ukv, int N,
+                        uint16_t* y, float* k_rope, unsigned* err_word, void* stream) {
+  if (T < 0 || n_slots < 0 || N < 256 || (N % 256) != 0) return KV8_EINVAL;
+  if (T == 0) return KV8_OK;
+  if (kv_codes == nullptr || kv_scales == nullptr || w_ukv == nullptr || y == nullptr)
+    return KV8_EINVAL;
+  if (slots == nullptr && T > n_slots) return KV8_EINVAL;
+  if (!aligned(kv_codes, 16) || !aligned(kv_scales, 8) || !aligned(slots, 8) ||
+      !aligned(w_ukv, 16) || !aligned(y, 16) || !aligned(k_rope, 16) || !aligned(err_word, 4))
+    return KV8_EALIGN;
+  cudaError_t e = launch_prefill(kv_codes, kv_scales, slots, n_slots, T, w_ukv, N, y, k_rope, err_word,
+                                 static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return KV8_EUNSUPPORTED;
+  return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
+}
+
+int kv8_selftest_wait_timeout(void* workspace, int64_t workspace_bytes, int64_t limit_us,
+                              void* stream) {
+  if (limit_us < 1 || limit_us > 10000000) return KV8_EINVAL;
+  if (workspace == nullptr || workspace_bytes < 256) return KV8_EWORKSPACE;
+  if (!aligned(workspace, 256)) return KV8_EALIGN;
+  unsigned* err = static_cast<unsigned*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(err, 0, sizeof(unsigned), s) != cudaSuccess) return KV8_ECUDA;
+  return launch_wait_timeout(err, (uint64_t)limit_us * 1000u, s) == cudaSuccess ? KV8_OK
+                                                                                : KV8_ECUDA;
+}
+
 int mla_wuv_epilogue(const float* o, const uint16_t* w_uv, int B, int H, int V, float* y,
                      void* stream) {
   if (B < 0 || H < 1 || H > 1024 || V < 1 || V > 4096) return KV8_EINVAL;

@@ -67,6 +67,10 @@ cudaError_t launch_produce(const float* src, int64_t n_rows, int64_t stride, con
                            const float* rope_sin, int64_t max_pos, const int64_t* dst_slot,
                            uint8_t* codes, float* scales, int64_t n_slots, unsigned* err,
                            cudaStream_t s);
+cudaError_t launch_prefill(const uint8_t* codes, const float* scales, const int64_t* slots,
+                           int64_t n_slots, int64_t T, const uint16_t* w, int N, uint16_t* y,
+                           float* k_rope, unsigned* err, cudaStream_t s);
+cudaError_t launch_wait_timeout(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_wuv(const float* o, const uint16_t* w, int B, int H, int V, float* y,
                        cudaStream_t s);
 

@@ -201,3 +201,25 @@ def producer_inputs(n: int, max_pos: int = 16384, seed: int = 4, base: float = 1
     slots = rng.permutation(n_slots)[:n].astype(np.int64)
     return ProducerInputs(rows, weight, eps, positions, np.cos(ang).astype(np.float32),
                           np.sin(ang).astype(np.float32), slots, n_slots)
+
+
+@dataclasses.dataclass
+class PrefillInputs:
+    rows: np.ndarray        # f32 [T, 576]: latent rows to quantize into the cache
+    slots: np.ndarray       # int64 [T]: cache slot of token t (a permutation of a pool)
+    n_slots: int
+    w_ukv: np.ndarray       # f32 [512, N]: up-projection weights (rounded to bf16 by the caller)
+
+
+def prefill_inputs(T: int = 4096, N: int = 32768, seed: int = 11) -> PrefillInputs:
+    """One prompt chunk of T tokens in a pool of T + 1024 slots (random injective map,
+    as pages hand out slots), rows with the decode workloads' per-channel spread
+    (Gaussian times a log-normal channel gain), and kv_b weights N(0, 1/512):
+    N = 128 heads x (128 qk_nope + 128 v_head)."""
+    rng = np.random.default_rng(seed)
+    gain = np.exp(0.5 * rng.standard_normal(D))
+    rows = (rng.standard_normal((T, D)) * gain).astype(np.float32)
+    n_slots = T + 1024
+    slots = rng.permutation(n_slots)[:T].astype(np.int64)
+    w = (rng.standard_normal((DL, N)) / math.sqrt(DL)).astype(np.float32)
+    return PrefillInputs(rows, slots, n_slots, w)

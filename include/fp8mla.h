@@ -156,6 +156,51 @@ int mla_wuv_epilogue(const float* o, const uint16_t* w_uv, int B, int H, int V, 
                      void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kv8_prefill_project -- the non-absorbed projection of the cached latent (KV8
+ * page, PR description: the projection path dequantizes the cached Lc rows
+ * before the kv_b up-projection):
+ *   Y[t][n] = sLc_t * sum_{d<512} dec(Lc_t[d]) * W_UKV[d][n]
+ * on the tensor cores (bf16 operands: every e4m3 value is exact in bf16; f32
+ * accumulation; the row scale applied to the f32 sum; Y rounded to bf16).
+ *
+ *   kv_codes, kv_scales  the cache, as written by kv8_quantize_rows
+ *                        ([n_slots][576] e4m3, 16-byte aligned; [n_slots][2] f32).
+ *   slots          device int64 [T]: cache slot of token t, or NULL for slot t.
+ *                  A slot outside [0, n_slots) gives a zero row and sets bit 0
+ *                  of *err_word.
+ *   T              tokens (>= 0).
+ *   w_ukv          device bf16 bit patterns [512][N], row-major, 16-byte aligned.
+ *   N              columns, a positive multiple of 256 (H x (qk_nope + v_head)).
+ *   y              device bf16 [T][N], 16-byte aligned.
+ *   k_rope         device f32 [T][64], 16-byte aligned, or NULL: the token's rope
+ *                  key dequantized, sRc_t * dec(Rc_t[j]) rounded once to f32
+ *                  (bit-exact; a zero row for a slot out of range).
+ *   err_word       device uint32 or NULL; bit 2 marks a device-side wait that
+ *                  timed out (the launch then returns without finishing).
+ * Tolerance: max-abs error <= 1e-2 * max|Y| against the float64 oracle (bf16
+ * rounding of the result; f32 sums of 512 products).
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_EUNSUPPORTED, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int kv8_prefill_project(const uint8_t* kv_codes, const float* kv_scales, int64_t n_slots,
+                        const int64_t* slots, int64_t T, const uint16_t* w_ukv, int N,
+                        uint16_t* y, float* k_rope, unsigned* err_word, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kv8_selftest_wait_timeout -- check of the failure path of the device-side
+ * waits.  The decode kernels' pipelines wait on mbarriers with a time limit; a
+ * wait that runs out makes the kernel flag the workspace error word and return
+ * (KV8_ETIMEOUT from kv8_workspace_error), never trap or hang.  This call runs
+ * one warp that waits, through the same bounded wait, on a barrier nothing
+ * arrives at, with the given limit (1 us .. 10 s): afterwards
+ * kv8_workspace_error(workspace) reports KV8_ETIMEOUT and the context is usable.
+ *   workspace  device, >= 256 bytes, 256-byte aligned (its error word is reset
+ *              first).
+ * Errors: KV8_EINVAL, KV8_EWORKSPACE, KV8_EALIGN, KV8_ECUDA.
+ * ------------------------------------------------------------------------- */
+int kv8_selftest_wait_timeout(void* workspace, int64_t workspace_bytes, int64_t limit_us,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
  * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph ("the
  * latent is both key and value in the absorbed attention"), attention_rows item
  * (score and context loops dequantize inline "with the scale hoisted out of the

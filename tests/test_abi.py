@@ -151,3 +151,38 @@ def test_workspace_sizes(variant):
     # more tokens never needs a smaller workspace per split partial
     assert (L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 4096, 64, variant)
             >= L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 1, 64, variant))
+
+
+def test_selftest_rejects_bad_arguments_on_host():
+    f = pkg.lib().kv8_selftest_wait_timeout
+    g = 1 << 20
+    assert f(P(g), 256, 0, None) == EINVAL
+    assert f(P(g), 256, 20_000_000, None) == EINVAL
+    assert f(None, 256, 1000, None) == EWORKSPACE
+    assert f(P(g), 255, 1000, None) == EWORKSPACE
+    assert f(P(g + 16), 256, 1000, None) == EALIGN
+
+
+def test_prefill_rejects_bad_arguments_on_host():
+    f = pkg.lib().kv8_prefill_project
+    g = 1 << 20
+    base = [P(g), P(g), 100, None, 64, P(g), 512, P(g), None, None, None]
+
+    def call(**kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return f(*a)
+    assert call(a4=-1) == EINVAL
+    assert call(a6=300) == EINVAL          # N not a multiple of 256
+    assert call(a6=0) == EINVAL
+    assert call(a4=101) == EINVAL          # identity slots past the pool
+    assert call(a0=None) == EINVAL
+    assert call(a5=None) == EINVAL
+    assert call(a0=P(g + 8)) == EALIGN
+    assert call(a5=P(g + 8)) == EALIGN
+    assert call(a7=P(g + 8)) == EALIGN
+    assert call(a3=P(g + 4)) == EALIGN
+    assert call(a8=P(g + 8)) == EALIGN      # k_rope
+    assert call(a9=P(g + 2)) == EALIGN      # err_word
+    assert call(a4=0, a0=None) == 0
