@@ -147,7 +147,7 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 int kv8_prefill_project(const uint8_t* kv_codes, const float* kv_scales, int64_t n_slots,
                         const int64_t* slots, int64_t T, const uint16_t* w_ukv, int N,
                         uint16_t* y, float* k_rope, unsigned* err_word, void* stream) {
-  if (T < 0 || n_slots < 0 || N < 256 || (N % 256) != 0) return KV8_EINVAL;
+  if (T < 0 || T > (int64_t)1 << 30 || n_slots < 0 || N < 256 || (N % 256) != 0) return KV8_EINVAL;
   if (T == 0) return KV8_OK;
   if (kv_codes == nullptr || kv_scales == nullptr || w_ukv == nullptr || y == nullptr)
     return KV8_EINVAL;

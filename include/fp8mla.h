@@ -168,7 +168,7 @@ int mla_wuv_epilogue(const float* o, const uint16_t* w_uv, int B, int H, int V, 
  *   slots          device int64 [T]: cache slot of token t, or NULL for slot t.
  *                  A slot outside [0, n_slots) gives a zero row and sets bit 0
  *                  of *err_word.
- *   T              tokens (>= 0).
+ *   T              tokens, 0 <= T <= 2^30.
  *   w_ukv          device bf16 bit patterns [512][N], row-major, 16-byte aligned.
  *   N              columns, a positive multiple of 256 (H x (qk_nope + v_head)).
  *   y              device bf16 [T][N], 16-byte aligned.
