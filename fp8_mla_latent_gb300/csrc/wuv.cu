@@ -12,7 +12,7 @@
 // columns), the sequences' context rows in shared memory.  When V is a multiple
 // of 8 (and the weights 16-byte aligned), thread (r, g) of 512 owns columns
 // 8g..8g+7 and the latent rows d = r, r+32, ...: one 16-byte load brings 8
-// weights, eight rows' loads in flight; the 32 row groups are then added in a
+// weights, all sixteen rows' loads in flight; the 32 row groups are then added in a
 // fixed order through shared memory.  Otherwise thread (k, v) sums half k of the
 // latent rows for column v with 2-byte loads.  The bf16 -> f32 conversion is
 // exact.
@@ -95,10 +95,15 @@ __global__ void __launch_bounds__(VT) wuv8_kernel(const float* __restrict__ o,
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
     if (v0 < V) {
-#pragma unroll 8
-      for (int d = r; d < DL; d += VR) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)d * V + v0));
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+      // all DL / VR = 16 of this thread's weight rows in flight at once
+      uint4 q[DL / VR];
+#pragma unroll
+      for (int i = 0; i < DL / VR; ++i)
+        q[i] = __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)(r + i * VR) * V + v0));
+#pragma unroll
+      for (int i = 0; i < DL / VR; ++i) {
+        const int d = r + i * VR;
+        const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
         float wf[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
