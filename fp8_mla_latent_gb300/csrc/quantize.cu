@@ -57,15 +57,16 @@ quantize_rows_kernel(const float* __restrict__ src, int64_t n_rows, int64_t stri
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (int64_t)blockIdx.x * QWARPS + (threadIdx.x >> 5);
   const int64_t n_warps = (int64_t)gridDim.x * QWARPS;
+  // the row's data is requested together with its slot (one round trip per row)
   for (int64_t r = warp_global; r < n_rows; r += n_warps) {
     const int64_t slot = dst_slot ? __ldg(&dst_slot[r]) : r;
-    if (slot < 0 || slot >= n_slots) continue;  // warp-uniform
     const float4* row = reinterpret_cast<const float4*>(src + r * stride);
     float4 L[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) L[k] = __ldcs(&row[lane * 4 + k]);
     float4 R = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane < 16) R = __ldcs(&row[128 + lane]);
+    if (slot < 0 || slot >= n_slots) continue;  // warp-uniform
 
     float aL = 0.0f, aR = 0.0f;
 #pragma unroll
@@ -119,19 +120,38 @@ produce_rows_kernel(const float* __restrict__ src, int64_t n_rows, int64_t strid
   float4 W[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) W[k] = __ldg(reinterpret_cast<const float4*>(weight) + lane * 4 + k);
-  for (int64_t r = warp_global; r < n_rows; r += n_warps) {
-    const int64_t slot = dst_slot ? __ldg(&dst_slot[r]) : r;
-    const int64_t pos = __ldg(&positions[r]);
-    if (slot < 0 || slot >= n_slots || pos < 0 || pos >= max_pos) {  // warp-uniform
-      if (lane == 0 && err != nullptr && (pos < 0 || pos >= max_pos)) atomicOr(err, 1u);
-      continue;
-    }
+  // Software pipeline: the slot and position of the next row are loaded while
+  // this row is processed, and a row's data is requested together with its
+  // rotation table entries, so each row costs one round trip to memory.
+  int64_t r = warp_global;
+  int64_t slot = 0, pos = 0;
+  if (r < n_rows) {
+    slot = dst_slot ? __ldg(&dst_slot[r]) : r;
+    pos = __ldg(&positions[r]);
+  }
+  for (; r < n_rows; r += n_warps) {
+    const bool valid = !(slot < 0 || slot >= n_slots || pos < 0 || pos >= max_pos);  // warp-uniform
+    const int64_t pc = valid ? pos : 0;
     const float4* row = reinterpret_cast<const float4*>(src + r * stride);
     float4 L[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) L[k] = __ldcs(&row[lane * 4 + k]);
     const float2 X = __ldcs(reinterpret_cast<const float2*>(src + r * stride + DL) + lane);
-    const float c = __ldg(&rope_cos[pos * (DR / 2) + lane]), sn = __ldg(&rope_sin[pos * (DR / 2) + lane]);
+    const float c = __ldg(&rope_cos[pc * (DR / 2) + lane]), sn = __ldg(&rope_sin[pc * (DR / 2) + lane]);
+    const int64_t rn = r + n_warps;
+    int64_t slot_n = 0, pos_n = 0;
+    if (rn < n_rows) {
+      slot_n = dst_slot ? __ldg(&dst_slot[rn]) : rn;
+      pos_n = __ldg(&positions[rn]);
+    }
+    const int64_t slot_c = slot;
+    slot = slot_n;
+    if (!valid) {
+      if (lane == 0 && err != nullptr && (pos < 0 || pos >= max_pos)) atomicOr(err, 1u);
+      pos = pos_n;
+      continue;
+    }
+    pos = pos_n;
 
     // RMS norm: sum of squares in the fixed order, then y = (x * inv) * w
     float ss = 0.0f;
@@ -177,10 +197,10 @@ produce_rows_kernel(const float* __restrict__ src, int64_t n_rows, int64_t strid
     cl.y = encode4(L[1], iL, gL);
     cl.z = encode4(L[2], iL, gL);
     cl.w = encode4(L[3], iL, gL);
-    uint8_t* dst = codes + slot * D;
+    uint8_t* dst = codes + slot_c * D;
     *reinterpret_cast<uint4*>(dst + lane * 16) = cl;
     *reinterpret_cast<uint16_t*>(dst + DL + lane * 2) = (uint16_t)encode2(y0, y1, iR, gR);
-    if (lane == 0) *reinterpret_cast<float2*>(scales + slot * 2) = make_float2(sL, sR);
+    if (lane == 0) *reinterpret_cast<float2*>(scales + slot_c * 2) = make_float2(sL, sR);
   }
 }
 
@@ -191,7 +211,16 @@ cudaError_t launch_quantize(const float* src, int64_t n_rows, int64_t stride,
                             int64_t n_slots, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int64_t want = (n_rows + QWARPS - 1) / QWARPS;
-  const int64_t cap = (int64_t)NUM_SMS * 8;  // 8 CTAs of 8 warps per SM: 64 rows in flight
+  // as many CTAs as are resident at once (the loop strides over the rest)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_rows_kernel, QWARPS * 32, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n < 1 ? 1 : n;
+  }
+  const int64_t cap = (int64_t)NUM_SMS * per_sm;
   const int grid = (int)(want < cap ? want : cap);
   quantize_rows_kernel<<<grid, QWARPS * 32, 0, s>>>(src, n_rows, stride, dst_slot, codes, scales,
                                                     n_slots);
@@ -209,7 +238,16 @@ cudaError_t launch_produce(const float* src, int64_t n_rows, int64_t stride, con
                           cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int64_t want = (n_rows + QWARPS - 1) / QWARPS;
-  const int64_t cap = (int64_t)NUM_SMS * 8;
+  // as many CTAs as are resident at once (the loop strides over the rest)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, produce_rows_kernel, QWARPS * 32, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = n < 1 ? 1 : n;
+  }
+  const int64_t cap = (int64_t)NUM_SMS * per_sm;
   const int grid = (int)(want < cap ? want : cap);
   produce_rows_kernel<<<grid, QWARPS * 32, 0, s>>>(src, n_rows, stride, weight, eps, positions,
                                                    rope_cos, rope_sin, max_pos, dst_slot, codes,
