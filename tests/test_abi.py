@@ -26,7 +26,8 @@ def test_header_declares_the_documented_calls():
     for want in ("kv8_quantize_rows", "kv8_produce_rows", "mla_absorb_decode_fp8",
                  "mla_absorb_decode_fp8_batch",
                  "mla_absorb_decode_fp8_workspace_size",
-                 "mla_absorb_decode_fp8_batch_workspace_size", "kv8_status_string"):
+                 "mla_absorb_decode_fp8_batch_workspace_size", "kv8_status_string",
+                 "mla_wuv_epilogue", "kv8_prefill_project", "kv8_selftest_wait_timeout"):
         assert want in names
 
 

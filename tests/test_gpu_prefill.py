@@ -97,3 +97,43 @@ def test_prefill_bad_slot_gives_zero_row_and_flag():
     ref = oracle.prefill_project(codes.cpu().numpy(), scales.cpu().numpy(),
                                  w.cpu().view(torch.int16).numpy().view(np.uint16), slots=np.arange(7))
     check(y[:7], ref)
+
+
+@pytest.mark.parametrize("T,N", [(129, 256), (257, 512), (383, 256), (640, 1024), (1100, 2560)])
+def test_prefill_ragged_pair_tiles(T, N):
+    """Token counts that end inside the first or the second 128-token half of a
+    256-token pair tile (the second CTA of the pair then holds no token, or a few),
+    through a random slot map, with the rope keys."""
+    rng = np.random.default_rng(1000 + T)
+    d = torch.device("cuda:0")
+    n_slots = 2 * T
+    codes, scales = make_cache(rng, n_slots)
+    w = weights(rng, N)
+    slots = rng.permutation(n_slots)[:T].astype(np.int64)
+    k_rope = torch.empty((T, 64), dtype=torch.float32, device=d)
+    y = torch.full((T, N), float("nan"), dtype=torch.bfloat16, device=d)
+    pkg.kv8_prefill_project(codes, scales, w.to(d), slots=torch.from_numpy(slots).to(d), y=y,
+                            k_rope=k_rope)
+    torch.cuda.synchronize()
+    c_np, s_np = codes.cpu().numpy(), scales.cpu().numpy()
+    ref = oracle.prefill_project(c_np, s_np, w.view(torch.int16).numpy().view(np.uint16), slots=slots)
+    check(y, ref)
+    kr = oracle.prefill_rope(c_np, s_np, slots)
+    assert np.array_equal(k_rope.cpu().numpy().view(np.uint32), kr.view(np.uint32))
+
+
+def test_prefill_calls_with_changing_shapes():
+    """Back-to-back calls with different token counts and widths on one stream."""
+    rng = np.random.default_rng(77)
+    d = torch.device("cuda:0")
+    codes, scales = make_cache(rng, 600)
+    c_np, s_np = codes.cpu().numpy(), scales.cpu().numpy()
+    outs = []
+    for T, N in ((600, 256), (5, 768), (300, 512)):
+        w = weights(rng, N)
+        outs.append((T, w, pkg.kv8_prefill_project(codes, scales, w.to(d), T=T)))
+    torch.cuda.synchronize()
+    for T, w, y in outs:
+        ref = oracle.prefill_project(c_np, s_np, w.view(torch.int16).numpy().view(np.uint16),
+                                     slots=np.arange(T))
+        check(y, ref)
