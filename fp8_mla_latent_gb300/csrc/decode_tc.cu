@@ -837,15 +837,16 @@ cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map) {
 template <int N>
 cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
   const int smem = Lay<N>::TOTAL + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<N>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<int> memo[MAX_DEVICES];
+  int done = 0;
+  cudaError_t e = per_device(memo, [smem](int* v) {
+    *v = 1;
+    return cudaFuncSetAttribute(decode_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
+  }, &done);
+  if (e != cudaSuccess) return e;
   CUtensorMap map;
-  const cudaError_t e = make_cache_map(a, &map);
+  e = make_cache_map(a, &map);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, smem, s>>>(a, map);
   return cudaGetLastError();

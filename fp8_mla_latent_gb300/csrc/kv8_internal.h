@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kv8 {
 
 constexpr int DL = 512;    // kv_lora latent width
@@ -55,6 +57,28 @@ struct DecodeArgs {
   float* ws_o;                 // [max_items][hg][512] unnormalised context
   SplitPlan plan;
 };
+
+// A launch setting that belongs to the current device (a kernel's shared-memory
+// opt-in, an occupancy figure): `make(&v)` computes it (v > 0) the first time a
+// device asks; later calls on that device return the stored value.  Settings are
+// per device (cudaFuncSetAttribute applies to the current device only), and
+// concurrent first calls just compute the same value twice.
+constexpr int MAX_DEVICES = 64;
+template <typename F>
+inline cudaError_t per_device(std::atomic<int> (&memo)[MAX_DEVICES], F&& make, int* value) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return make(value);
+  int v = memo[dev].load(std::memory_order_acquire);
+  if (v <= 0) {
+    e = make(&v);
+    if (e != cudaSuccess) return e;
+    memo[dev].store(v, std::memory_order_release);
+  }
+  *value = v;
+  return cudaSuccess;
+}
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);

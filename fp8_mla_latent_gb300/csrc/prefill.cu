@@ -401,22 +401,24 @@ cudaError_t launch_prefill(const uint8_t* codes, const float* scales, const int6
                            float* k_rope, unsigned* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   // pairs that can be resident at once: the work is cut into that many ranges
-  static int max_pairs = 0;
-  if (max_pairs == 0) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
+  static std::atomic<int> memo[MAX_DEVICES];
+  int max_pairs = 0;
+  cudaError_t e = per_device(memo, [](int* v) {
+    cudaError_t r = cudaFuncSetAttribute(prefill_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
+    if (r != cudaSuccess) return r;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(NUM_SMS, 1, 1);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    max_pairs = n < 1 ? 1 : (n > NUM_SMS / 2 ? NUM_SMS / 2 : n);
-  }
+    r = cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg);
+    *v = n < 1 ? 1 : (n > NUM_SMS / 2 ? NUM_SMS / 2 : n);
+    return r;
+  }, &max_pairs);
+  if (e != cudaSuccess) return e;
   CUtensorMap wmap, ymap;
-  cudaError_t e = make_map(w, N, PT_K, KS, &wmap);
+  e = make_map(w, N, PT_K, KS, &wmap);
   if (e != cudaSuccess) return e;
   e = make_map(y, N, T, 32, &ymap);
   if (e != cudaSuccess) return e;

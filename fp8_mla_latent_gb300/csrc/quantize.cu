@@ -212,14 +212,15 @@ cudaError_t launch_quantize(const float* src, int64_t n_rows, int64_t stride,
   if (n_rows == 0) return cudaSuccess;
   const int64_t want = (n_rows + QWARPS - 1) / QWARPS;
   // as many CTAs as are resident at once (the loop strides over the rest)
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static std::atomic<int> memo[MAX_DEVICES];
+  int per_sm = 0;
+  const cudaError_t e = per_device(memo, [](int* v) {
     int n = 0;
-    const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_rows_kernel, QWARPS * 32, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = n < 1 ? 1 : n;
-  }
+    const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_rows_kernel, QWARPS * 32, 0);
+    *v = n < 1 ? 1 : n;
+    return r;
+  }, &per_sm);
+  if (e != cudaSuccess) return e;
   const int64_t cap = (int64_t)NUM_SMS * per_sm;
   const int grid = (int)(want < cap ? want : cap);
   quantize_rows_kernel<<<grid, QWARPS * 32, 0, s>>>(src, n_rows, stride, dst_slot, codes, scales,
@@ -239,14 +240,15 @@ cudaError_t launch_produce(const float* src, int64_t n_rows, int64_t stride, con
   if (n_rows == 0) return cudaSuccess;
   const int64_t want = (n_rows + QWARPS - 1) / QWARPS;
   // as many CTAs as are resident at once (the loop strides over the rest)
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static std::atomic<int> memo[MAX_DEVICES];
+  int per_sm = 0;
+  const cudaError_t e = per_device(memo, [](int* v) {
     int n = 0;
-    const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, produce_rows_kernel, QWARPS * 32, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = n < 1 ? 1 : n;
-  }
+    const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, produce_rows_kernel, QWARPS * 32, 0);
+    *v = n < 1 ? 1 : n;
+    return r;
+  }, &per_sm);
+  if (e != cudaSuccess) return e;
   const int64_t cap = (int64_t)NUM_SMS * per_sm;
   const int grid = (int)(want < cap ? want : cap);
   produce_rows_kernel<<<grid, QWARPS * 32, 0, s>>>(src, n_rows, stride, weight, eps, positions,

@@ -145,13 +145,13 @@ cudaError_t launch_wuv(const float* o, const uint16_t* w, int B, int H, int V, f
   if (B == 0) return cudaSuccess;
   dim3 grid(H, (V + 127) / 128);
   if (V % 8 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
-    static bool configured = false;
-    if (!configured) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(wuv8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, V8_SMEM);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static std::atomic<int> memo[MAX_DEVICES];
+    int done = 0;
+    const cudaError_t e = per_device(memo, [](int* v) {
+      *v = 1;
+      return cudaFuncSetAttribute(wuv8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, V8_SMEM);
+    }, &done);
+    if (e != cudaSuccess) return e;
     wuv8_kernel<<<grid, VT, V8_SMEM, s>>>(o, w, B, H, V, y);
   }
   else
