@@ -82,6 +82,26 @@ def traffic_for(kernel, workload):
     return float(d["bytes_per_launch"])
 
 
+def rank_sync():
+    """Barrier across the ranks of a torchrun launch (no-op in a single process)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def slowest_rank(values, device):
+    """Each timing's maximum over the ranks (the values themselves in a single
+    process): replicas report the whole job's throughput at the slowest rank's pace."""
+    import torch
+    import torch.distributed as dist
+    vals = [float(v) for v in values]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return vals
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -257,10 +277,7 @@ def run_ours(args, rank, world, local_rank):
     d2h = out_h.numel() * 4
 
     # ---- max over ranks
-    t = torch.tensor([ms_step, ms_dec, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step, ms_dec, e2e_ms = (float(x) for x in t.tolist())
+    ms_step, ms_dec, e2e_ms = slowest_rank([ms_step, ms_dec, e2e_ms], dev)
     if rank != 0:
         return None
 
@@ -350,6 +367,7 @@ def run_produce(args, rank, world, local_rank):
         flush.zero_()
         once()
     torch.cuda.synchronize()
+    rank_sync()
     sampler = ClockSampler(local_rank)
     sampler.start()
     times = []
@@ -362,12 +380,8 @@ def run_produce(args, rank, world, local_rank):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     clocks = sampler.stop()
-    ms = float(np.mean(times))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    rank_sync()
+    ms, = slowest_rank([float(np.mean(times))], dev)
     nbytes = n * PRODUCE_ROW_BYTES
     value = world * nbytes / (ms * 1e-3) / 1e9
     # end to end: raw rows from pinned host memory, error word back
@@ -386,7 +400,7 @@ def run_produce(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e.append(e0.elapsed_time(e1))
-    e2e_ms = float(np.mean(e2e))
+    e2e_ms, = slowest_rank([float(np.mean(e2e))], dev)
     peaks = load_peaks()
     achieved = nbytes / (ms * 1e-3) / 1e9
     res = {
@@ -434,6 +448,7 @@ def run_wuv(args, rank, world, local_rank):
         flush.zero_()
         pkg.mla_wuv_epilogue(o, w, y)
     torch.cuda.synchronize()
+    rank_sync()
     times = []
     for _ in range(args.steps):
         flush.zero_()
@@ -443,7 +458,8 @@ def run_wuv(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
-    ms = float(np.mean(times))
+    rank_sync()
+    ms, = slowest_rank([float(np.mean(times))], dev)
     nbytes = H * 512 * V * 2 + B * H * 512 * 4 + B * H * V * 4
     peaks = load_peaks()
     achieved = nbytes / (ms * 1e-3) / 1e9
@@ -502,6 +518,7 @@ def run_prefill(args, rank, world, local_rank):
         flush.zero_()
         once()
     torch.cuda.synchronize()
+    rank_sync()
     sampler = ClockSampler(local_rank)
     sampler.start()
     times = []
@@ -515,12 +532,8 @@ def run_prefill(args, rank, world, local_rank):
         times.append(e0.elapsed_time(e1))
     clocks = sampler.stop()
     assert err.item() == 0, f"prefill error word {err.item()}"
-    ms = float(np.mean(times))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    rank_sync()
+    ms, = slowest_rank([float(np.mean(times))], dev)
     flops = 2.0 * T * 512 * N
     tflops = flops / (ms * 1e-3) / 1e12
     # end to end: the chunk's cache rows and slot map from pinned host memory, Y and
@@ -546,7 +559,7 @@ def run_prefill(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e.append(e0.elapsed_time(e1))
-    e2e_ms = float(np.mean(e2e))
+    e2e_ms, = slowest_rank([float(np.mean(e2e))], dev)
     peaks = load_peaks()
     nbytes = prefill_bytes(T, N)
     res = {
