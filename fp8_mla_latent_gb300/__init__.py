@@ -6,7 +6,7 @@ declared in ``include/fp8mla.h``); this package holds its in-tree build step
 synthetic workloads (``workloads``).
 """
 from ._lib import (KV8_BLOCK, KV8_D, KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05,
-                   KV8_DL, KV8_DR, Kv8Error, alloc_workspace, kv8_prefill_project, kv8_produce_rows, kv8_quantize_rows,
+                   KV8_DL, KV8_DR, Kv8Disk, Kv8Error, alloc_workspace, kv8_prefill_project, kv8_produce_rows, kv8_quantize_rows,
                    kv8_selftest_wait_timeout,
                    kv8_workspace_error, lib, library_path, mla_absorb_decode_fp8,
                    mla_absorb_decode_fp8_batch, mla_absorb_decode_fp8_batch_combine,
@@ -16,7 +16,7 @@ from ._lib import (KV8_BLOCK, KV8_D, KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECOD
 
 __all__ = [
     "KV8_BLOCK", "KV8_D", "KV8_DECODE_AUTO", "KV8_DECODE_SIMT", "KV8_DECODE_TCGEN05", "KV8_DL",
-    "KV8_DR", "Kv8Error", "alloc_workspace", "kv8_prefill_project", "kv8_produce_rows", "kv8_quantize_rows",
+    "KV8_DR", "Kv8Disk", "Kv8Error", "alloc_workspace", "kv8_prefill_project", "kv8_produce_rows", "kv8_quantize_rows",
     "kv8_selftest_wait_timeout", "kv8_workspace_error", "lib",
     "library_path", "mla_absorb_decode_fp8", "mla_absorb_decode_fp8_batch",
     "mla_absorb_decode_fp8_batch_combine", "mla_absorb_decode_fp8_batch_noalloc",

@@ -20,7 +20,7 @@ KV8_DL, KV8_DR, KV8_D, KV8_BLOCK = 512, 64, 576, 64
 KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05 = 0, 1, 2
 STATUS = {0: "KV8_OK", -1: "KV8_EINVAL", -2: "KV8_EALIGN", -3: "KV8_EUNSUPPORTED",
           -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE", -7: "KV8_ETIMEOUT",
-          -8: "KV8_ESCRATCH"}
+          -8: "KV8_ESCRATCH", -9: "KV8_EIO", -10: "KV8_EFORMAT"}
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +62,11 @@ def lib() -> ctypes.CDLL:
                                                               i64, f32, P, P, i32, P]),
                 "kv8_noalloc_error": (i32, [P]),
                 "kv8_workspace_error": (i32, [P, P]),
+                "kv8_disk_open": (i32, [ctypes.c_char_p, i64, ctypes.POINTER(P)]),
+                "kv8_disk_info": (i32, [P, ctypes.POINTER(i64), ctypes.POINTER(i32)]),
+                "kv8_disk_append": (i32, [P, P, P, i64, P, i64, P]),
+                "kv8_disk_load": (i32, [P, i64, i64, P, P, i64, P, P]),
+                "kv8_disk_close": (i32, [P]),
                 "kv8_status_string": (ctypes.c_char_p, [i32]),
                 "kv8_abi_version": (i32, []),
             }
@@ -344,3 +349,59 @@ def mla_absorb_decode_fp8_batch_noalloc(q_lat, q_rope, kv_codes, kv_scales, bloc
         _stream(stream))
     _check("mla_absorb_decode_fp8_batch_noalloc", st)
     return out
+
+
+# ----------------------------------------------------------------- cache file
+class Kv8Disk:
+    """An open cache file (the kv8_disk_* calls): save rows of a device cache to it,
+    load them back.  Use as a context manager or call close()."""
+
+    def __init__(self, path: str, staging_rows: int = 4096):
+        h = ctypes.c_void_p()
+        _check("kv8_disk_open", lib().kv8_disk_open(os.fsencode(path), int(staging_rows),
+                                                    ctypes.byref(h)))
+        self._h = h
+
+    def info(self):
+        """(committed rows, version)."""
+        n, v = ctypes.c_int64(), ctypes.c_int()
+        _check("kv8_disk_info", lib().kv8_disk_info(self._h, ctypes.byref(n), ctypes.byref(v)))
+        return n.value, v.value
+
+    def append(self, kv_codes, kv_scales, slots=None, n=None, stream=None):
+        """Append the cache rows at device slots (int64 [n]) or slots 0..n-1."""
+        _need(kv_codes, "kv_codes", torch.uint8, 2)
+        _need(kv_scales, "kv_scales", torch.float32, 2)
+        if slots is not None:
+            _need(slots, "slots", torch.int64, 1)
+            n = slots.numel()
+        elif n is None:
+            n = kv_codes.shape[0]
+        _check("kv8_disk_append", lib().kv8_disk_append(self._h, _ptr(kv_codes), _ptr(kv_scales),
+                                                        kv_codes.shape[0], _ptr(slots), int(n),
+                                                        _stream(stream)))
+
+    def load(self, kv_codes, kv_scales, first_row=0, n=None, dst_slot=None, stream=None):
+        """Load committed rows [first_row, first_row + n) into the cache at device
+        dst_slot (int64 [n]) or slots first_row + i."""
+        _need(kv_codes, "kv_codes", torch.uint8, 2)
+        _need(kv_scales, "kv_scales", torch.float32, 2)
+        if dst_slot is not None:
+            _need(dst_slot, "dst_slot", torch.int64, 1)
+            n = dst_slot.numel()
+        elif n is None:
+            n = self.info()[0] - first_row
+        _check("kv8_disk_load", lib().kv8_disk_load(self._h, int(first_row), int(n), _ptr(kv_codes),
+                                                    _ptr(kv_scales), kv_codes.shape[0],
+                                                    _ptr(dst_slot), _stream(stream)))
+
+    def close(self):
+        if self._h is not None and self._h.value is not None:
+            _check("kv8_disk_close", lib().kv8_disk_close(self._h))
+        self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

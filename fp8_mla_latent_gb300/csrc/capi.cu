@@ -101,6 +101,8 @@ const char* kv8_status_string(int status) {
     case KV8_EWORKSPACE: return "workspace missing or too small";
     case KV8_ETIMEOUT: return "device-side wait timed out";
     case KV8_ESCRATCH: return "problem needs more scratch than the static no-alloc buffer";
+    case KV8_EIO: return "cache file read, write or rename failed";
+    case KV8_EFORMAT: return "not a cache file, or shorter than its committed rows";
     default: return "unknown status";
   }
 }

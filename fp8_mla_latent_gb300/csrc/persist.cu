@@ -1,0 +1,350 @@
+// persist.cu -- save and resume of the fp8 cache through a cache file.
+//
+// KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"), PR
+// description, persistence item: version 2 of the cache file starts with the
+// magic COLIKV2 and records its data type in its header; its rows are the fp8
+// codes with their scales; rows are appended through a persistent handle with a
+// staging buffer; a version-1 file (f32 rows) is quantized on resume and
+// rewritten as version 2 at the first append; opening repairs a damaged magic.
+// The byte layout (the page gives none) is stated in fp8mla.h.
+//
+// A handle owns the open file and a pinned, device-mapped host staging buffer.
+// Append: a gather kernel packs the rows of the requested cache slots into
+// 584-byte records straight into the staging buffer (over the host link), the
+// host writes them after the last committed record, and only then rewrites the
+// header's row count, so a torn append is never part of the file.  Load: the
+// host reads records into the staging buffer and a scatter kernel puts them into
+// cache slots; version-1 rows go through the library's quantizer instead.
+#include <errno.h>
+#include <stdio.h>
+#include <string.h>
+#include <sys/stat.h>
+#include <unistd.h>
+
+#include <string>
+
+#include "fp8mla.h"
+#include "kv8_internal.h"
+
+namespace kv8 {
+namespace {
+
+constexpr int HDR = 64;
+constexpr int REC2 = D + 8;      // version-2 record: codes, then sLc and sRc
+constexpr int REC1 = D * 4;      // version-1 record: 576 f32
+constexpr int STAGE_ROW = REC1 + D + 8;  // f32 rows (or records) + codes + scales per staged row
+const char MAGIC2[8] = {'C', 'O', 'L', 'I', 'K', 'V', '2', 0};
+const char MAGIC1[8] = {'C', 'O', 'L', 'I', 'K', 'V', '1', 0};
+
+// One warp per record; a record is 73 eight-byte words (72 of codes, 1 of scales).
+__global__ void gather_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                              int64_t n_slots, const int64_t* __restrict__ slots, int64_t first,
+                              int64_t n, uint8_t* __restrict__ rec, int* flag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (i >= n) return;
+  const int64_t slot = slots != nullptr ? slots[i] : first + i;
+  uint64_t* dst = reinterpret_cast<uint64_t*>(rec + i * REC2);
+  if (slot < 0 || slot >= n_slots) {
+    for (int k = lane; k < REC2 / 8; k += 32) dst[k] = 0;
+    if (lane == 0) *reinterpret_cast<volatile int*>(flag) = 1;
+    return;
+  }
+  const uint64_t* src = reinterpret_cast<const uint64_t*>(codes + slot * D);
+  for (int k = lane; k < D / 8; k += 32) dst[k] = src[k];
+  if (lane == 0) dst[D / 8] = *reinterpret_cast<const uint64_t*>(scales + slot * 2);
+}
+
+__global__ void scatter_kernel(const uint8_t* __restrict__ rec, int64_t n, uint8_t* __restrict__ codes,
+                               float* __restrict__ scales, int64_t n_slots,
+                               const int64_t* __restrict__ slots, int64_t first, int* flag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (i >= n) return;
+  const int64_t slot = slots != nullptr ? slots[i] : first + i;
+  if (slot < 0 || slot >= n_slots) {
+    if (lane == 0) *reinterpret_cast<volatile int*>(flag) = 1;
+    return;
+  }
+  const uint64_t* src = reinterpret_cast<const uint64_t*>(rec + i * REC2);
+  uint64_t* dst = reinterpret_cast<uint64_t*>(codes + slot * D);
+  for (int k = lane; k < D / 8; k += 32) dst[k] = src[k];
+  if (lane == 0) *reinterpret_cast<uint64_t*>(scales + slot * 2) = src[D / 8];
+}
+
+__global__ void check_slots_kernel(const int64_t* __restrict__ slots, int64_t n, int64_t n_slots,
+                                   int* flag) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n && (slots[i] < 0 || slots[i] >= n_slots)) *reinterpret_cast<volatile int*>(flag) = 1;
+}
+
+void put_u32(uint8_t* p, uint32_t v) { memcpy(p, &v, 4); }
+void put_u64(uint8_t* p, uint64_t v) { memcpy(p, &v, 8); }
+uint32_t get_u32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
+uint64_t get_u64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
+
+void make_header(uint8_t* h, int version, int64_t n_rows) {
+  memset(h, 0, HDR);
+  memcpy(h, version == 2 ? MAGIC2 : MAGIC1, 8);
+  put_u32(h + 8, HDR);
+  put_u32(h + 12, version == 2 ? 2u : 1u);
+  put_u32(h + 16, D);
+  put_u32(h + 20, version == 2 ? REC2 : REC1);
+  put_u64(h + 24, (uint64_t)n_rows);
+}
+
+// Version of a header from its fields after the magic (0 if they fit neither).
+int version_of_fields(const uint8_t* h) {
+  if (get_u32(h + 8) != HDR || get_u32(h + 16) != D) return 0;
+  if (get_u32(h + 12) == 2 && get_u32(h + 20) == REC2) return 2;
+  if (get_u32(h + 12) == 1 && get_u32(h + 20) == REC1) return 1;
+  return 0;
+}
+
+bool write_at(FILE* f, int64_t off, const void* p, size_t n) {
+  if (fseeko(f, (off_t)off, SEEK_SET) != 0) return false;
+  return n == 0 || fwrite(p, 1, n, f) == n;
+}
+bool read_at(FILE* f, int64_t off, void* p, size_t n) {
+  if (fseeko(f, (off_t)off, SEEK_SET) != 0) return false;
+  return n == 0 || fread(p, 1, n, f) == n;
+}
+
+}  // namespace
+}  // namespace kv8
+
+using namespace kv8;
+
+struct kv8_disk {
+  FILE* f = nullptr;
+  std::string path;
+  int version = 2;
+  int64_t n_rows = 0;
+  int64_t staging_rows = 0;
+  uint8_t* stage = nullptr;   // pinned, mapped: staging_rows x STAGE_ROW bytes
+  uint8_t* stage_dev = nullptr;
+  int* flag = nullptr;        // pinned, mapped: set by the kernels on a bad slot
+  int* flag_dev = nullptr;
+};
+
+namespace {
+
+// the three areas of the staging buffer (host and device views)
+uint8_t* area_rows(kv8_disk* d, bool dev) { return dev ? d->stage_dev : d->stage; }
+uint8_t* area_codes(kv8_disk* d, bool dev) {
+  return (dev ? d->stage_dev : d->stage) + d->staging_rows * REC1;
+}
+float* area_scales(kv8_disk* d, bool dev) {
+  return reinterpret_cast<float*>((dev ? d->stage_dev : d->stage) + d->staging_rows * (REC1 + D));
+}
+
+int commit_rows(kv8_disk* d, int64_t n_rows) {
+  uint8_t h[HDR];
+  make_header(h, d->version, n_rows);
+  if (!write_at(d->f, 0, h, HDR) || fflush(d->f) != 0) return KV8_EIO;
+  d->n_rows = n_rows;
+  return KV8_OK;
+}
+
+// Version 1 -> 2: quantize the f32 rows chunk by chunk with the library's
+// quantizer into a new file beside the old one, then replace it.
+int convert_to_v2(kv8_disk* d, cudaStream_t s) {
+  const std::string tmp = d->path + ".v2tmp";
+  FILE* g = fopen(tmp.c_str(), "w+b");
+  if (g == nullptr) return KV8_EIO;
+  uint8_t h[HDR];
+  make_header(h, 2, 0);
+  int st = fwrite(h, 1, HDR, g) == HDR ? KV8_OK : KV8_EIO;
+  for (int64_t r0 = 0; st == KV8_OK && r0 < d->n_rows; r0 += d->staging_rows) {
+    const int64_t m = (d->n_rows - r0) < d->staging_rows ? (d->n_rows - r0) : d->staging_rows;
+    if (!read_at(d->f, HDR + r0 * REC1, area_rows(d, false), (size_t)(m * REC1))) { st = KV8_EIO; break; }
+    if (launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
+                        area_codes(d, true), area_scales(d, true), m, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      st = KV8_ECUDA;
+      break;
+    }
+    // interleave codes and scales into records over the (now free) f32 area
+    uint8_t* rec = area_rows(d, false);
+    const uint8_t* c = area_codes(d, false);
+    const float* sc = area_scales(d, false);
+    for (int64_t i = 0; i < m; ++i) {
+      memcpy(rec + i * REC2, c + i * D, D);
+      memcpy(rec + i * REC2 + D, sc + i * 2, 8);
+    }
+    if (fwrite(rec, 1, (size_t)(m * REC2), g) != (size_t)(m * REC2)) st = KV8_EIO;
+  }
+  if (st == KV8_OK) {
+    make_header(h, 2, d->n_rows);
+    if (!write_at(g, 0, h, HDR) || fflush(g) != 0 || fsync(fileno(g)) != 0) st = KV8_EIO;
+  }
+  if (fclose(g) != 0 && st == KV8_OK) st = KV8_EIO;
+  if (st != KV8_OK) {
+    remove(tmp.c_str());
+    return st;
+  }
+  fclose(d->f);
+  d->f = nullptr;
+  if (rename(tmp.c_str(), d->path.c_str()) != 0) return KV8_EIO;
+  d->f = fopen(d->path.c_str(), "r+b");
+  if (d->f == nullptr) return KV8_EIO;
+  d->version = 2;
+  return KV8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv8_disk_open(const char* path, int64_t staging_rows, kv8_disk** out) {
+  if (out == nullptr) return KV8_EINVAL;
+  *out = nullptr;
+  if (path == nullptr || path[0] == 0 || staging_rows < 1 || staging_rows > (int64_t)1 << 22)
+    return KV8_EINVAL;
+  kv8_disk* d = new kv8_disk();
+  d->path = path;
+  d->staging_rows = staging_rows;
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, (size_t)(staging_rows * STAGE_ROW) + 64, cudaHostAllocMapped) != cudaSuccess) {
+    delete d;
+    return KV8_ECUDA;
+  }
+  d->stage = static_cast<uint8_t*>(p);
+  d->flag = reinterpret_cast<int*>(d->stage + staging_rows * STAGE_ROW);
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, p, 0) != cudaSuccess) {
+    cudaFreeHost(p);
+    delete d;
+    return KV8_ECUDA;
+  }
+  d->stage_dev = static_cast<uint8_t*>(dp);
+  d->flag_dev = reinterpret_cast<int*>(d->stage_dev + staging_rows * STAGE_ROW);
+
+  int st = KV8_OK;
+  d->f = fopen(path, "r+b");
+  if (d->f == nullptr && errno == ENOENT) d->f = fopen(path, "w+b");
+  if (d->f == nullptr) st = KV8_EIO;
+  uint8_t h[HDR];
+  size_t got = 0;
+  if (st == KV8_OK) {
+    if (fseeko(d->f, 0, SEEK_SET) != 0) st = KV8_EIO;
+    else got = fread(h, 1, HDR, d->f);
+  }
+  if (st == KV8_OK && got < (size_t)HDR) {
+    // empty or torn at creation: a fresh version-2 file
+    if (ftruncate(fileno(d->f), 0) != 0) st = KV8_EIO;
+    else {
+      d->version = 2;
+      st = commit_rows(d, 0);
+    }
+  } else if (st == KV8_OK) {
+    const int v = version_of_fields(h);
+    if (v == 0) {
+      st = KV8_EFORMAT;
+    } else {
+      d->version = v;
+      d->n_rows = (int64_t)get_u64(h + 24);
+      if (memcmp(h, v == 2 ? MAGIC2 : MAGIC1, 8) != 0) st = commit_rows(d, d->n_rows);  // repair the magic
+      struct stat sb;
+      if (st == KV8_OK && (fstat(fileno(d->f), &sb) != 0 || d->n_rows < 0 ||
+                           (int64_t)sb.st_size < HDR + d->n_rows * (v == 2 ? REC2 : REC1)))
+        st = KV8_EFORMAT;  // fewer bytes than the committed rows
+    }
+  }
+  if (st != KV8_OK) {
+    kv8_disk_close(d);
+    return st;
+  }
+  *out = d;
+  return KV8_OK;
+}
+
+int kv8_disk_info(const kv8_disk* d, int64_t* n_rows, int* version) {
+  if (d == nullptr) return KV8_EINVAL;
+  if (n_rows != nullptr) *n_rows = d->n_rows;
+  if (version != nullptr) *version = d->version;
+  return KV8_OK;
+}
+
+int kv8_disk_append(kv8_disk* d, const uint8_t* kv_codes, const float* kv_scales, int64_t n_slots,
+                    const int64_t* slots, int64_t n, void* stream) {
+  if (d == nullptr || n < 0 || n_slots < 0) return KV8_EINVAL;
+  if (n == 0) return KV8_OK;
+  if (kv_codes == nullptr || kv_scales == nullptr) return KV8_EINVAL;
+  if (slots == nullptr && n > n_slots) return KV8_EINVAL;
+  if (((uintptr_t)kv_codes & 15) || ((uintptr_t)kv_scales & 7) || ((uintptr_t)slots & 7))
+    return KV8_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d->version == 1) {
+    const int st = convert_to_v2(d, s);
+    if (st != KV8_OK) return st;
+  }
+  for (int64_t r0 = 0; r0 < n; r0 += d->staging_rows) {
+    const int64_t m = (n - r0) < d->staging_rows ? (n - r0) : d->staging_rows;
+    *reinterpret_cast<volatile int*>(d->flag) = 0;
+    const int64_t threads = m * 32;
+    gather_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        kv_codes, kv_scales, n_slots, slots != nullptr ? slots + r0 : nullptr, r0, m,
+        area_rows(d, true), d->flag_dev);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+    if (*reinterpret_cast<volatile int*>(d->flag) != 0) return KV8_EBOUNDS;  // nothing committed
+    if (!write_at(d->f, HDR + (d->n_rows + r0) * REC2, area_rows(d, false), (size_t)(m * REC2)))
+      return KV8_EIO;
+  }
+  if (fflush(d->f) != 0) return KV8_EIO;
+  return commit_rows(d, d->n_rows + n);
+}
+
+int kv8_disk_load(kv8_disk* d, int64_t first_row, int64_t n, uint8_t* kv_codes, float* kv_scales,
+                  int64_t n_slots, const int64_t* dst_slot, void* stream) {
+  if (d == nullptr || n < 0 || first_row < 0 || n_slots < 0) return KV8_EINVAL;
+  if (first_row + n > d->n_rows) return KV8_EINVAL;
+  if (n == 0) return KV8_OK;
+  if (kv_codes == nullptr || kv_scales == nullptr) return KV8_EINVAL;
+  if (dst_slot == nullptr && first_row + n > n_slots) return KV8_EINVAL;
+  if (((uintptr_t)kv_codes & 15) || ((uintptr_t)kv_scales & 7) || ((uintptr_t)dst_slot & 7))
+    return KV8_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t r0 = 0; r0 < n; r0 += d->staging_rows) {
+    const int64_t m = (n - r0) < d->staging_rows ? (n - r0) : d->staging_rows;
+    const int64_t row = first_row + r0;
+    const int64_t* sl = dst_slot != nullptr ? dst_slot + r0 : nullptr;
+    *reinterpret_cast<volatile int*>(d->flag) = 0;
+    if (d->version == 2) {
+      if (!read_at(d->f, HDR + row * REC2, area_rows(d, false), (size_t)(m * REC2))) return KV8_EIO;
+      const int64_t threads = m * 32;
+      scatter_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+          area_rows(d, true), m, kv_codes, kv_scales, n_slots, sl, row, d->flag_dev);
+      if (cudaGetLastError() != cudaSuccess) return KV8_ECUDA;
+    } else {
+      if (!read_at(d->f, HDR + row * REC1, area_rows(d, false), (size_t)(m * REC1))) return KV8_EIO;
+      // version 1: the rows are quantized on the way in (identity slots start at `row`;
+      // the quantizer skips a slot outside the pool, which the check reports)
+      if (sl != nullptr) {
+        check_slots_kernel<<<(unsigned)((m + 255) / 256), 256, 0, s>>>(sl, m, n_slots, d->flag_dev);
+        if (cudaGetLastError() != cudaSuccess) return KV8_ECUDA;
+      }
+      const cudaError_t e =
+          sl != nullptr
+              ? launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, sl,
+                                kv_codes, kv_scales, n_slots, s)
+              : launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
+                                kv_codes + row * D, kv_scales + row * 2, n_slots - row, s);
+      if (e != cudaSuccess) return KV8_ECUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+    if (*reinterpret_cast<volatile int*>(d->flag) != 0) return KV8_EBOUNDS;
+  }
+  return KV8_OK;
+}
+
+int kv8_disk_close(kv8_disk* d) {
+  if (d == nullptr) return KV8_OK;
+  int st = KV8_OK;
+  if (d->f != nullptr && fclose(d->f) != 0) st = KV8_EIO;
+  if (d->stage != nullptr) cudaFreeHost(d->stage);
+  delete d;
+  return st;
+}
+
+}  // extern "C"

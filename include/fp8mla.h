@@ -49,7 +49,9 @@ typedef enum {
     KV8_EBOUNDS = -5,       /* a device-side index (block table, seq_len) was bad    */
     KV8_EWORKSPACE = -6,    /* workspace missing or smaller than *_workspace_size    */
     KV8_ETIMEOUT = -7,      /* a bounded device-side wait gave up (internal error)   */
-    KV8_ESCRATCH = -8       /* problem too large for the library's static scratch    */
+    KV8_ESCRATCH = -8,      /* problem too large for the library's static scratch    */
+    KV8_EIO = -9,           /* a cache-file read, write or rename failed             */
+    KV8_EFORMAT = -10       /* not a cache file, or shorter than its committed rows  */
 } kv8_status;
 
 /* Decode kernel choice.  Both accumulate in f32.  Tolerance classes, as max-abs
@@ -332,6 +334,58 @@ const char* kv8_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */
 int kv8_abi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Cache file: save and resume of the fp8 cache (KV8 page, PR description,
+ * persistence item: version 2 starts with the magic COLIKV2 and keeps its data
+ * type in the header; rows are the fp8 codes with their scales, appended through
+ * a persistent handle with a staging buffer; a version-1 file (f32 rows) is
+ * quantized on resume and rewritten as version 2 at the first append; opening
+ * repairs a damaged magic).  Byte layout (the page gives none), little-endian:
+ *   header, 64 bytes: [0,8) magic "COLIKV2\0" (version 1: "COLIKV1\0");
+ *     [8,12) u32 64 (header bytes); [12,16) u32 data type, 2 = e4m3 codes + two
+ *     f32 scales, 1 = f32 values; [16,20) u32 576 (values per row); [20,24) u32
+ *     bytes per record, 584 or 2304; [24,32) u64 rows committed; [32,64) zero.
+ *   then the committed records: version 2: 576 code bytes, then sLc and sRc
+ *     (f32); version 1: 576 f32.  Bytes after the last committed record (a torn
+ *     append) are not content and are overwritten by the next append.
+ * A handle is used by one host thread at a time.  Appends and loads are
+ * synchronous: they synchronize `stream` and return when the file or the cache
+ * holds the rows.
+ * ------------------------------------------------------------------------- */
+typedef struct kv8_disk kv8_disk;
+
+/* Open (or create) the file at `path`.  A missing, empty or shorter-than-a-header
+ * file becomes an empty version-2 file; a header whose fields after the magic are
+ * a valid version-1 or version-2 header gets its magic rewritten.  The handle
+ * owns a pinned, device-mapped host staging buffer of staging_rows x 2888 bytes
+ * (1 <= staging_rows <= 2^22); it holds no device memory.
+ * Errors: KV8_EINVAL, KV8_ECUDA (staging buffer), KV8_EIO, KV8_EFORMAT (a
+ * header of neither version, or fewer bytes than the committed rows). */
+int kv8_disk_open(const char* path, int64_t staging_rows, kv8_disk** out);
+
+/* Committed rows and version (1 or 2) of an open file. */
+int kv8_disk_info(const kv8_disk* d, int64_t* n_rows, int* version);
+
+/* Append n rows taken from the cache (kv_codes [n_slots][576], 16-byte aligned;
+ * kv_scales [n_slots][2]) at device slots[i] (int64, or NULL for slots 0..n-1).
+ * A version-1 file is first rewritten as version 2.  The row count in the header
+ * is rewritten only after the records are written.  A slot outside [0, n_slots)
+ * gives KV8_EBOUNDS and commits nothing.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_EBOUNDS, KV8_ECUDA, KV8_EIO. */
+int kv8_disk_append(kv8_disk* d, const uint8_t* kv_codes, const float* kv_scales, int64_t n_slots,
+                    const int64_t* slots, int64_t n, void* stream);
+
+/* Load committed rows [first_row, first_row + n) into the cache at device
+ * dst_slot[i] (int64, or NULL for slots first_row + i).  Version-1 rows are
+ * quantized on the way in (the same codes as kv8_quantize_rows).  A row whose
+ * slot is outside [0, n_slots) is not written and the call returns KV8_EBOUNDS.
+ * Errors: KV8_EINVAL, KV8_EALIGN, KV8_EBOUNDS, KV8_ECUDA, KV8_EIO. */
+int kv8_disk_load(kv8_disk* d, int64_t first_row, int64_t n, uint8_t* kv_codes, float* kv_scales,
+                  int64_t n_slots, const int64_t* dst_slot, void* stream);
+
+/* Close the file and free the staging buffer (NULL is accepted). */
+int kv8_disk_close(kv8_disk* d);
 
 #ifdef __cplusplus
 }

@@ -187,3 +187,19 @@ def test_prefill_rejects_bad_arguments_on_host():
     assert call(a8=P(g + 8)) == EALIGN      # k_rope
     assert call(a9=P(g + 2)) == EALIGN      # err_word
     assert call(a4=0, a0=None) == 0
+
+
+def test_disk_rejects_bad_arguments_on_host():
+    L = pkg.lib()
+    h = ctypes.c_void_p()
+    assert L.kv8_disk_open(None, 16, ctypes.byref(h)) == EINVAL
+    assert L.kv8_disk_open(b"", 16, ctypes.byref(h)) == EINVAL
+    assert L.kv8_disk_open(b"/tmp/x.kv", 0, ctypes.byref(h)) == EINVAL
+    assert L.kv8_disk_open(b"/tmp/x.kv", 1 << 23, ctypes.byref(h)) == EINVAL
+    assert L.kv8_disk_open(b"/tmp/x.kv", 16, None) == EINVAL
+    n = ctypes.c_int64()
+    assert L.kv8_disk_info(None, ctypes.byref(n), None) == EINVAL
+    assert L.kv8_disk_append(None, None, None, 0, None, 0, None) == EINVAL
+    assert L.kv8_disk_load(None, 0, 0, None, None, 0, None, None) == EINVAL
+    assert L.kv8_disk_close(None) == 0
+    assert L.kv8_status_string(-9) == b"cache file read, write or rename failed"
