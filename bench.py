@@ -7,7 +7,7 @@ kv_lora 512 + qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token,
 One step = one decode query per sequence over its whole cache (the "append"
 workload also quantizes 65536 fresh rows into the cache inside the step).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce|wuv|prefill]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|produce|wuv|prefill|persist]
                     [--variant auto|simt|tcgen05] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  `value` = KV GB/s over all ranks (KV bytes the
@@ -627,6 +627,106 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+PERSIST_METRIC = "fp8 cache save + resume through the cache file (COLIKV2 records): GB/s"
+
+
+def run_persist(args, rank, world, local_rank):
+    """Save 65536 cache rows (the append workload's fresh rows, at scattered slots) to
+    a new cache file and load them back into other slots: one step.  The calls are
+    synchronous host I/O (page cache, no fsync), so the step is timed on the host."""
+    import shutil
+    import tempfile
+
+    import torch
+    import fp8_mla_latent_gb300 as pkg
+    from fp8_mla_latent_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    n = max(1, int(65536 * args.scale))
+    p = workloads.producer_inputs(n)
+    codes = torch.zeros((p.n_slots, 576), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((p.n_slots, 2), dtype=torch.float32, device=dev)
+    slots = torch.from_numpy(p.slots).to(dev)
+    pkg.kv8_quantize_rows(torch.from_numpy(p.rows).to(dev), codes, scales, dst_slot=slots)
+    back = torch.from_numpy(np.random.default_rng(5).permutation(p.n_slots)[:n].astype(np.int64)).to(dev)
+    c2, s2 = torch.zeros_like(codes), torch.zeros_like(scales)
+    tmp = tempfile.mkdtemp(prefix=f"kv8_persist_{rank}_")
+    staging = 16384
+
+    def step(k):
+        path = os.path.join(tmp, f"cache{k}.kv")
+        t0 = time.perf_counter()
+        with pkg.Kv8Disk(path, staging_rows=staging) as d:
+            d.append(codes, scales, slots=slots)
+        t1 = time.perf_counter()
+        with pkg.Kv8Disk(path, staging_rows=staging) as d:
+            d.load(c2, s2, dst_slot=back)
+        t2 = time.perf_counter()
+        os.remove(path)
+        return t1 - t0, t2 - t1
+
+    try:
+        for k in range(args.warmup):
+            step(k)
+        torch.cuda.synchronize()
+        rank_sync()
+        times = [step(args.warmup + k) for k in range(args.steps)]
+        rank_sync()
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    ok = bool(torch.equal(c2[back], codes[slots]))
+    save_ms = 1e3 * float(np.mean([a for a, _ in times]))
+    load_ms = 1e3 * float(np.mean([b for _, b in times]))
+    save_ms, load_ms = slowest_rank([save_ms, load_ms], dev)
+    ms = save_ms + load_ms
+    nbytes = 2 * n * 584
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    chunks = (n + staging - 1) // staging
+    return {
+        "metric": PERSIST_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 codes + f32 scales (bytes moved)",
+        "data": "synthetic (seeded; the producer workload's rows, quantized, at scattered slots)",
+        "config": {"workload": "persist", "rows": n, "staging_rows": staging,
+                   "file": "fresh file on the host's temporary directory each step (page cache, no fsync)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "phases_ms": {"save": save_ms, "load": load_ms},
+        "save_gbs": n * 584 / (save_ms * 1e-3) / 1e9, "load_gbs": n * 584 / (load_ms * 1e-3) / 1e9,
+        "round_trip_bit_exact": ok,
+        "roofline": {"bound": "io", "achieved": value, "peak": None, "unit": "GB/s", "frac": None,
+                     "traffic": None, "kernel": "gather_kernel / scatter_kernel + file I/O",
+                     "note": "host file I/O through the page cache dominates; no device roofline",
+                     "algorithmic": {"bytes": nbytes, "per_unit": "584 B per row, each way"}},
+        "e2e": {"value": value, "unit": "GB/s", "ms_per_step": ms,
+                "h2d_bytes_per_step": n * 584, "d2h_bytes_per_step": n * 584},
+        "gpu_launches": 2 * chunks * args.steps,
+        "clocks": {"note": "host-timed I/O step"},
+    }, p
+
+
+def persist_cpu_baseline(p, budget_s=4.0):
+    """The oracle's writer and reader of the file on the same rows, from host arrays."""
+    import tempfile
+    import oracle
+    from oracle import coli_kv
+    codes, scales = oracle.quantize_rows(p.rows)
+    n = codes.shape[0]
+    d = tempfile.mkdtemp(prefix="kv8_persist_oracle_")
+    path = os.path.join(d, "o.kv")
+    t0 = time.time()
+    k = 0
+    while time.time() - t0 < budget_s and k < 20:
+        coli_kv.write_v2(path, codes, scales)
+        coli_kv.read(path)
+        k += 1
+    dt = time.time() - t0
+    os.remove(path)
+    os.rmdir(d)
+    return {"value": 2 * k * n * 584 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{k} save + read round trips of {n} rows, numpy + Python file I/O, {dt:.2f} s wall"}
+
+
 def produce_cpu_baseline(p, budget_s=8.0):
     import oracle
     n = p.rows.shape[0]
@@ -694,6 +794,22 @@ def oracle_sample(w, budget_s, codes=None, scales=None):
 def run_reference(args, world):
     from fp8_mla_latent_gb300 import workloads
     import oracle
+    if args.workload == "persist":
+        p = workloads.producer_inputs(max(1, int(65536 * args.scale)))
+        persist_cpu_baseline(p, 0.5)
+        vals = [persist_cpu_baseline(p, 1.0) for _ in range(args.steps)]
+        value = float(np.mean([v["value"] for v in vals]))
+        n = p.rows.shape[0]
+        return {
+            "impl": "reference", "metric": PERSIST_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 2 * n * 584 / (value * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8 + f32",
+            "data": "synthetic (seeded; same rows as our arm)",
+            "config": {"workload": "persist", "rows": n},
+            "cpu_baseline": dict(vals[-1], value=value),
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     if args.workload == "prefill":
         p = workloads.prefill_inputs(max(128, int(4096 * args.scale)))
         prefill_cpu_baseline(p, 0.5)
@@ -784,6 +900,12 @@ def main():
     if args.workload == "wuv":
         res = run_wuv(args, rank, world, local_rank)
         if rank == 0:
+            print(json.dumps(res), flush=True)
+    elif args.workload == "persist":
+        res, p = run_persist(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = persist_cpu_baseline(p)
             print(json.dumps(res), flush=True)
     elif args.workload == "prefill":
         res, p = run_prefill(args, rank, world, local_rank)
