@@ -14,7 +14,9 @@
 // host writes them after the last committed record, and only then rewrites the
 // header's row count, so a torn append is never part of the file.  Load: the
 // host reads records into the staging buffer and a scatter kernel puts them into
-// cache slots; version-1 rows go through the library's quantizer instead.
+// cache slots; version-1 rows go through the library's quantizer instead.  The
+// records use two buffers, so the kernel of one chunk overlaps the file transfer
+// of the next (append) or previous (load).
 #include <errno.h>
 #include <stdio.h>
 #include <string.h>
@@ -279,17 +281,28 @@ int kv8_disk_append(kv8_disk* d, const uint8_t* kv_codes, const float* kv_scales
     const int st = convert_to_v2(d, s);
     if (st != KV8_OK) return st;
   }
-  for (int64_t r0 = 0; r0 < n; r0 += d->staging_rows) {
-    const int64_t m = (n - r0) < d->staging_rows ? (n - r0) : d->staging_rows;
+  // two record buffers in the staging area: the gather of chunk k + 1 runs on the
+  // device while the host writes chunk k
+  const int64_t cap = d->staging_rows;
+  auto launch = [&](int64_t r0, int b) -> bool {
+    const int64_t m = (n - r0) < cap ? (n - r0) : cap;
     *reinterpret_cast<volatile int*>(d->flag) = 0;
-    const int64_t threads = m * 32;
-    gather_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+    gather_kernel<<<(unsigned)((m * 32 + 255) / 256), 256, 0, s>>>(
         kv_codes, kv_scales, n_slots, slots != nullptr ? slots + r0 : nullptr, r0, m,
-        area_rows(d, true), d->flag_dev);
-    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+        area_rows(d, true) + b * cap * REC2, d->flag_dev);
+    return cudaGetLastError() == cudaSuccess;
+  };
+  if (!launch(0, 0)) return KV8_ECUDA;
+  for (int64_t r0 = 0, k = 0; r0 < n; r0 += cap, ++k) {
+    const int64_t m = (n - r0) < cap ? (n - r0) : cap;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
     if (*reinterpret_cast<volatile int*>(d->flag) != 0) return KV8_EBOUNDS;  // nothing committed
-    if (!write_at(d->f, HDR + (d->n_rows + r0) * REC2, area_rows(d, false), (size_t)(m * REC2)))
+    if (r0 + cap < n && !launch(r0 + cap, (int)((k + 1) & 1))) return KV8_ECUDA;
+    if (!write_at(d->f, HDR + (d->n_rows + r0) * REC2, area_rows(d, false) + (k & 1) * cap * REC2,
+                  (size_t)(m * REC2))) {
+      cudaStreamSynchronize(s);
       return KV8_EIO;
+    }
   }
   if (fflush(d->f) != 0) return KV8_EIO;
   return commit_rows(d, d->n_rows + n);
@@ -305,33 +318,48 @@ int kv8_disk_load(kv8_disk* d, int64_t first_row, int64_t n, uint8_t* kv_codes, 
   if (((uintptr_t)kv_codes & 15) || ((uintptr_t)kv_scales & 7) || ((uintptr_t)dst_slot & 7))
     return KV8_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int64_t r0 = 0; r0 < n; r0 += d->staging_rows) {
-    const int64_t m = (n - r0) < d->staging_rows ? (n - r0) : d->staging_rows;
+  const int64_t cap = d->staging_rows;
+  if (d->version == 2) {
+    // two record buffers: the host reads chunk k + 1 while the device scatters chunk k
+    auto read_chunk = [&](int64_t r0, int b) -> bool {
+      const int64_t m = (n - r0) < cap ? (n - r0) : cap;
+      return read_at(d->f, HDR + (first_row + r0) * REC2, area_rows(d, false) + b * cap * REC2,
+                     (size_t)(m * REC2));
+    };
+    if (!read_chunk(0, 0)) return KV8_EIO;
+    *reinterpret_cast<volatile int*>(d->flag) = 0;
+    for (int64_t r0 = 0, k = 0; r0 < n; r0 += cap, ++k) {
+      const int64_t m = (n - r0) < cap ? (n - r0) : cap;
+      scatter_kernel<<<(unsigned)((m * 32 + 255) / 256), 256, 0, s>>>(
+          area_rows(d, true) + (k & 1) * cap * REC2, m, kv_codes, kv_scales, n_slots,
+          dst_slot != nullptr ? dst_slot + r0 : nullptr, first_row + r0, d->flag_dev);
+      if (cudaGetLastError() != cudaSuccess) return KV8_ECUDA;
+      const bool more = r0 + cap < n;
+      const bool read_ok = !more || read_chunk(r0 + cap, (int)((k + 1) & 1));
+      if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
+      if (!read_ok) return KV8_EIO;
+    }
+    return *reinterpret_cast<volatile int*>(d->flag) != 0 ? KV8_EBOUNDS : KV8_OK;
+  }
+  for (int64_t r0 = 0; r0 < n; r0 += cap) {
+    const int64_t m = (n - r0) < cap ? (n - r0) : cap;
     const int64_t row = first_row + r0;
     const int64_t* sl = dst_slot != nullptr ? dst_slot + r0 : nullptr;
     *reinterpret_cast<volatile int*>(d->flag) = 0;
-    if (d->version == 2) {
-      if (!read_at(d->f, HDR + row * REC2, area_rows(d, false), (size_t)(m * REC2))) return KV8_EIO;
-      const int64_t threads = m * 32;
-      scatter_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-          area_rows(d, true), m, kv_codes, kv_scales, n_slots, sl, row, d->flag_dev);
+    if (!read_at(d->f, HDR + row * REC1, area_rows(d, false), (size_t)(m * REC1))) return KV8_EIO;
+    // version 1: the rows are quantized on the way in (identity slots start at `row`;
+    // the quantizer skips a slot outside the pool, which the check reports)
+    if (sl != nullptr) {
+      check_slots_kernel<<<(unsigned)((m + 255) / 256), 256, 0, s>>>(sl, m, n_slots, d->flag_dev);
       if (cudaGetLastError() != cudaSuccess) return KV8_ECUDA;
-    } else {
-      if (!read_at(d->f, HDR + row * REC1, area_rows(d, false), (size_t)(m * REC1))) return KV8_EIO;
-      // version 1: the rows are quantized on the way in (identity slots start at `row`;
-      // the quantizer skips a slot outside the pool, which the check reports)
-      if (sl != nullptr) {
-        check_slots_kernel<<<(unsigned)((m + 255) / 256), 256, 0, s>>>(sl, m, n_slots, d->flag_dev);
-        if (cudaGetLastError() != cudaSuccess) return KV8_ECUDA;
-      }
-      const cudaError_t e =
-          sl != nullptr
-              ? launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, sl,
-                                kv_codes, kv_scales, n_slots, s)
-              : launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
-                                kv_codes + row * D, kv_scales + row * 2, n_slots - row, s);
-      if (e != cudaSuccess) return KV8_ECUDA;
     }
+    const cudaError_t e =
+        sl != nullptr
+            ? launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, sl,
+                              kv_codes, kv_scales, n_slots, s)
+            : launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
+                              kv_codes + row * D, kv_scales + row * 2, n_slots - row, s);
+    if (e != cudaSuccess) return KV8_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KV8_ECUDA;
     if (*reinterpret_cast<volatile int*>(d->flag) != 0) return KV8_EBOUNDS;
   }
