@@ -7,17 +7,30 @@
 // partials of one (sequence, head) in log2 units, M = max_s m_s and
 // w_s = 2^(m_s - M):
 //   out = sum_s w_s o_s / sum_s w_s l_s,   lse = ln2 * (M + log2 sum_s w_s l_s).
-// One CTA of 256 threads per (head, sequence).  The maxima and weights of the
-// splits are computed by all threads together (block reductions), the weights
-// kept in shared memory; then thread i of half q sums channels 4i..4i+3 over the
-// splits s = q, q+2, ... in order, with eight splits' loads in flight, and the
-// two halves are added (half 0 first), so the result is reproducible.
+// Two forms.  With fewer than 1024 (sequence, head) pairs, one CTA of 256
+// threads per pair: the maxima and weights of the splits by block reductions,
+// weights kept in shared memory; thread i of half q sums channels 4i..4i+3 over
+// the splits s = q, q+2, ... in order, eight splits' loads in flight, and the two
+// halves are added (half 0 first).  Otherwise one warp per pair, eight per CTA,
+// no block barriers: the warp takes M by a butterfly over its lanes' strided
+// maxima, then walks the splits in order, every lane computing the same weight
+// w_s and running denominator (so the sum order is fixed and no reduction is
+// needed) while it accumulates its 16 channels (four 16-byte pieces, 512 B per
+// warp load, coalesced); the splits' loads go out two splits ahead of their use.
+// Both forms are deterministic.
 #include "kv8_common.cuh"
 
 namespace kv8 {
 namespace {
 
-constexpr int CT = 256;         // threads per CTA
+constexpr int CT = 256;                 // threads per CTA (warp form: eight pairs)
+constexpr int WPC = CT / 32;
+constexpr int AHEAD = 2;                // splits whose loads are in flight per warp
+// Few (sequence, head) pairs come with many splits each (a long sequence cut into
+// one wave of items): a CTA of 256 threads per pair then keeps more loads in
+// flight.  Many pairs come with few splits: one warp per pair.
+constexpr int64_t WARP_PATH_MIN = 1024;
+
 constexpr int WCHUNK = 1024;    // split weights held in shared memory at a time
 
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -31,7 +44,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
-__global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(CT) combine_cta_kernel(DecodeArgs a) {
   const int h = blockIdx.x, b = blockIdx.y;
   __shared__ long long s_first, s_count;
   __shared__ float red[8];
@@ -98,11 +111,76 @@ __global__ void __launch_bounds__(CT) combine_kernel(DecodeArgs a) {
     a.lse[(int64_t)b * a.H + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
+__global__ void __launch_bounds__(CT) combine_warp_kernel(DecodeArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bh = (int64_t)blockIdx.x * WPC + warp;
+  if (bh >= (int64_t)a.B * a.H) return;
+  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+  const int64_t* e = a.seg + ((int64_t)b * a.plan.n_hg + h / a.plan.hg) * 2;
+  const int64_t first = e[0], ns = e[1];
+  const int hl = h % a.plan.hg, hg = a.plan.hg;
+  auto part = [&](int64_t s) -> int64_t { return (first + s) * hg + hl; };
+  const float4* o = reinterpret_cast<const float4*>(a.ws_o) + lane;
+
+  float M = -INFINITY;
+  for (int64_t s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_m[part(s)]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  if (M != -INFINITY) {
+    // v[d][k]: split s + d, piece k; AHEAD splits in flight ahead of their use
+    float4 v[AHEAD][4];
+    float mv[AHEAD], lv[AHEAD];
+    auto fetch = [&](int64_t s, int d) {
+      if (s < ns) {
+        const int64_t p = part(s);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[d][k] = o[p * (DL / 4) + 32 * k];
+        mv[d] = a.ws_m[p];
+        lv[d] = a.ws_l[p];
+      }
+    };
+#pragma unroll
+    for (int d = 0; d < AHEAD; ++d) fetch(d, d);
+    for (int64_t s = 0; s < ns; s += AHEAD) {
+#pragma unroll
+      for (int d = 0; d < AHEAD; ++d) {
+        if (s + d < ns) {
+          const float w = (mv[d] == -INFINITY) ? 0.f : exp2f(mv[d] - M);
+          L += w * lv[d];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc[k].x += w * v[d][k].x; acc[k].y += w * v[d][k].y;
+            acc[k].z += w * v[d][k].z; acc[k].w += w * v[d][k].w;
+          }
+          fetch(s + d + AHEAD, d);
+        }
+      }
+    }
+  }
+  const float inv = (L > 0.f) ? 1.0f / L : 0.f;
+  float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.H + h) * DL) + lane;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    out[32 * k] = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+  if (a.lse != nullptr && lane == 0)
+    a.lse[(int64_t)b * a.H + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
-  dim3 grid(a.H, a.B);
-  combine_kernel<<<grid, CT, 0, s>>>(a);
+  const int64_t warps = (int64_t)a.B * a.H;
+  if (warps >= WARP_PATH_MIN) {
+    combine_warp_kernel<<<(unsigned)((warps + WPC - 1) / WPC), CT, 0, s>>>(a);
+  } else {
+    dim3 grid(a.H, a.B);
+    combine_cta_kernel<<<grid, CT, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
