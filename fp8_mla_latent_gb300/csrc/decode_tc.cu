@@ -24,10 +24,10 @@
 // swizzle, K-major).  The e4m3 context operand: one d-block of 128 tokens x 128
 // channels (the TMA box, 128-byte swizzle), read as V^T.
 //
-// Warp roles (14 warps):
+// Warp roles (14 warps; 16 for 16-head groups, which have six converters):
 //   warp 0       issues the score MMAs of every tile (lane 0 alone, or for N = 16
 //                the whole warp with one elected lane); the warp owns TMEM.
-//   warp 13      loads each tile's four e4m3 d-blocks by TMA (the next tile's
+//   last warp    loads each tile's four e4m3 d-blocks by TMA (the next tile's
 //                block as soon as this tile's MMAs on it are done), zeroes rows
 //                that hold no data, and issues the context MMAs as soon as the
 //                tile's P'' is written.
@@ -36,8 +36,8 @@
 //                transposed warp reduction, running denominators per thread, lazy
 //                rescaling of O (only the heads whose max grew by more than 2^1),
 //                P'' split into e4m3 hi + lo in f16 arithmetic.
-//   warps 9-12   score converters: the chunks Lc 0..7, Rc of every tile, in order,
-//                into a 4-slot fp16 ring; warp w takes every fourth chunk (16-byte
+//   warps 9..     score converters: the chunks Lc 0..7, Rc of every tile, in order,
+//                into a 4-slot (6 for 16 heads) fp16 ring, one warp per slot (16-byte
 //                loads, the next chunk's loads in flight while it waits for its
 //                slot, hardware cvt, swizzled 16-byte stores).  The bulk-copy
 //                engine prefetches tiles into L2 three tiles ahead.
@@ -62,14 +62,36 @@ using namespace ptx;
 
 constexpr int CHUNK = TILE * 64 * 2;         // 16 KB: 128 rows x 64 fp16
 constexpr int VBLK = TILE * 128;             // 16 KB: 128 rows x 128 e4m3 (one d-block of V)
-constexpr int S_RING = 4;                    // score-operand chunk slots
 constexpr int S_PER_TILE = 9;                // Lc channel blocks 0..7, then Rc
 constexpr int NSOFT = 8;
-constexpr int NCONV = 4;
 constexpr int WARP_SOFT = 1;
-constexpr int WARP_CONV = WARP_SOFT + NSOFT;  // 9..12
-constexpr int WARP_VMMA = WARP_CONV + NCONV;  // 13: V tile loads and context MMAs
-constexpr int NTHREADS = (WARP_VMMA + 1) * 32;
+constexpr int WARP_CONV = WARP_SOFT + NSOFT;  // first converter warp (9)
+constexpr int NBAR_ALLOC = 48;               // mbarriers allocated
+
+// Per head-group width: the score ring and its converter warps (one warp per
+// slot).  16-head groups leave room in shared memory for six slots, half as many
+// e4m3 bytes again in flight; six converters keep the block at 16 warps, four per
+// SM sub-partition, so each thread keeps 128 registers (eight slots and 18 warps
+// would cap them at 96 and spill).
+template <int N>
+struct Cfg {
+  static constexpr int S_RING = (N <= 16) ? 6 : 4;        // score-operand chunk slots
+  static constexpr int NCONV = S_RING;
+  static constexpr int WARP_VMMA = WARP_CONV + NCONV;     // V tile loads and context MMAs
+  static constexpr int NTHREADS = (WARP_VMMA + 1) * 32;
+  // barrier indices
+  static constexpr int B_SF = 0;                      // [S_RING] score chunk converted
+  static constexpr int B_SE = B_SF + S_RING;          // [S_RING] score chunk consumed
+  static constexpr int B_VT = B_SE + S_RING;          // [4] e4m3 d-block loaded (TMA transactions)
+  static constexpr int B_VD = B_VT + 4;               // [4] context MMAs on a d-block done
+  static constexpr int B_S_FULL = B_VD + 4;           // [2] scores of a tile in TMEM
+  static constexpr int B_S_EMPTY = B_S_FULL + 2;      // [2] scores read by the softmax
+  static constexpr int B_P_FULL = B_S_EMPTY + 2;      // P'' of a tile written
+  static constexpr int B_O_DONE = B_P_FULL + 1;       // context MMAs of a tile done
+  static constexpr int B_G = B_O_DONE + 1;            // [group][2] softmax group barriers
+  static constexpr int B_DRAIN = B_G + 4;             // [2] issuers' final drains
+  static_assert(B_DRAIN + 2 <= NBAR_ALLOC, "barrier layout exceeds the barriers allocated");
+};
 constexpr int L2_AHEAD = 3;                  // tiles prefetched into L2 ahead of the converters
 // Lazy rescaling thresholds.  The e4m3 weights P'' = 2^(z - m) (sLc / s_ref)
 // P_TOP are at most 2^TAU * TAU_S_POW * P_TOP = 256 <= 448, and with this
@@ -88,10 +110,10 @@ struct Lay {
   static constexpr int NH = N / 2;                         // heads per softmax group
   static constexpr int Q = 0;                              // 9 chunks [N x 64] fp16
   static constexpr int RINGO = align1k(Q + 9 * N * 128);
-  static constexpr int VT = RINGO + S_RING * CHUNK;         // e4m3 V tile: 4 d-blocks
+  static constexpr int VT = RINGO + Cfg<N>::S_RING * CHUNK; // e4m3 V tile: 4 d-blocks
   static constexpr int P = VT + 4 * VBLK;                   // e4m3 P'' hi, lo: [N x 128 tokens] each
-  static constexpr int BAR = P + 2 * N * 128;              // 32 mbarriers
-  static constexpr int FLAGS = BAR + 32 * 8;               // tmem base, abort, corr flags
+  static constexpr int BAR = P + 2 * N * 128;              // NBAR_ALLOC mbarriers
+  static constexpr int FLAGS = BAR + NBAR_ALLOC * 8;       // tmem base, abort, corr flags
   static constexpr int CS = FLAGS + 32;                    // score constant per head
   static constexpr int MU = CS + N * 4;                    // max in use per head (log2)
   static constexpr int ALPHA = MU + N * 4;                 // rescale of l this tile
@@ -103,18 +125,7 @@ struct Lay {
   static constexpr int TMEM_COLS = (8 * N <= 128) ? 128 : (8 * N <= 256 ? 256 : 512);
 };
 
-// barrier indices (the layout follows the ring size; 32 barriers are allocated)
-constexpr int B_SF = 0;                      // [S_RING] score chunk converted
-constexpr int B_SE = B_SF + S_RING;          // [S_RING] score chunk consumed
-constexpr int B_VT = B_SE + S_RING;          // [4] e4m3 d-block loaded (TMA transactions)
-constexpr int B_VD = B_VT + 4;               // [4] context MMAs on a d-block done
-constexpr int B_S_FULL = B_VD + 4;           // [2] scores of a tile in TMEM
-constexpr int B_S_EMPTY = B_S_FULL + 2;      // [2] scores read by the softmax
-constexpr int B_P_FULL = B_S_EMPTY + 2;      // P'' of a tile written
-constexpr int B_O_DONE = B_P_FULL + 1;       // context MMAs of a tile done
-constexpr int B_G = B_O_DONE + 1;            // [group][2] softmax group barriers
-constexpr int B_DRAIN = B_G + 4;             // [2] issuers' final drains
-static_assert(B_DRAIN + 2 <= 32, "barrier layout exceeds the 32 barriers allocated");
+
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   uint4 v;
@@ -179,9 +190,15 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[NV], int
 }
 
 template <int N>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<N>::NTHREADS, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using L = Lay<N>;
+  using C = Cfg<N>;
+  constexpr int S_RING = C::S_RING, NCONV = C::NCONV, WARP_VMMA = C::WARP_VMMA,
+                NTHREADS = C::NTHREADS;
+  constexpr int B_SF = C::B_SF, B_SE = C::B_SE, B_VT = C::B_VT, B_VD = C::B_VD,
+                B_S_FULL = C::B_S_FULL, B_S_EMPTY = C::B_S_EMPTY, B_P_FULL = C::B_P_FULL,
+                B_O_DONE = C::B_O_DONE, B_G = C::B_G, B_DRAIN = C::B_DRAIN;
   constexpr int NH = L::NH;
   constexpr int LOG2_NH = NH == 8 ? 3 : (NH == 16 ? 4 : 5);
   extern __shared__ uint8_t smem_raw[];
@@ -848,7 +865,7 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
   CUtensorMap map;
   e = make_cache_map(a, &map);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, smem, s>>>(a, map);
+  decode_tc_kernel<N><<<a.plan.max_items, Cfg<N>::NTHREADS, smem, s>>>(a, map);
   return cudaGetLastError();
 }
 
