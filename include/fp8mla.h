@@ -44,7 +44,7 @@ typedef enum {
     KV8_OK = 0,
     KV8_EINVAL = -1,        /* null pointer, negative size, bad dimension            */
     KV8_EALIGN = -2,        /* a pointer or stride breaks the alignment rule stated  */
-    KV8_EUNSUPPORTED = -3,  /* a size this build does not handle (e.g. block_size)   */
+    KV8_EUNSUPPORTED = -3,  /* a size the library does not handle (e.g. block_size)  */
     KV8_ECUDA = -4,         /* a CUDA launch or runtime call failed                  */
     KV8_EBOUNDS = -5,       /* a device-side index (block table, seq_len) was bad    */
     KV8_EWORKSPACE = -6,    /* workspace missing or smaller than *_workspace_size    */
