@@ -225,24 +225,18 @@ void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
  * kv8_oracle.h.  Each f32 operation goes through a volatile, so it is rounded
  * once, in the order written.                                                  */
 void orc_rmsnorm_row(const float* x, const float* weight, float eps, float* y) {
-    float p[32];
-    for (int l = 0; l < 32; ++l) {
-        volatile float acc = 0.0f;
-        for (int k = 0; k < 16; ++k) {
-            volatile float sq = x[16 * l + k] * x[16 * l + k];
-            acc = acc + sq;
-        }
-        p[l] = acc;
+    /* The sum of squares as written: each square is exact in double (a 24-bit
+     * significand squared fits in 53 bits), the 512 squares are added in index
+     * order in double, and the total is rounded to f32 once.  Away from f32
+     * rounding boundaries this is the correctly rounded f32 of the exact sum,
+     * whatever order any other implementation adds in. */
+    double acc = 0.0;
+    for (int i = 0; i < ORC_DL; ++i) {
+        const double xi = (double)x[i];
+        acc += xi * xi;
     }
-    for (int o = 16; o >= 1; o >>= 1) {
-        float q[32];
-        for (int l = 0; l < 32; ++l) {
-            volatile float t = p[l] + p[l ^ o];
-            q[l] = t;
-        }
-        for (int l = 0; l < 32; ++l) p[l] = q[l];
-    }
-    volatile float ms = p[0] * (1.0f / 512.0f);   /* exact: a power of two */
+    volatile float ss = (float)acc;
+    volatile float ms = ss * (1.0f / 512.0f);     /* exact: a power of two */
     volatile float t = ms + eps;
     volatile float r = sqrtf(t);
     volatile float inv = 1.0f / r;

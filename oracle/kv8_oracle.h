@@ -56,11 +56,12 @@ void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
  *       cosine and sine the caller tabulates per position (rope_cos/sin[pos][32]):
  *       y0 = x0*c - x1*s,  y1 = x0*s + x1*c;
  *   then the per-row quantizer above, into dst_slot[r].
- * Every f32 operation is rounded once (no FMA).  The sum of squares ss has a
- * fixed order, the one a 32-lane warp reduction takes: 32 partial sums p_l of
- * x[16l .. 16l+15] in index order, then for o = 16, 8, 4, 2, 1 every p_l becomes
- * p_l + p_(l xor o); ss = p_0.  Rows whose position is outside [0, max_pos) are
- * skipped (their slots are left as they were).                                  */
+ * Every f32 operation is rounded once (no FMA).  The sum of squares ss is the
+ * plain sum: the squares (exact in double) added in index order in double, the
+ * total rounded to f32 once -- the correctly rounded f32 sum except on rows whose
+ * exact sum sits within about 2^-44 of an f32 rounding boundary.  Rows whose
+ * position is outside [0, max_pos) are skipped (their slots are left as they
+ * were).                                                                        */
 void orc_rmsnorm_row(const float* x, const float* weight, float eps, float* y);
 void orc_rope_pairs(const float* x, const float* cos_row, const float* sin_row, float* y);
 void orc_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,

@@ -57,6 +57,70 @@ def test_rmsnorm_against_float64_and_unit_mean_square():
         assert np.mean(y1.astype(np.float64) ** 2) == pytest.approx(ms / (ms + EPS), rel=2e-6)
 
 
+def np_rmsnorm_f32(x, w, eps, ss):
+    """The f32 steps after the sum of squares, each rounded once (numpy float32
+    scalars are IEEE single operations): ms = ss/512, inv = 1/sqrt(ms + eps),
+    y = (x * inv) * w."""
+    f = np.float32
+    inv = f(1.0) / np.sqrt(f(f(ss) * f(1.0 / 512.0)) + f(eps))
+    return ((x.astype(np.float32) * inv).astype(np.float32) * w).astype(np.float32)
+
+
+def exact_ss(x):
+    """f32 of the exactly rounded (math.fsum) double sum of the squares."""
+    return np.float32(math.fsum(float(v) * float(v) for v in np.asarray(x, np.float64)))
+
+
+def butterfly_ss(x):
+    """The sum of squares in another f32 order (32 partial sums of 16, then a
+    pairwise tree), which is not the oracle's definition."""
+    sq = (x.astype(np.float32) ** 2).astype(np.float32).reshape(32, 16)
+    p = np.zeros(32, np.float32)
+    for k in range(16):
+        p = (p + sq[:, k]).astype(np.float32)
+    idx = np.arange(32)
+    for o in (16, 8, 4, 2, 1):
+        p = (p + p[idx ^ o]).astype(np.float32)
+    return p[0]
+
+
+def test_rmsnorm_sum_of_squares_is_the_exact_sum_rounded_once():
+    """On rows where a reordered f32 sum of squares gives a different f32 total,
+    the oracle still gives the f32 of the exact sum: its output equals the f32
+    pipeline run from f32(fsum(x^2)) bit for bit, and not the one run from the
+    reordered sum."""
+    rng = np.random.default_rng(21)
+    w = np.ones(512, np.float32)
+    discriminating = 0
+    for r in range(400):
+        x = (rng.standard_normal(512) * np.exp(rng.uniform(-3, 3))).astype(np.float32)
+        y = oracle.rmsnorm_row(x, w, EPS)
+        ss = exact_ss(x)
+        assert np.array_equal(y.view(np.uint32), np_rmsnorm_f32(x, w, EPS, ss).view(np.uint32)), r
+        other = np_rmsnorm_f32(x, w, EPS, butterfly_ss(x))
+        discriminating += not np.array_equal(y.view(np.uint32), other.view(np.uint32))
+    # the pin discriminates: on these rows an f32 sum in another order gives other bits
+    assert discriminating >= 20
+
+
+def test_rmsnorm_sum_of_squares_hand_worked():
+    """1 + 2^-24 * 511 (exactly): index-order f32 accumulation loses every 2^-24
+    (1 + 2^-24 rounds back to 1), the exact sum is 1 + 511 * 2^-24, which rounds
+    to 1 + 2^-23 * 256 = 1.0000305 in f32 (halfway cases are absent)."""
+    x = np.zeros(512, np.float32)
+    x[0] = 1.0
+    x[1:] = np.float32(2.0 ** -12)          # squares: 2^-24 each
+    ss = exact_ss(x)
+    assert ss == np.float32(1.0 + 511 * 2.0 ** -24)
+    seq = np.float32(0)
+    for v in x:
+        seq = np.float32(seq + np.float32(v * v))
+    assert seq == np.float32(1.0) != ss      # naive f32 order differs from the definition
+    y = oracle.rmsnorm_row(x, np.ones(512, np.float32), 0.0)
+    assert np.array_equal(y.view(np.uint32), np_rmsnorm_f32(x, np.ones(512, np.float32), 0.0,
+                                                             ss).view(np.uint32))
+
+
 def test_rmsnorm_weight_is_a_per_channel_factor_bit_exact():
     rng = np.random.default_rng(4)
     x = rng.standard_normal(512).astype(np.float32)
