@@ -59,6 +59,8 @@ def source_hash(files):
 
 KERNEL_SOURCES = {
     "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "decode_pair": ["fp8_mla_latent_gb300/csrc/decode_pair.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh",
+                    "fp8_mla_latent_gb300/csrc/tc_ptx.cuh"],
     "produce_rows": ["fp8_mla_latent_gb300/csrc/quantize.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "wuv": ["fp8_mla_latent_gb300/csrc/wuv.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "prefill": ["fp8_mla_latent_gb300/csrc/prefill.cu", "fp8_mla_latent_gb300/csrc/tc_ptx.cuh",
@@ -167,7 +169,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
     variant = {"auto": pkg.KV8_DECODE_AUTO, "simt": pkg.KV8_DECODE_SIMT,
-               "tcgen05": pkg.KV8_DECODE_TCGEN05}[args.variant]
+               "tcgen05": pkg.KV8_DECODE_TCGEN05, "tc_cta": pkg.KV8_DECODE_TCGEN05_CTA,
+               "tc_pair": pkg.KV8_DECODE_TCGEN05_PAIR}[args.variant]
 
     w = workloads.make(args.workload, scale=args.scale)
     codes = torch.zeros((w.n_slots, 576), dtype=torch.uint8, device=dev)
@@ -193,6 +196,8 @@ def run_ours(args, rank, world, local_rank):
     if variant == pkg.KV8_DECODE_AUTO:
         plan_variant = pkg.KV8_DECODE_TCGEN05 if (w.H >= 16 and tc_built(pkg, dev)) \
             else pkg.KV8_DECODE_SIMT
+    if plan_variant == pkg.KV8_DECODE_TCGEN05:
+        plan_variant = pkg.KV8_DECODE_TCGEN05_PAIR if w.H > 64 else pkg.KV8_DECODE_TCGEN05_CTA
 
     def step(evs=None):
         if evs is not None:
@@ -286,7 +291,22 @@ def run_ours(args, rank, world, local_rank):
     value = kv_bytes / (ms_step * 1e-3) / 1e9
     peaks = load_peaks()
     flops = FLOP_PER_TOKEN_HEAD * w.total_tokens * w.H
-    if plan_variant == pkg.KV8_DECODE_TCGEN05:
+    if plan_variant == pkg.KV8_DECODE_TCGEN05_PAIR:
+        kernel = "decode_pair"
+        # both contractions on e4m3 operands: the e4m3 tensor peak is twice the measured
+        # bf16 dense peak (the nominal fp8 / bf16 ratio)
+        p8 = 2 * peaks["bf16_tflops"] * 1e12
+        t_tensor = flops / p8
+        t_hbm = w.kv_bytes() / (peaks["hbm_gbs"] * 1e9)
+        if t_tensor >= t_hbm:
+            roof = {"bound": "tensor", "achieved": flops / (ms_dec * 1e-3) / 1e12,
+                    "peak": p8 / 1e12, "unit": "TFLOP/s",
+                    "peak_note": f"{peaks['src']} bf16 dense burst x 2 (e4m3 operands)"}
+        else:
+            roof = {"bound": "hbm", "achieved": w.kv_bytes() / (ms_dec * 1e-3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_note": f"{peaks['src']} copy",
+                    "tensor_frac": flops / (ms_dec * 1e-3) / p8}
+    elif plan_variant == pkg.KV8_DECODE_TCGEN05_CTA:
         kernel = "decode_tc"
         # two contractions, two operand types: the scores (2*576*H FLOP per token) on fp16
         # operands at the measured bf16 rate, the context (2*512*H) on e4m3 operands at twice
@@ -327,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
         "token_heads_per_s": tok_heads / (ms_step * 1e-3),
         "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H,
                    "T_total": w.total_tokens, "kv_lora": 512, "qk_rope": 64,
-                   "variant": {1: "simt", 2: "tcgen05"}[plan_variant],
+                   "variant": {1: "simt", 3: "tcgen05_cta", 4: "tcgen05_pair"}[plan_variant],
                    "l2": "flushed between steps (256 MB write) and KV > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "phases_ms": {"quantize": float(q_ms.mean()), "decode": ms_dec,
@@ -884,7 +904,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="long")
-    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05", "tc_cta", "tc_pair"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale", type=float, default=1.0,

@@ -6,6 +6,7 @@ declared in ``include/fp8mla.h``); this package holds its in-tree build step
 synthetic workloads (``workloads``).
 """
 from ._lib import (KV8_BLOCK, KV8_D, KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05,
+                   KV8_DECODE_TCGEN05_CTA, KV8_DECODE_TCGEN05_PAIR,
                    KV8_DL, KV8_DR, Kv8Disk, Kv8Error, alloc_workspace, kv8_prefill_project, kv8_produce_rows, kv8_quantize_rows,
                    kv8_selftest_wait_timeout,
                    kv8_workspace_error, lib, library_path, mla_absorb_decode_fp8,
@@ -15,7 +16,8 @@ from ._lib import (KV8_BLOCK, KV8_D, KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECOD
                    mla_absorb_decode_fp8_workspace_size, mla_wuv_epilogue)
 
 __all__ = [
-    "KV8_BLOCK", "KV8_D", "KV8_DECODE_AUTO", "KV8_DECODE_SIMT", "KV8_DECODE_TCGEN05", "KV8_DL",
+    "KV8_BLOCK", "KV8_D", "KV8_DECODE_AUTO", "KV8_DECODE_SIMT", "KV8_DECODE_TCGEN05",
+    "KV8_DECODE_TCGEN05_CTA", "KV8_DECODE_TCGEN05_PAIR", "KV8_DL",
     "KV8_DR", "Kv8Disk", "Kv8Error", "alloc_workspace", "kv8_prefill_project", "kv8_produce_rows", "kv8_quantize_rows",
     "kv8_selftest_wait_timeout", "kv8_workspace_error", "lib",
     "library_path", "mla_absorb_decode_fp8", "mla_absorb_decode_fp8_batch",

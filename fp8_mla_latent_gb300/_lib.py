@@ -18,6 +18,7 @@ from . import build as _build
 
 KV8_DL, KV8_DR, KV8_D, KV8_BLOCK = 512, 64, 576, 64
 KV8_DECODE_AUTO, KV8_DECODE_SIMT, KV8_DECODE_TCGEN05 = 0, 1, 2
+KV8_DECODE_TCGEN05_CTA, KV8_DECODE_TCGEN05_PAIR = 3, 4
 STATUS = {0: "KV8_OK", -1: "KV8_EINVAL", -2: "KV8_EALIGN", -3: "KV8_EUNSUPPORTED",
           -4: "KV8_ECUDA", -5: "KV8_EBOUNDS", -6: "KV8_EWORKSPACE", -7: "KV8_ETIMEOUT",
           -8: "KV8_ESCRATCH", -9: "KV8_EIO", -10: "KV8_EFORMAT"}
@@ -30,6 +31,8 @@ class Kv8Error(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
         msg = lib().kv8_status_string(status).decode()
+        if status in (-3, -4):
+            msg += ", " + lib().kv8_last_cuda_error().decode()
         super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({msg})")
 
 
@@ -68,6 +71,7 @@ def lib() -> ctypes.CDLL:
                 "kv8_disk_load": (i32, [P, i64, i64, P, P, i64, P, P]),
                 "kv8_disk_close": (i32, [P]),
                 "kv8_status_string": (ctypes.c_char_p, [i32]),
+                "kv8_last_cuda_error": (ctypes.c_char_p, []),
                 "kv8_abi_version": (i32, []),
             }
             for name, (res, args) in sig.items():

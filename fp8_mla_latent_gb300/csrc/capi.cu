@@ -19,18 +19,23 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   SplitPlan p{};
   int v = variant;
   if (v == kAuto) v = (H >= 16 && tc_available()) ? kTc : kSimt;
+  if (v == kTc) v = (H > 64) ? kTcPair : kTcCta;
   p.variant = v;
-  if (v == kTc) {
+  if (v == kTcPair) {
+    p.hg = 128;  // MMA M = heads of the item, on a pair of SMs
+  } else if (v == kTcCta) {
     p.hg = H <= 16 ? 16 : (H <= 32 ? 32 : 64);  // MMA N = heads per CTA
   } else {
     p.hg = 4;
   }
   p.n_hg = (H + p.hg - 1) / p.hg;
   (void)max_len;
-  // One wave: the tensor-core kernel holds a whole SM per CTA, the SIMT kernel
-  // runs about four CTAs per SM.  Cutting every (sequence, head group) into
-  // items of ceil(jobs / target) tiles gives at most target + B * n_hg items.
-  p.target = NUM_SMS * (v == kTc ? 1 : 4);
+  // One wave: the one-CTA tensor-core kernel holds a whole SM per CTA, the pair
+  // kernel two SMs per item (the launch lowers this to the pairs the device
+  // holds at once), the SIMT kernel runs about four CTAs per SM.  Cutting every
+  // (sequence, head group) into items of ceil(jobs / target) tiles gives at most
+  // target + B * n_hg items.
+  p.target = v == kTcPair ? NUM_SMS / 2 : NUM_SMS * (v == kTcCta ? 1 : 4);
   p.max_items = p.target + B * p.n_hg;
   const int64_t parts = (int64_t)p.max_items * p.hg;
   p.off_seg = 64;  // header: error word, then the item table of the split
@@ -54,6 +59,10 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The CUDA error behind this thread's most recent KV8_ECUDA / KV8_EUNSUPPORTED
+// from a decode launch (kv8_last_cuda_error reports its name).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes) {
   if (workspace == nullptr || workspace_bytes < a.plan.ws_bytes) return KV8_EWORKSPACE;
   if (!aligned(workspace, 256)) return KV8_EALIGN;
@@ -68,8 +77,13 @@ int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes
 
 int run_partials(DecodeArgs& a, cudaStream_t s) {
   if (cudaMemsetAsync(a.err, 0, a.plan.hdr_bytes, s) != cudaSuccess) return KV8_ECUDA;
-  cudaError_t e = (a.plan.variant == kTc) ? launch_decode_tc(a, s) : launch_decode_simt(a, s);
-  if (e != cudaSuccess) return e == cudaErrorNotSupported ? KV8_EUNSUPPORTED : KV8_ECUDA;
+  cudaError_t e = a.plan.variant == kTcPair  ? launch_decode_pair(a, s)
+                  : a.plan.variant == kTcCta ? launch_decode_tc(a, s)
+                                             : launch_decode_simt(a, s);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = e;
+    return e == cudaErrorNotSupported ? KV8_EUNSUPPORTED : KV8_ECUDA;
+  }
   return KV8_OK;
 }
 
@@ -78,17 +92,27 @@ int run_decode(DecodeArgs& a, void* workspace, int64_t workspace_bytes, cudaStre
   if (st != KV8_OK) return st;
   st = run_partials(a, s);
   if (st != KV8_OK) return st;
-  if (launch_combine(a, s) != cudaSuccess) return KV8_ECUDA;
+  const cudaError_t e = launch_combine(a, s);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = e;
+    return KV8_ECUDA;
+  }
   return KV8_OK;
 }
 
-bool valid_variant(int v) { return v == kAuto || v == kSimt || v == kTc; }
+bool valid_variant(int v) { return v >= kAuto && v <= kTcPair; }
+
+// The softmax scale: positive and finite (the kernels take running maxima of
+// the raw dot products, which is only the maximum of the scores for a scale > 0).
+bool valid_scale(float s) { return s > 0.0f && s <= 3.0e38f; }
 
 }  // namespace
 
 extern "C" {
 
-int kv8_abi_version(void) { return 100; }
+int kv8_abi_version(void) { return 101; }
+
+const char* kv8_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 const char* kv8_status_string(int status) {
   switch (status) {
@@ -194,11 +218,12 @@ int mla_absorb_decode_fp8(const float* q_lat, const float* q_rope, const uint8_t
                           const float* kv_scales, int64_t T, int H, float sm_scale, float* out,
                           float* lse, void* workspace, int64_t workspace_bytes, int variant,
                           void* stream) {
-  if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant)) return KV8_EINVAL;
+  if (T < 0 || H < 1 || H > 1024 || !valid_variant(variant) || !valid_scale(sm_scale))
+    return KV8_EINVAL;
   if (q_lat == nullptr || q_rope == nullptr || out == nullptr) return KV8_EINVAL;
   if (T > 0 && (kv_codes == nullptr || kv_scales == nullptr)) return KV8_EINVAL;
   if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16) ||
-      !aligned(kv_codes, 16) || !aligned(kv_scales, 8) || !aligned(lse, 4))
+      !aligned(kv_codes, 16) || !aligned(kv_scales, 16) || !aligned(lse, 4))
     return KV8_EALIGN;
   DecodeArgs a{};
   a.q_lat = q_lat;
@@ -236,7 +261,7 @@ int batch_args(DecodeArgs& a, const float* q_lat, const float* q_rope, const uin
                int B, int H, int max_blocks, int block_size, int64_t n_blocks, float sm_scale,
                float* out, float* lse, int variant, bool need_inputs, bool need_outputs) {
   if (B < 0 || H < 1 || H > 1024 || max_blocks < 1 || !valid_variant(variant)) return KV8_EINVAL;
-  if (need_inputs && n_blocks < 1) return KV8_EINVAL;
+  if (need_inputs && (n_blocks < 1 || !valid_scale(sm_scale))) return KV8_EINVAL;
   if (block_size != KV8_BLOCK) return KV8_EUNSUPPORTED;
   if (seq_lens == nullptr || !aligned(seq_lens, 4)) return seq_lens ? KV8_EALIGN : KV8_EINVAL;
   if (need_inputs) {
@@ -244,7 +269,7 @@ int batch_args(DecodeArgs& a, const float* q_lat, const float* q_rope, const uin
         block_table == nullptr)
       return KV8_EINVAL;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_codes, 16) ||
-        !aligned(kv_scales, 8) || !aligned(block_table, 4))
+        !aligned(kv_scales, 16) || !aligned(block_table, 4))
       return KV8_EALIGN;
   }
   if (need_outputs) {
@@ -313,7 +338,9 @@ int mla_absorb_decode_fp8_batch_combine(const int32_t* seq_lens, int B, int H, i
   if (st != KV8_OK || B == 0) return st;
   st = bind_workspace(a, workspace, workspace_bytes);
   if (st != KV8_OK) return st;
-  return launch_combine(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV8_OK : KV8_ECUDA;
+  const cudaError_t e = launch_combine(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) g_last_cuda_error = e;
+  return e == cudaSuccess ? KV8_OK : KV8_ECUDA;
 }
 
 int kv8_workspace_error(const void* workspace, void* stream) {

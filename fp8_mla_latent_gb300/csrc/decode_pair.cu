@@ -1,0 +1,915 @@
+// decode_pair.cu -- split-T absorbed MLA decode on pairs of SMs (a cluster of
+// two CTAs) for groups of 128 heads: one CTA computes the scores and the
+// softmax, the other the context, both on tcgen05 tensor cores with e4m3
+// operands and f32 accumulators in TMEM.
+//
+// Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with
+// .coli_kv v2"), PR description: the latent Lc is both key and value of the
+// absorbed attention, the RoPE part Rc is key only, and each row's f32 scale is
+// applied outside its dot product; closing note: split-T kernels for long
+// caches.  Per (sequence b, head h):
+//   z_t = sm * ( sLc_t <q_lat, dec(Lc_t)> + sRc_t <q_rope, dec(Rc_t)> )
+//   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)
+//
+// A work item is (sequence, group of 128 heads, range of 128-token tiles); a
+// cluster of two CTAs takes one item.
+//
+// Score CTA (rank 0), per tile:
+//   S[h][t] = Q_h . K_t   kind::f8f6f4, M = 128 heads, N = 128 tokens, K = 512
+//             (S_L) and 64 (S_R) in two TMEM accumulators (the row scales of Lc
+//             and Rc differ).  A = the query in two e4m3 terms (hi + the e4m3
+//             residual) on one per-head power-of-two scale: its Lc part in TMEM,
+//             its Rc part in shared memory.  B = the e4m3 cache tile itself,
+//             loaded by TMA (five [128 tokens x 128 bytes] blocks: Lc 0..3 and Rc,
+//             whose box runs past column 576 into zero fill), never converted.
+//   softmax   eight warps; a thread owns one head (its TMEM lane) and one page
+//             (64 tokens) of the tile: z = c_h (sLc S_L + sRc S_R), tile maximum
+//             per head over both pages, lazy running maxima, running denominators
+//             of the exact weights p = 2^(z - m_h), and p as f16.  Each warp
+//             stages its 32 heads x 64 tokens of p, its heads' O rescale factors
+//             and its page's token weights w_t = sLc_t P_TOP / s_ref in shared
+//             memory and sends them with one bulk copy to the context CTA.
+// Context CTA (rank 1), per tile:
+//   eight warps turn the received p into the context operand in place,
+//   P''[h][t] = p w_t (f16) as two e4m3 terms, hi + lo; zero the V rows without
+//   data; rescale the O rows of heads whose factor moved, one half of O while the
+//   MMAs of the other half run; and write the partial o at the end.
+//   O[h][d] += sum_t P''[h][t] V[t][d]   kind::f8f6f4, M = 128 heads, N = 256
+//             latent channels (two halves of 512), K = 32 tokens per MMA, hi and
+//             lo terms into the same accumulator (all 512 TMEM columns).  V is the
+//             e4m3 cache tile (Lc, by TMA), read as an MN-major operand.
+// The two MMA-issuing threads wait on as few barriers as possible (one per tile
+// for the scores, one per O half for the context): a barrier wait on the issuing
+// thread leaves the tensor pipe idle for about two hundred cycles.
+//
+// Lazy maxima: a head's running maximum moves up when a tile's maximum exceeds
+// it by more than 2^TAU, and down to the tile's maximum when that lies more than
+// 2^DOWN below it (but within 2^DOWN_CAP of the highest maximum so far), so that
+// the weights of a bulk of tokens far below an earlier dominant token stay inside
+// the e4m3 range instead of flushing to zero; the row-scale reference moves when a
+// scale exceeds it TAU_S times.  Every wait is bounded (2 s): on a timeout the CTA
+// flags the workspace error word, drains its MMAs and copies, meets its partner
+// at the closing cluster barrier, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kv8_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace kv8 {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int HG = 128;                      // heads per work item
+constexpr int NTHREADS = 320;                // warp 0 TMA, warp 1 MMA, warps 2..9 lane workers
+constexpr int W_TMA = 0, W_MMA = 1, W_LANE = 2, N_LANE_WARPS = 8;
+constexpr int KBLK = TILE * 128;             // 16 KB: [128 tokens x 128 bytes]
+constexpr int BLKS = 5;                      // K blocks per tile: Lc 0..3, Rc
+constexpr int NKS = 2 * BLKS;                // K-block ring slots (score CTA): two tiles
+constexpr int NSC = 4;                       // scale ring slots (score CTA), one tile each
+constexpr int VTILE = 4 * KBLK;              // 64 KB: the tile's Lc, four d-blocks
+constexpr int NVT = 2;                       // V ring slots (context CTA), one tile each
+// Payload of one tile, one chunk per softmax warp (chunk c = page * 4 + lane
+// quarter; the context CTA registers the bytes it expects on its own barrier): p as f16 for its 32 heads x 64 tokens (rows of 128 bytes, 16-byte
+// units swizzled by the row), the O rescale factors of its heads, the token
+// weights of its page, and s_ref.
+constexpr int C_P16 = 0, C_FCOL = 4096, C_W = C_FCOL + 32 * 4, C_EXTRA = C_W + 64 * 4;
+constexpr int CHUNK = C_EXTRA + 16;          // 4496 bytes
+constexpr int P_BYTES = N_LANE_WARPS * CHUNK;
+constexpr int P_STRIDE = 36 * 1024;
+constexpr int L2_AHEAD = 3;                  // tiles prefetched into L2 ahead of the K loads
+constexpr float TAU = 1.0f;
+constexpr float TAU_S = 2.0f;
+constexpr float P_TOP = 64.0f;               // P'' <= 2^TAU * TAU_S * P_TOP = 256 <= 448
+constexpr float DOWN = 10.0f;
+constexpr float DOWN_CAP = 60.0f;
+constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// mbarriers, indices derived from the ring sizes (the payload-free pair sits at
+// the same offset in both CTAs: the context CTA's commit multicasts to it)
+constexpr int B_PFREE = 0;                   // [2] score: the context MMAs of the payload buffer's last tile are done
+constexpr int B_KT = B_PFREE + 2;            // [2] score: all K blocks of a tile loaded (by tile parity)
+constexpr int B_KEMPTY = B_KT + 2;           // [NKS] score: K block consumed by the score MMAs
+constexpr int B_SCFULL = B_KEMPTY + NKS;     // [NSC] score: row scales of a tile loaded
+constexpr int B_SCEMPTY = B_SCFULL + NSC;    // [NSC] score: row scales read by the softmax
+constexpr int B_SFULL = B_SCEMPTY + NSC;     // score: S of a tile in TMEM
+constexpr int B_SEMPTY = B_SFULL + 1;        // score: S read and next tile's K loaded (8 arrivals)
+constexpr int B_PX = B_SEMPTY + 1;           // [4] score: the two warps of a lane quarter meet
+constexpr int B_VT = B_PX + 4;               // [NVT] context: V tile loaded
+constexpr int B_VEMPTY = B_VT + NVT;         // [NVT] context: V tile consumed
+constexpr int B_PFULL = B_VEMPTY + NVT;      // [2] context: payload of a tile arrived (bulk-copy bytes)
+constexpr int B_CVT = B_PFULL + 2;           // context: the payload is read, its buffer may be overwritten (8 arrivals)
+constexpr int B_RS = B_CVT + 1;              // [2] context: operand, V rows and O half ready (8 arrivals)
+constexpr int B_ODONE = B_RS + 2;            // [2] context: MMAs of an O half done
+constexpr int B_DRAIN = B_ODONE + 2;
+constexpr int NBAR = B_DRAIN + 1;
+
+// shared memory (offsets from the 1024-aligned base)
+constexpr int OFF_BAR = 0;
+constexpr int OFF_FLAGS = 512;               // tmem base, abort flag
+constexpr int OFF_CS = 1024;                 // score: c_h per head
+constexpr int OFF_XMAX = OFF_CS + HG * 4;    // score: [2 tiles][2 pages][128] page maxima
+constexpr int OFF_XSM = OFF_XMAX + 4 * HG * 4;  // score: [2 tiles][2 pages][4] page row-scale maxima
+constexpr int OFF_XL = OFF_XSM + 64;         // score: [2 pages][128] denominators
+constexpr int OFF_XA = OFF_XL + 2 * HG * 4;  // score: [2 halves][128] query maxima
+constexpr int OFF_QR = 6144;                 // score: [128 heads x 128 bytes]: Rc query hi | lo
+constexpr int OFF_KRING = OFF_QR + KBLK;
+constexpr int OFF_SCR = OFF_KRING + NKS * KBLK;  // [NSC][128 tokens][2] f32
+constexpr int OFF_STG = OFF_SCR + NSC * TILE * 8;  // [8 warps] staged payload chunks
+constexpr int TOTAL_S = OFF_STG + P_BYTES;
+constexpr int OFF_P = 4096;                  // context: 2 payloads / context operands
+constexpr int OFF_VRING = OFF_P + 2 * P_STRIDE;
+constexpr int TOTAL_C = OFF_VRING + NVT * VTILE;
+constexpr int SMEM = (TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C) + 1024;
+// score CTA TMEM columns: S_L, S_R (one tile), then the Lc query's hi and lo terms
+// (e4m3, four channels per column) as the A operand of the score MMAs
+constexpr int T_SL = 0, T_SR = 128, T_QH = 256, T_QL = 384;
+static_assert(OFF_XA + 2 * HG * 4 <= OFF_QR, "score CTA scratch overlaps the Rc query");
+static_assert(NBAR * 8 <= OFF_FLAGS, "barriers overlap the flags");
+static_assert(P_BYTES <= P_STRIDE && (P_STRIDE % 1024) == 0 && (OFF_VRING % 1024) == 0,
+              "payload layout");
+static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits in its payload buffer");
+static_assert((CHUNK % 16) == 0 && (OFF_STG % 16) == 0, "bulk-copied chunks");
+static_assert(SMEM <= 232448, "shared memory above the per-CTA limit");
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// byte offset of 16-byte unit u of row r in a 128-byte-swizzled K-major atom
+__device__ __forceinline__ uint32_t sw128(int r, int u) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// Two e4m3 terms of four f32 values already on the head's scale: hi = e4m3(x),
+// lo = e4m3(x - hi) (the difference is exact in f32).
+__device__ __forceinline__ void split4(const float* x, uint32_t& hi, uint32_t& lo) {
+  const uint16_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
+  const uint32_t f01 = e4m3x2_to_f16x2(h01), f23 = e4m3x2_to_f16x2(h23);
+  const float2 d01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+  const float2 d23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+  const uint16_t l01 = f32x2_to_e4m3x2(x[0] - d01.x, x[1] - d01.y);
+  const uint16_t l23 = f32x2_to_e4m3x2(x[2] - d23.x, x[3] - d23.y);
+  hi = (uint32_t)h01 | ((uint32_t)h23 << 16);
+  lo = (uint32_t)l01 | ((uint32_t)l23 << 16);
+}
+
+// Two e4m3 terms of an f16 pair, in f16 arithmetic (the residual of the hi term
+// is exact there).
+__device__ __forceinline__ void split_h2(__half2 x, uint16_t& hi, uint16_t& lo) {
+  hi = f16x2_to_e4m3x2(x);
+  const uint32_t d = e4m3x2_to_f16x2(hi);
+  lo = f16x2_to_e4m3x2(__hsub2(x, *reinterpret_cast<const __half2*>(&d)));
+}
+
+// Per-tile page facts, the same in every warp that asks.
+struct TileRows {
+  int64_t s0, s1;  // cache slot of the tile's first / second page, or -1 (absent or unmapped)
+  int nv;          // tokens of the tile inside the item
+};
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int64_t t0, int64_t t_end,
+                                              int i) {
+  TileRows r;
+  const int64_t tb = t0 + (int64_t)i * TILE;
+  const int64_t n = t_end - tb;
+  r.nv = n < TILE ? (int)n : TILE;
+  r.s0 = slot_of(a, b, tb);
+  r.s1 = r.nv > PAGE ? slot_of(a, b, tb + PAGE) : -1;
+  return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    decode_pair_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap smap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int64_t item = blockIdx.x >> 1;
+  __shared__ WorkItem s_it;
+  __shared__ int s_ok;
+  if (warp == 0) {
+    WorkItem it;
+    const bool ok = find_item(a, item, it);
+    if (lane == 0 && ok && rank == 0) record_segment(a, item, it);
+    if (lane == 0) {
+      s_it = it;
+      s_ok = ok ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;  // past the last work item: both CTAs of the pair leave here
+  const int b = s_it.b;
+  const int h0 = s_it.g * HG;
+  const int64_t t0 = s_it.t0, t_end = s_it.t1;
+  const int n_tiles = (int)((t_end - t0 + TILE - 1) / TILE);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_FLAGS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_FLAGS + 4);
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(a.err, ERR_TIMEOUT);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_PFREE + i], 1);
+      mbar_init(&bars[B_KT + i], 1);
+      mbar_init(&bars[B_PFULL + i], 1);
+      mbar_init(&bars[B_RS + i], N_LANE_WARPS);
+      mbar_init(&bars[B_ODONE + i], 1);
+    }
+    for (int i = 0; i < NKS; ++i) mbar_init(&bars[B_KEMPTY + i], 1);
+    for (int i = 0; i < NSC; ++i) {
+      mbar_init(&bars[B_SCFULL + i], 1);
+      mbar_init(&bars[B_SCEMPTY + i], N_LANE_WARPS);
+    }
+    mbar_init(&bars[B_SFULL], 1);
+    mbar_init(&bars[B_SEMPTY], N_LANE_WARPS);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PX + i], 2);
+    for (int i = 0; i < NVT; ++i) {
+      mbar_init(&bars[B_VT + i], 1);
+      mbar_init(&bars[B_VEMPTY + i], 1);
+    }
+    mbar_init(&bars[B_CVT], N_LANE_WARPS);
+    mbar_init(&bars[B_DRAIN], 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the context CTA expects the payloads of its first two tiles (one per
+    // buffer); each later one is expected when its buffer's previous tile is read
+    if (rank == 1) {
+      mbar_arrive_expect_tx(&bars[B_PFULL], (uint32_t)P_BYTES);
+      if (n_tiles > 1) mbar_arrive_expect_tx(&bars[B_PFULL + 1], (uint32_t)P_BYTES);
+    }
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  float* cs = reinterpret_cast<float*>(sm + OFF_CS);
+  __syncthreads();  // the TMEM base address is in shared memory
+  if (rank == 0 && warp >= W_LANE) {
+    // Query -> two e4m3 terms with a per-head power-of-two scale that puts max|q|
+    // in [128, 256); c_h undoes it and folds in sm_scale * log2(e).  Thread
+    // (head hh, half hf) converts Lc channels [256 hf, 256 hf + 256) into TMEM
+    // lane hh (four channels per column, channel 4j in the low byte of column j),
+    // and half 0 also the 64 Rc channels into row hh of the Rc operand in shared
+    // memory (hi in bytes 0..63, lo in 64..127).
+    const uint32_t tm = *tmem_slot;
+    const int q = warp & 3, hf = (warp - W_LANE) >> 2, hh = q * 32 + lane, h = h0 + hh;
+    const bool real = h < a.H;
+    const float4* src = reinterpret_cast<const float4*>(a.q_lat + ((int64_t)b * a.H + h) * DL) + 64 * hf;
+    const float2* rsrc = reinterpret_cast<const float2*>(a.q_rope + ((int64_t)b * a.H + h) * DR);
+    float* xa = reinterpret_cast<float*>(sm + OFF_XA);
+    float amax = 0.f;
+    if (real) {
+      for (int k = 0; k < 64; ++k) {
+        const float4 x = __ldg(src + k);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      }
+      if (hf == 0)
+        for (int k = 0; k < 32; ++k) {
+          const float2 y = __ldg(rsrc + k);
+          amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+        }
+    }
+    xa[hf * HG + hh] = amax;
+    named_bar_sync(1, N_LANE_WARPS * 32);
+    amax = fmaxf(xa[hh], xa[HG + hh]);
+    int e = 0;
+    if (amax > 0.f && isfinite(amax)) {
+      int x;
+      frexpf(amax, &x);
+      e = min(max(8 - x, -120), 120);
+    }
+    const float sc = ldexpf(1.0f, e);
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t hw[32], lw[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float4 x = real ? __ldg(src + ch * 32 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float v[4] = {x.x * sc, x.y * sc, x.z * sc, x.w * sc};
+        split4(v, hw[j], lw[j]);
+      }
+      __syncwarp();
+      tmem_st32(tm + lane_addr + T_QH + hf * 64 + ch * 32, hw);
+      tmem_st32(tm + lane_addr + T_QL + hf * 64 + ch * 32, lw);
+    }
+    if (hf == 0) {
+      const uint32_t qr = smem_u32(sm + OFF_QR);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 y0 = real ? __ldg(rsrc + 8 * u + 2 * k) : make_float2(0.f, 0.f);
+          float2 y1 = real ? __ldg(rsrc + 8 * u + 2 * k + 1) : make_float2(0.f, 0.f);
+          const float v[4] = {y0.x * sc, y0.y * sc, y1.x * sc, y1.y * sc};
+          split4(v, hw[k], lw[k]);
+        }
+        sts128(qr + sw128(hh, u), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+        sts128(qr + sw128(hh, u + 4), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      }
+      cs[hh] = real ? a.sm_scale * LOG2E / sc : 0.f;
+    }
+    __syncwarp();
+    tmem_wait_st();
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised before any remote arrive or copy
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (rank == 0) {
+    // ================================================================ score CTA
+    const uint32_t kring = smem_u32(sm + OFF_KRING);
+    const uint32_t qr = smem_u32(sm + OFF_QR);
+    const uint32_t scr = smem_u32(sm + OFF_SCR);
+    if (warp == W_TMA) {
+      if (lane == 0) {
+        bool ok = true;
+        auto prefetch_tile = [&](int i) {
+          const int64_t tb = t0 + (int64_t)i * TILE;
+          for (int pg = 0; pg < 2; ++pg) {
+            const int64_t tk = tb + pg * PAGE;
+            if (tk >= t_end) break;
+            const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
+            const int64_t slot = slot_of(a, b, tk);
+            if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
+          }
+        };
+        int nk = 0, nsc = 0;  // tiles whose K blocks / row scales were requested
+        for (int i = 0; i < L2_AHEAD && i < n_tiles; ++i) prefetch_tile(i);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          if (i + L2_AHEAD < n_tiles) prefetch_tile(i + L2_AHEAD);
+          const TileRows tr = tile_rows(a, b, t0, t_end, i);
+          const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
+          const int sc = i % NSC;
+          if (!mbar_wait(&bars[B_SCEMPTY + sc], ((i / NSC) & 1) ^ 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars[B_SCFULL + sc], 512u * pages);
+          if (tr.s0 >= 0) tma_load_1d(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
+          if (tr.s1 >= 0)
+            tma_load_1d(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
+          ++nsc;
+          // the tile's five blocks complete on one barrier; a slot is free once the
+          // MMAs of the tile two before have read it
+          uint64_t* kt = &bars[B_KT + (i & 1)];
+          for (int blk = 0; blk < BLKS; ++blk) {
+            const int j = i * BLKS + blk, ks = j % NKS;
+            if (!mbar_wait(&bars[B_KEMPTY + ks], ((j / NKS) & 1) ^ 1, abort_flag, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            if (blk == 0) {
+              mbar_arrive_expect_tx(kt, 8192u * pages * BLKS);
+              nk = i + 1;
+            }
+            const uint32_t dst = kring + ks * KBLK;
+            if (tr.s0 >= 0) tma_load_2d(dst, &kmap, 128 * blk, (int)tr.s0, kt);
+            if (tr.s1 >= 0) tma_load_2d(dst + 8192, &kmap, 128 * blk, (int)tr.s1, kt);
+          }
+        }
+        if (!ok) {
+          // after an abort, let the loads already requested land before the CTA can
+          // leave (a tile requested in part never completes its barrier: the wait
+          // then ends at its bound, after those loads have landed)
+          fail();
+          const int zero = 0;
+          for (int i = (nk > 2 ? nk - 2 : 0); i < nk; ++i)
+            (void)mbar_wait(&bars[B_KT + (i & 1)], (i >> 1) & 1, &zero, WAIT_NS);
+          for (int i = (nsc > NSC ? nsc - NSC : 0); i < nsc; ++i)
+            (void)mbar_wait(&bars[B_SCFULL + i % NSC], (i / NSC) & 1, &zero, WAIT_NS);
+        }
+      }
+      __syncwarp();
+    } else if (warp == W_MMA) {
+      if (lane == 0) {
+        const uint32_t idS = idesc_f16(128, 128, false, false);  // e4m3 x e4m3 (format 0)
+        const uint64_t kdesc = smem_desc(kring, 16, 1024, SW128);
+        const uint64_t qdesc = smem_desc(qr, 16, 1024, SW128);
+        // tile 0's K blocks; a later tile's are waited for by the softmax warps
+        // before they release S, so one barrier per tile gates these MMAs
+        bool ok = mbar_wait(&bars[B_KT], 0, abort_flag, WAIT_NS);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          if (!mbar_wait(&bars[B_SEMPTY], (i & 1) ^ 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int blk = 0; blk < BLKS; ++blk) {
+            const int ks = (i * BLKS + blk) % NKS;
+            const uint64_t bd = kdesc + (uint64_t)((ks * KBLK) >> 4);
+            if (blk < 4) {
+              // A = the Lc query from TMEM: 8 columns (32 channels) per MMA
+              const uint32_t ah = tmem + T_QH + blk * 32, al = tmem + T_QL + blk * 32;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                mma_f8_ts(tmem + T_SL, ah + kk * 8, bd + 2 * kk, idS, (blk | kk) != 0);
+                mma_f8_ts(tmem + T_SL, al + kk * 8, bd + 2 * kk, idS, 1u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                mma_f8(tmem + T_SR, qdesc + 2 * kk, bd + 2 * kk, idS, kk != 0);
+                mma_f8(tmem + T_SR, qdesc + 4 + 2 * kk, bd + 2 * kk, idS, 1u);
+              }
+            }
+            mma_commit(&bars[B_KEMPTY + ks]);
+          }
+          mma_commit(&bars[B_SFULL]);
+        }
+        if (!ok) fail();
+        const int zero = 0;
+        mma_commit(&bars[B_DRAIN]);
+        (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- softmax
+      const int q = warp & 3;                  // TMEM lane quarter
+      const int pg = (warp - W_LANE) >> 2;     // page of the tile: tokens [64 pg, 64 pg + 64)
+      const int hh = q * 32 + lane;            // head of the group = TMEM lane
+      const int chunk = pg * 4 + q;            // this warp's payload chunk
+      const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+      float* xmax = reinterpret_cast<float*>(sm + OFF_XMAX);  // [2][2][128]
+      float* xsm = reinterpret_cast<float*>(sm + OFF_XSM);    // [2][2][4]
+      float* xl = reinterpret_cast<float*>(sm + OFF_XL);      // [2][128]
+      uint8_t* stg_p = sm + OFF_STG + chunk * CHUNK;
+      const uint32_t stg = smem_u32(stg_p);
+      const float c = cs[hh];
+      const bool live = c > 0.f;               // a real head (padding heads have c = 0)
+      const uint32_t prem = map_to(smem_u32(sm + OFF_P), 1) + chunk * CHUNK;  // partner's buffers
+      const uint32_t pfull_rem = map_to(smem_u32(&bars[B_PFULL]), 1);
+      float mu = -INFINITY, mhi = -INFINITY, lsum = 0.f, sref = 0.f;
+      int px_phase = 0;
+      bool ok = true;
+      auto pair_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_PX + q]);
+        return mbar_wait_warp(&bars[B_PX + q], (px_phase++) & 1, abort_flag, WAIT_NS);
+      };
+      for (int i = 0; i < n_tiles; ++i) {
+        const int buf = i & 1, sc = i % NSC, pb = i & 1;
+        const TileRows tr = tile_rows(a, b, t0, t_end, i);
+        const int64_t my_slot = pg ? tr.s1 : tr.s0;
+        const int my_n = (my_slot >= 0) ? min(max(tr.nv - pg * PAGE, 0), PAGE) : 0;
+        if (!mbar_wait_warp(&bars[B_SCFULL + sc], (i / NSC) & 1, abort_flag, WAIT_NS) ||
+            !mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        __syncwarp();  // the TMEM loads are warp-collective: every lane, converged
+        // u = sLc S_L + sRc S_R for this thread's head and page, from the TMEM
+        // accumulators in two halves of 32 tokens (the row scales by broadcast
+        // loads: every lane reads the same 16 bytes)
+        const float4* sc4 = reinterpret_cast<const float4*>(sm + OFF_SCR + sc * TILE * 8) + pg * (PAGE / 2);
+        float u[PAGE];
+        float umax = -INFINITY;
+        const bool full = (my_n == PAGE);  // warp-uniform: every token of the page has data
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          uint32_t rl[32], rr[32];
+          tmem_ld32(tmem + lane_addr + T_SL + pg * PAGE + hlf * 32, rl);
+          tmem_ld32(tmem + lane_addr + T_SR + pg * PAGE + hlf * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int t = hlf * 32 + j;
+            const float4 s4 = sc4[t / 2];  // (sLc, sRc) of tokens t and t + 1
+            u[t] = fmaf(s4.y, __uint_as_float(rr[j]), s4.x * __uint_as_float(rl[j]));
+            u[t + 1] = fmaf(s4.w, __uint_as_float(rr[j + 1]), s4.z * __uint_as_float(rl[j + 1]));
+          }
+        }
+        if (full) {
+#pragma unroll
+          for (int t = 0; t < PAGE; ++t) umax = fmaxf(umax, u[t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < PAGE; ++t) {
+            u[t] = (t < my_n) ? u[t] : -INFINITY;
+            umax = fmaxf(umax, u[t]);
+          }
+        }
+        // the page's largest row scale: lane l holds tokens l and l + 32
+        const float2 sa = reinterpret_cast<const float2*>(sc4)[lane];
+        const float2 sb = reinterpret_cast<const float2*>(sc4)[lane + 32];
+        float smax = fmaxf(lane < my_n ? sa.x : 0.f, lane + 32 < my_n ? sb.x : 0.f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        tc_fence_before();
+        // S is read; the next tile's K blocks are waited for here, so that the MMA
+        // thread's one wait per tile covers both
+        if (i + 1 < n_tiles &&
+            !mbar_wait_warp(&bars[B_KT + ((i + 1) & 1)], ((i + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
+        // tile maxima (score of this head, and row scale) over both pages
+        xmax[(buf * 2 + pg) * HG + hh] = umax;
+        if (lane == 0) xsm[(buf * 2 + pg) * 4 + q] = smax;
+        if (!pair_sync()) {
+          ok = false;
+          break;
+        }
+        const float umax_t = fmaxf(xmax[(buf * 2) * HG + hh], xmax[(buf * 2 + 1) * HG + hh]);
+        smax = fmaxf(xsm[(buf * 2) * 4 + q], xsm[(buf * 2 + 1) * 4 + q]);
+        const float tmax = (c > 0.f) ? c * umax_t : -INFINITY;
+        float mn = mu;
+        if (tmax > mu + TAU) {
+          mn = tmax;
+        } else if (tmax < mu - DOWN && tmax >= mhi - DOWN_CAP && tmax > -INFINITY) {
+          mn = tmax;  // far below: move down so that this bulk stays inside the e4m3 range
+        }
+        const float alpha = (mn == mu) ? 1.f : (mu == -INFINITY ? 0.f : ex2_approx(mu - mn));
+        mu = mn;
+        mhi = fmaxf(mhi, mu);
+        const float sref_new = (smax > sref * TAU_S) ? smax : sref;
+        const float beta = (sref_new == sref) ? 1.f : (sref > 0.f ? sref / sref_new : 0.f);
+        sref = sref_new;
+        const float fcol = alpha * beta;
+        lsum *= alpha;
+        const float wk = sref > 0.f ? P_TOP / sref : 0.f;
+        const float mneg = -fmaxf(mu, -3.0e38f);
+        // p = 2^(z - m) as f16 pairs (tokens without data, and padding heads, 0; u is
+        // -inf there, and c = 0 only for padding heads)
+        uint32_t ph[PAGE / 2];
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < PAGE; t += 2) {
+          const float p0 = live ? ex2_approx(fmaf(c, u[t], mneg)) : 0.f;
+          const float p1 = live ? ex2_approx(fmaf(c, u[t + 1], mneg)) : 0.f;
+          ls0 += p0;
+          ls1 += p1;
+          const __half2 h2 = __floats2half2_rn(p0, p1);
+          ph[t / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        lsum += ls0 + ls1;
+        // this page's token weights w_t = sLc_t P_TOP / s_ref (0 without data):
+        // lane l takes tokens l and l + 32
+        const float w_lo = (lane < my_n) ? sa.x * wk : 0.f;
+        const float w_hi = (lane + 32 < my_n) ? sb.x * wk : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_SCEMPTY + sc]);
+        // the context CTA must be done with this payload buffer's previous tile
+        if (i >= 2 &&
+            !mbar_wait_warp(&bars[B_PFREE + pb], ((i >> 1) + 1) & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        // this warp's previous bulk copy has read the staging chunk
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int u16 = 0; u16 < 8; ++u16)
+          sts128(stg + C_P16 + lane * 128 + ((u16 ^ (lane & 7)) << 4),
+                 make_uint4(ph[4 * u16], ph[4 * u16 + 1], ph[4 * u16 + 2], ph[4 * u16 + 3]));
+        reinterpret_cast<float*>(stg_p + C_FCOL)[lane] = fcol;
+        reinterpret_cast<float*>(stg_p + C_W)[lane] = w_lo;
+        reinterpret_cast<float*>(stg_p + C_W)[lane + 32] = w_hi;
+        if (lane == 0)
+          *reinterpret_cast<uint4*>(stg_p + C_EXTRA) = make_uint4(__float_as_uint(sref), 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_copy_to_cta(prem + pb * P_STRIDE, stg, (uint32_t)CHUNK, pfull_rem + pb * 8);
+          bulk_commit();
+        }
+        __syncwarp();
+      }
+      if (!ok) {
+        fail();
+      } else {
+        // denominators over both pages; the partial's (m, l) per head
+        xl[pg * HG + hh] = lsum;
+        if (pair_sync()) {
+          if (pg == 0 && h0 + hh < a.H) {
+            const int64_t base = item * HG;
+            a.ws_m[base + hh] = mu;
+            a.ws_l[base + hh] = xl[hh] + xl[HG + hh];
+          }
+        } else {
+          fail();
+        }
+      }
+      // the copies have left this CTA, and the context CTA's last commits to this
+      // CTA's barriers have landed
+      if (lane == 0) bulk_wait_all();
+      if (ok && warp == W_LANE && lane == 0) {
+        const int zero = 0;
+        for (int i = (n_tiles > 2 ? n_tiles - 2 : 0); i < n_tiles; ++i)
+          (void)mbar_wait(&bars[B_PFREE + (i & 1)], (i >> 1) & 1, &zero, WAIT_NS);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ================================================================ context CTA
+    const uint32_t pbuf = smem_u32(sm + OFF_P);
+    const uint32_t vring = smem_u32(sm + OFF_VRING);
+    if (warp == W_TMA) {
+      if (lane == 0) {
+        bool ok = true;
+        int nv = 0;  // tiles requested
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const TileRows tr = tile_rows(a, b, t0, t_end, i);
+          const int vs = i % NVT;
+          if (!mbar_wait(&bars[B_VEMPTY + vs], ((i / NVT) & 1) ^ 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars[B_VT + vs],
+                                4u * ((tr.s0 >= 0 ? 8192u : 0u) + (tr.s1 >= 0 ? 8192u : 0u)));
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t dst = vring + vs * VTILE + m * KBLK;
+            if (tr.s0 >= 0) tma_load_2d(dst, &kmap, 128 * m, (int)tr.s0, &bars[B_VT + vs]);
+            if (tr.s1 >= 0) tma_load_2d(dst + 8192, &kmap, 128 * m, (int)tr.s1, &bars[B_VT + vs]);
+          }
+          ++nv;
+        }
+        if (!ok) {
+          fail();
+          const int zero = 0;
+          for (int i = (nv > NVT ? nv - NVT : 0); i < nv; ++i)
+            (void)mbar_wait(&bars[B_VT + i % NVT], (i / NVT) & 1, &zero, WAIT_NS);
+        }
+      }
+      __syncwarp();
+    } else if (warp == W_MMA) {
+      if (lane == 0) {
+        const uint32_t idV = idesc_f16(128, 256, false, true);  // A = P'' K-major, B = V MN-major
+        const uint64_t pdesc = smem_desc(pbuf, 16, 1024, SW128);
+        const uint64_t vdesc = smem_desc(vring, KBLK, 1024, SW128);
+        bool ok = true;
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int pb = i & 1, vs = i % NVT;
+          for (int half = 0; half < 2; ++half) {
+            // operand, V rows and this O half ready (the lane workers' barrier)
+            if (!mbar_wait(&bars[B_RS + half], i & 1, abort_flag, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = pdesc + (uint64_t)((pb * P_STRIDE) >> 4);
+            const uint64_t bd = vdesc + (uint64_t)((vs * VTILE + half * 2 * KBLK) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // A: 32 tokens of the hi / lo atom (32 bytes in); B: 32 token rows of V (4 KB in)
+              mma_f8(tmem + half * 256, ad + 2 * kk, bd + 256 * kk, idV, (i > 0 || kk > 0) ? 1u : 0u);
+              mma_f8(tmem + half * 256, ad + (KBLK >> 4) + 2 * kk, bd + 256 * kk, idV, 1u);
+            }
+            mma_commit(&bars[B_ODONE + half]);
+          }
+          if (!ok) break;
+          mma_commit(&bars[B_VEMPTY + vs]);
+          mma_commit_mc(&bars[B_PFREE + pb], (uint16_t)0x3);
+        }
+        if (!ok) fail();
+        const int zero = 0;
+        mma_commit(&bars[B_DRAIN]);
+        (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- operand, V rows,
+      // O rescale and epilogue
+      const int q = warp & 3;
+      const int sub = (warp - W_LANE) >> 2;    // page of the tile / 128 columns of an O half
+      const int hh = q * 32 + lane;
+      const int chunk = sub * 4 + q;           // the payload chunk of these heads and tokens
+      const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+      bool ok = true;
+      float sref_fin = 0.f;
+      int cvt_phase = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int pb = i & 1, vs = i % NVT;
+        if (!mbar_wait_warp(&bars[B_PFULL + pb], (i >> 1) & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        // this thread's row of the payload (p for 64 tokens of head hh), the head's
+        // rescale factor and the page's token weights (as f16 pairs)
+        const uint32_t cb = pbuf + pb * P_STRIDE + chunk * CHUNK;
+        const uint8_t* cp = sm + OFF_P + pb * P_STRIDE + chunk * CHUNK;
+        uint4 pv[8];
+#pragma unroll
+        for (int u16 = 0; u16 < 8; ++u16) pv[u16] = lds128(cb + C_P16 + lane * 128 + ((u16 ^ (lane & 7)) << 4));
+        const float f = reinterpret_cast<const float*>(cp + C_FCOL)[lane];
+        if (i == n_tiles - 1) sref_fin = reinterpret_cast<const float*>(cp + C_EXTRA)[0];
+        uint32_t wh[PAGE / 2];
+#pragma unroll
+        for (int t = 0; t < PAGE; t += 4) {
+          const float4 w4 = reinterpret_cast<const float4*>(cp + C_W)[t / 4];
+          const __half2 a2 = __floats2half2_rn(w4.x, w4.y), b2 = __floats2half2_rn(w4.z, w4.w);
+          wh[t / 2] = *reinterpret_cast<const uint32_t*>(&a2);
+          wh[t / 2 + 1] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        const bool any = __any_sync(0xffffffffu, f != 1.f) && i > 0;
+        // every warp has read this payload: its buffer may now take the operand
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_CVT]);
+        if (!mbar_wait_warp(&bars[B_CVT], (cvt_phase++) & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        // the buffer's next payload (tile i + 2) may only be expected once this one
+        // has been read; its bytes come after the context MMAs of tile i
+        if (warp == W_LANE && lane == 0 && i + 2 < n_tiles)
+          mbar_arrive_expect_tx(&bars[B_PFULL + pb], (uint32_t)P_BYTES);
+        // P''[h][t] = p w_t in f16, as two e4m3 terms, into the hi and lo atoms
+        // (K-major, 128-byte swizzle) of the same buffer
+        const uint32_t opnd = pbuf + pb * P_STRIDE;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // 16 tokens per 16-byte unit
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int t = 16 * j + 4 * k;  // tokens t .. t + 3: two f16 pairs of p and of w
+            const uint4 src = pv[t / 8];
+            const uint32_t p01 = (t % 8 == 0) ? src.x : src.z, p23 = (t % 8 == 0) ? src.y : src.w;
+            const __half2 x01 = __hmul2(*reinterpret_cast<const __half2*>(&p01),
+                                        *reinterpret_cast<const __half2*>(&wh[t / 2]));
+            const __half2 x23 = __hmul2(*reinterpret_cast<const __half2*>(&p23),
+                                        *reinterpret_cast<const __half2*>(&wh[t / 2 + 1]));
+            uint16_t h01, l01, h23, l23;
+            split_h2(x01, h01, l01);
+            split_h2(x23, h23, l23);
+            hw[k] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+            lw[k] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+          }
+          const uint32_t off = sw128(hh, sub * 4 + j);
+          sts128(opnd + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+          sts128(opnd + KBLK + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+        }
+        // V tile: rows without data (past the item, or a page that is absent or
+        // unmapped) are zeroed so that their zero weights meet no NaN; warp w takes
+        // rows r = w (mod 8), a lane one 16-byte unit of one d-block
+        if (!mbar_wait_warp(&bars[B_VT + vs], (i / NVT) & 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        const TileRows tr = tile_rows(a, b, t0, t_end, i);
+        if (tr.s0 < 0 || tr.s1 < 0 || tr.nv < TILE) {
+          const uint32_t vb = vring + vs * VTILE;
+          for (int r = warp - W_LANE; r < TILE; r += N_LANE_WARPS) {
+            const bool has = r < tr.nv && (r < PAGE ? tr.s0 >= 0 : tr.s1 >= 0);
+            if (!has) sts128(vb + (lane >> 3) * KBLK + r * 128 + (lane & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+          }
+        }
+        fence_proxy_async_smem();
+        for (int half = 0; half < 2; ++half) {
+          if (any) {
+            if (!mbar_wait_warp(&bars[B_ODONE + half], (i - 1) & 1, abort_flag, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            __syncwarp();
+            const uint32_t col = tmem + lane_addr + half * 256 + sub * 128;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+              uint32_t r0[32], r1[32];
+              tmem_ld32(col + c0, r0);
+              tmem_ld32(col + c0 + 32, r1);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                r0[k] = __float_as_uint(__uint_as_float(r0[k]) * f);
+                r1[k] = __float_as_uint(__uint_as_float(r1[k]) * f);
+              }
+              tmem_st32(col + c0, r0);
+              tmem_st32(col + c0 + 32, r1);
+            }
+            __syncwarp();
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_RS + half]);
+        }
+        if (!ok) break;
+      }
+      if (ok) {
+        ok = mbar_wait_warp(&bars[B_ODONE], (n_tiles - 1) & 1, abort_flag, WAIT_NS) &&
+             mbar_wait_warp(&bars[B_ODONE + 1], (n_tiles - 1) & 1, abort_flag, WAIT_NS);
+      }
+      if (ok) {
+        // epilogue: the partial's unnormalised o = acc * s_ref / P_TOP
+        tc_fence_after();
+        __syncwarp();
+        const float oscale = sref_fin * (1.0f / P_TOP);
+        float* dst = a.ws_o + (item * HG + hh) * DL;
+        const bool mine = h0 + hh < a.H;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const int cbase = half * 256 + sub * 128;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld32(tmem + lane_addr + cbase + c0, r);
+            tmem_wait_ld();
+            if (mine) {
+#pragma unroll
+              for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(dst + cbase + c0 + k) =
+                    make_float4(__uint_as_float(r[k]) * oscale, __uint_as_float(r[k + 1]) * oscale,
+                                __uint_as_float(r[k + 2]) * oscale, __uint_as_float(r[k + 3]) * oscale);
+            }
+          }
+        }
+      } else {
+        fail();
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while its partner may still write to it
+  tc_fence_after();
+  if (warp == W_MMA) tmem_dealloc(tmem, 512);
+}
+
+// 1-D tensor map of the row scales (f32, two per slot): boxes of 128 floats (one
+// page); floats past the end read as zeros.
+cudaError_t make_scale_map(const DecodeArgs& a, CUtensorMap* map) {
+  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
+  if (rows < 1 || a.scales == nullptr) {
+    memset(map, 0, sizeof(*map));
+    return cudaSuccess;
+  }
+  if (2 * rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  const cuuint64_t dims[1] = {(cuuint64_t)(2 * rows)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(2 * rows) * 4};  // unused for one dimension
+  const cuuint32_t box[1] = {2 * PAGE};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(a.scales), dims,
+                      strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
+// Pairs that can be resident at once (clusters of two on this device).
+cudaError_t pair_capacity(int* pairs) {
+  static std::atomic<int> memo[MAX_DEVICES];
+  return per_device(memo, [](int* v) {
+    cudaError_t r = cudaFuncSetAttribute(decode_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (r != cudaSuccess) return r;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(NUM_SMS, 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    int n = 0;
+    r = cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel, &cfg);
+    if (r != cudaSuccess) return r;
+    if (n < 1) return cudaErrorLaunchOutOfResources;  // no pair fits: say so, never plan for one
+    *v = n > NUM_SMS / 2 ? NUM_SMS / 2 : n;
+    return cudaSuccess;
+  }, pairs);
+}
+
+cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s) {
+  if (a.plan.hg != HG) return cudaErrorNotSupported;
+  int pairs = 0;
+  cudaError_t e = pair_capacity(&pairs);
+  if (e != cudaSuccess) return e;
+  // the items are cut for the pairs this device holds at once (never more than
+  // the plan's bound, so the workspace the plan sized still holds every item)
+  DecodeArgs d = a;
+  if (pairs < d.plan.target) d.plan.target = pairs;
+  CUtensorMap kmap, smap;
+  e = make_cache_map(d, &kmap);
+  if (e != cudaSuccess) return e;
+  e = make_scale_map(d, &smap);
+  if (e != cudaSuccess) return e;
+  decode_pair_kernel<<<2 * d.plan.max_items, NTHREADS, SMEM, s>>>(d, kmap, smap);
+  return cudaGetLastError();
+}
+
+}  // namespace kv8

@@ -34,7 +34,8 @@
 //   warps 1-8    softmax, two groups of four warps; a thread owns one token row
 //                (its TMEM lane) and half of the heads: tile max per head by a
 //                transposed warp reduction, running denominators per thread, lazy
-//                rescaling of O (only the heads whose max grew by more than 2^1),
+//                rescaling of O (only the heads whose max grew by more than 2^1, or
+//                whose tile max lies more than 2^10 below it),
 //                P'' split into e4m3 hi + lo in f16 arithmetic.
 //   warps 9..     score converters: the chunks Lc 0..7, Rc of every tile, in order,
 //                into a 4-slot (6 for 16 heads) fp16 ring, one warp per slot (16-byte
@@ -100,6 +101,12 @@ constexpr int L2_AHEAD = 3;                  // tiles prefetched into L2 ahead o
 constexpr float TAU = 1.0f;                  // rescale O if a head's max grows by > 2^1
 constexpr float TAU_S_POW = 2.0f;            // ... or the scale reference by > 2
 constexpr float P_TOP = 64.0f;
+// A head's running max also moves down, to a tile's max that lies more than
+// 2^DOWN below it (and within 2^DOWN_CAP of the highest max so far): the weights
+// of a bulk of tokens far below an earlier dominant token then stay inside the
+// e4m3 range instead of flushing to zero in both terms.
+constexpr float DOWN = 10.0f;
+constexpr float DOWN_CAP = 60.0f;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bound on any single wait
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -116,7 +123,8 @@ struct Lay {
   static constexpr int FLAGS = BAR + NBAR_ALLOC * 8;       // tmem base, abort, corr flags
   static constexpr int CS = FLAGS + 32;                    // score constant per head
   static constexpr int MU = CS + N * 4;                    // max in use per head (log2)
-  static constexpr int ALPHA = MU + N * 4;                 // rescale of l this tile
+  static constexpr int MHI = MU + N * 4;                   // highest max in use so far per head
+  static constexpr int ALPHA = MHI + N * 4;                // rescale of l this tile
   static constexpr int FCOL = ALPHA + N * 4;               // rescale of O columns this tile
   static constexpr int LFIN = FCOL + N * 4;                // final denominators
   static constexpr int RMAX = LFIN + N * 4;                // [4][N] per-warp tile maxima
@@ -262,7 +270,10 @@ __global__ void __launch_bounds__(Cfg<N>::NTHREADS, 1)
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
-  if (threadIdx.x < N) mu_s[threadIdx.x] = -INFINITY;
+  if (threadIdx.x < N) {
+    mu_s[threadIdx.x] = -INFINITY;
+    reinterpret_cast<float*>(sm + L::MHI)[threadIdx.x] = -INFINITY;
+  }
   // Query -> fp16, one warp per head, with a per-head power-of-two scale that
   // puts max|q| in [2^14, 2^15); c_h undoes it and folds in sm_scale*log2(e).
   if (warp >= 1) {
@@ -564,12 +575,19 @@ __global__ void __launch_bounds__(Cfg<N>::NTHREADS, 1)
               fmaxf(fmaxf(rmax[hh], rmax[N + hh]), fmaxf(rmax[2 * N + hh], rmax[3 * N + hh]));
           const float tmax = (cs[hh] > 0.f) ? cs[hh] * umax : -INFINITY;
           float mu = mu_s[hh];
-          const float mn = fmaxf(mu, tmax);
+          float* mhi = reinterpret_cast<float*>(sm + L::MHI) + hh;
+          float mn = mu;
+          if (tmax > mu + TAU) {
+            mn = tmax;
+          } else if (tmax < mu - DOWN && tmax >= *mhi - DOWN_CAP && tmax > -INFINITY) {
+            mn = tmax;
+          }
           float alpha = 1.f;
-          if (mn > mu + TAU) {
+          if (mn != mu) {
             alpha = (mu == -INFINITY) ? 0.f : ex2_approx(mu - mn);
             mu = mn;
           }
+          *mhi = fmaxf(*mhi, mu);
           mu_s[hh] = mu;
           alpha_s[hh] = alpha;
           fcol[hh] = alpha * beta;
@@ -818,39 +836,6 @@ __global__ void __launch_bounds__(Cfg<N>::NTHREADS, 1)
   if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
-// Tensor map of the e4m3 cache for the V tile loads: rows of 576 bytes, boxes
-// of 64 rows (one page) x 128 bytes (one d-block), 128-byte swizzle.  Rows past
-// the end of the map read as zeros.
-cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
-  if (rows < 1 || a.codes == nullptr) {
-    // no cache rows: no tile is ever loaded, the map is never read
-    memset(map, 0, sizeof(*map));
-    return cudaSuccess;
-  }
-  if (rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)D};
-  const cuuint32_t box[2] = {128, PAGE};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.codes), dims,
-                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int N>
 cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
   const int smem = Lay<N>::TOTAL + 1024;
@@ -870,6 +855,48 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to
+// libcuda), then the map: `rank` dimensions, row strides in bytes (rank - 1 of
+// them), unit element strides, rows past the extent read as zeros.
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, unsigned rank, void* base,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                         CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, type, rank, base, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Tensor map of the e4m3 cache for the tile loads: rows of 576 bytes, boxes of
+// 64 rows (one page) x 128 bytes (one channel block), 128-byte swizzle.  Rows
+// (and columns) past the end of the map read as zeros.
+cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map) {
+  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
+  if (rows < 1 || a.codes == nullptr) {
+    // no cache rows: no tile is ever loaded, the map is never read
+    memset(map, 0, sizeof(*map));
+    return cudaSuccess;
+  }
+  if (rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D};
+  const cuuint32_t box[2] = {128, PAGE};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.codes), dims,
+                      strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
 bool tc_available() { return true; }
 

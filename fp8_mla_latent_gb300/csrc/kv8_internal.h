@@ -1,5 +1,6 @@
 // kv8_internal.h -- launch interface shared by the C-ABI shim and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,10 +20,12 @@ constexpr unsigned ERR_BLOCK_TABLE = 1u;
 constexpr unsigned ERR_SEQ_LEN = 2u;
 constexpr unsigned ERR_TIMEOUT = 4u;  // a bounded wait in a kernel gave up
 
-enum Variant { kAuto = 0, kSimt = 1, kTc = 2 };
+// Decode variants (the public kv8_decode_variant values): kTc resolves to the
+// SM-pair kernel for H > 64 and to the one-CTA kernel otherwise.
+enum Variant { kAuto = 0, kSimt = 1, kTc = 2, kTcCta = 3, kTcPair = 4 };
 
 struct SplitPlan {
-  int variant;      // resolved: kSimt or kTc
+  int variant;      // resolved: kSimt, kTcCta or kTcPair
   int hg;           // heads per CTA (head group)
   int n_hg;         // head groups
   int target;       // CTAs the work is spread over (one wave of the split kernel)
@@ -80,7 +83,17 @@ inline cudaError_t per_device(std::atomic<int> (&memo)[MAX_DEVICES], F&& make, i
   return cudaSuccess;
 }
 
+// Tensor maps for TMA loads (decode_tc.cu): a tiled map of `rank` dimensions
+// (row strides in bytes, rows past the extent read as zeros), and the e4m3
+// cache's map (boxes of one 64-row page x 128 bytes, 128-byte swizzle).
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, unsigned rank, void* base,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                         CUtensorMapSwizzle swizzle);
+cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map);
+
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s);
+cudaError_t pair_capacity(int* pairs);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_quantize(const float* src, int64_t n_rows, int64_t stride,

@@ -54,20 +54,26 @@ typedef enum {
     KV8_EFORMAT = -10       /* not a cache file, or shorter than its committed rows  */
 } kv8_status;
 
-/* Decode kernel choice.  Both accumulate in f32.  Tolerance classes, as max-abs
+/* Decode kernel choice.  All accumulate in f32.  Tolerance classes, as max-abs
  * error against the exact attention of the stored cache:
  *   SIMT     f32 operands:                      <= 2e-3 * max|out|
- *   TCGEN05  reduced-precision MMA operands: the query rounded to fp16 for the
- *            scores (the cache's e4m3 values convert to fp16 exactly), and the
- *            softmax weights as two e4m3 terms (about 8 significant bits) for the
- *            context, which reads the e4m3 cache values as they are:
- *                                               <= 1e-2 * max|out|
- * (the tensor-core kernel's error is dominated by the fp16 query; see the test
- * report for the measured worst case).                                         */
+ *   TCGEN05  reduced-precision MMA operands on e4m3 tensor cores: the query as
+ *            two e4m3 terms on a per-head power-of-two scale (about 8 significant
+ *            bits) against the cache's e4m3 values for the scores (the one-CTA
+ *            kernel rounds the query to fp16 instead), and the softmax weights as
+ *            two e4m3 terms on one scale for the context, which reads the e4m3
+ *            cache values as they are:         <= 1e-2 * max|out|
+ * (see the test report for the measured worst case of each kernel).
+ * TCGEN05 runs the SM-pair kernel (a cluster of two CTAs per work item: one
+ * computes scores and softmax, the other the context, for 128 heads) when
+ * H > 64, and the one-CTA kernel (16, 32 or 64 heads per CTA) otherwise;
+ * TCGEN05_CTA and TCGEN05_PAIR force one of the two at any H.              */
 typedef enum {
-    KV8_DECODE_AUTO = 0,     /* tcgen05 when H >= 16, else SIMT                   */
-    KV8_DECODE_SIMT = 1,     /* CUDA-core split-T kernel, any H >= 1              */
-    KV8_DECODE_TCGEN05 = 2   /* tcgen05 tensor-core split-T kernel, H >= 1        */
+    KV8_DECODE_AUTO = 0,         /* TCGEN05 when H >= 16, else SIMT              */
+    KV8_DECODE_SIMT = 1,         /* CUDA-core split-T kernel, any H >= 1         */
+    KV8_DECODE_TCGEN05 = 2,      /* tcgen05 tensor cores, H >= 1                 */
+    KV8_DECODE_TCGEN05_CTA = 3,  /* tcgen05, one CTA per work item               */
+    KV8_DECODE_TCGEN05_PAIR = 4  /* tcgen05, a pair of SMs per work item         */
 } kv8_decode_variant;
 
 /* ---------------------------------------------------------------------------
@@ -220,8 +226,9 @@ int kv8_selftest_wait_timeout(void* workspace, int64_t workspace_bytes, int64_t 
  *   q_lat     device f32 [H][512], 16-byte aligned.
  *   q_rope    device f32 [H][64],  16-byte aligned.
  *   kv_codes  device uint8 [>= T][576], 16-byte aligned.
- *   kv_scales device f32 [>= T][2], 8-byte aligned.
+ *   kv_scales device f32 [>= T][2], 16-byte aligned.
  *   T         >= 0.  H >= 1 and H <= 1024.
+ *   sm_scale  > 0 and finite (KV8_EINVAL otherwise).
  *   out       device f32 [H][512], 16-byte aligned.  lse: device f32 [H] or NULL.
  *   workspace device, >= mla_absorb_decode_fp8_workspace_size(T, H, variant)
  *             bytes, 256-byte aligned; scratch for the split-T partials.  Calls
@@ -243,7 +250,9 @@ int mla_absorb_decode_fp8(const float* q_lat, const float* q_rope, const uint8_t
  * the arithmetic is that of mla_absorb_decode_fp8.
  *
  *   q_lat       device f32 [B][H][512];  q_rope device f32 [B][H][64].
- *   kv_codes    device uint8 [n_blocks * 64][576];  kv_scales f32 [n_blocks*64][2].
+ *   kv_codes    device uint8 [n_blocks * 64][576], 16-byte aligned;
+ *               kv_scales f32 [n_blocks*64][2], 16-byte aligned.
+ *   sm_scale    > 0 and finite (KV8_EINVAL otherwise).
  *   block_table device int32 [B][max_blocks];  seq_lens device int32 [B].
  *   block_size  must be 64 (KV8_EUNSUPPORTED otherwise).
  *   out         device f32 [B][H][512];  lse device f32 [B][H] or NULL.
@@ -330,6 +339,11 @@ int kv8_noalloc_error(void* stream);
 int kv8_workspace_error(const void* workspace, void* stream);
 
 /* Human-readable text for a kv8_status value (static storage). */
+/* kv8_last_cuda_error -- the name of the CUDA error behind the calling thread's
+ * most recent KV8_ECUDA (or KV8_EUNSUPPORTED) from a decode call, e.g.
+ * "cudaErrorInvalidValue"; "cudaSuccess" if there was none.  Diagnostics only;
+ * the paper has no counterpart.  Static string, never NULL. */
+const char* kv8_last_cuda_error(void);
 const char* kv8_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */

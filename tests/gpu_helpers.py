@@ -11,9 +11,11 @@ import oracle
 
 # max-abs error <= TOL * max|out| per sequence against the f64 oracle on the same codes:
 #   CUDA-core kernel (f32 operands and accumulation): 2e-3;
-#   tensor-core kernel (reduced-precision MMA operands: q rounded to fp16 for the scores,
-#   the softmax weights as two e4m3 terms for the context; f32 accumulation): 1e-2.
-TOLS = {1: 2e-3, 2: 1e-2}
+#   tensor-core kernels (reduced-precision MMA operands: the query as fp16 (one-CTA kernel)
+#   or as two e4m3 terms (pair kernel) for the scores, the softmax weights as two e4m3
+#   terms for the context; f32 accumulation): 1e-2.
+TOLS = {1: 2e-3, 2: 1e-2, 3: 1e-2, 4: 1e-2}
+NAMES = {1: "simt", 2: "tcgen05", 3: "tcgen05_cta", 4: "tcgen05_pair"}
 LSE_TOL = 2e-3   # natural-log units
 WORST = {}       # variant -> worst observed err / max|out|, reported by the tests
 
@@ -92,3 +94,18 @@ def check(w, out, lse, codes_np, scales_np, pairs, variant=1):
             assert lerr <= LSE_TOL * max(1.0, np.abs(ref_lse).max()), f"lse err {lerr}"
     WORST[variant] = max(WORST.get(variant, 0.0), worst)
     return worst
+
+
+def custom_workload(seqs, q_lat, q_rope, sm_scale=None, shuffle=True, seed=0):
+    """A paged workload from explicit f32 rows: seqs = list of [T_b, 576] arrays,
+    q_lat [B, H, 512], q_rope [B, H, 64]; pages in a random order of one pool."""
+    from fp8_mla_latent_gb300 import workloads
+    rng = np.random.default_rng(seed)
+    lens = np.array([s.shape[0] for s in seqs], np.int32)
+    bt, n_slots, slots = workloads._paged_tables(rng, lens, shuffle=shuffle)
+    rows = np.concatenate(seqs).astype(np.float32) if len(seqs) else np.zeros((0, 576), np.float32)
+    B, H = q_lat.shape[:2]
+    return workloads.Workload("custom", B, H, lens, bt, n_slots, rows, slots, None, None,
+                              np.ascontiguousarray(q_lat, np.float32),
+                              np.ascontiguousarray(q_rope, np.float32),
+                              sm_scale=workloads.SM_SCALE if sm_scale is None else sm_scale)

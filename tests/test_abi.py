@@ -118,6 +118,13 @@ def test_decode_rejects_bad_arguments_on_host():
     assert d(P(g), P(g), P(g), P(g), -1, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
     assert d(P(g), P(g), P(g), P(g), 10, 0, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
     assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 7, None) == EINVAL
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 5, None) == EINVAL
+    assert d(P(g), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, -1, None) == EINVAL
+    # the softmax scale must be positive and finite
+    for bad in (0.0, -0.1, float("nan"), float("inf"), -float("inf")):
+        assert d(P(g), P(g), P(g), P(g), 10, 4, bad, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
+    # the row scales are read by TMA: 16-byte aligned
+    assert d(P(g), P(g), P(g), P(g + 8), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EALIGN
     assert d(None, P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EINVAL
     assert d(P(g + 8), P(g), P(g), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EALIGN
     assert d(P(g), P(g), P(g + 1), P(g), 10, 4, 0.1, P(g), None, P(g), 1 << 30, 0, None) == EALIGN
@@ -137,10 +144,19 @@ def test_decode_rejects_bad_arguments_on_host():
     a = list(args)
     a[10] = 0
     assert b(*a) == EINVAL
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        a = list(args)
+        a[11] = bad
+        assert b(*a) == EINVAL
+        assert L.mla_absorb_decode_fp8_batch_partials(*(a[:12] + [P(g), 1 << 30, 0, None])) == EINVAL
+        assert L.mla_absorb_decode_fp8_batch_noalloc(*(a[:14] + [0, None])) == EINVAL
+    a = list(args)
+    a[3] = P(g + 8)
+    assert b(*a) == EALIGN
     assert b(*([P(g)] * 6 + [0, 4, 8, 64, 16, 0.1, P(g), None, P(g), 1 << 30, 0, None])) == 0
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_workspace_sizes(variant):
     L = pkg.lib()
     for T, H in ((0, 1), (1, 4), (256, 4), (4096, 128), (262144, 128)):
@@ -152,6 +168,18 @@ def test_workspace_sizes(variant):
     # more tokens never needs a smaller workspace per split partial
     assert (L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 4096, 64, variant)
             >= L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 1, 64, variant))
+    assert L.mla_absorb_decode_fp8_batch_workspace_size(2, 128, 4096, 64, 5) < 0
+
+
+def test_tensor_core_workspace_covers_both_kernels():
+    """The automatic tensor-core choice and the two forced kernels plan their own
+    splits; each size query matches the kernel its call runs."""
+    L = pkg.lib()
+    for B, H in ((1, 16), (2, 64), (2, 65), (2, 128), (32, 128), (3, 200)):
+        auto = L.mla_absorb_decode_fp8_batch_workspace_size(B, H, 512, 64, 2)
+        cta = L.mla_absorb_decode_fp8_batch_workspace_size(B, H, 512, 64, 3)
+        pair = L.mla_absorb_decode_fp8_batch_workspace_size(B, H, 512, 64, 4)
+        assert auto == (pair if H > 64 else cta)
 
 
 def test_selftest_rejects_bad_arguments_on_host():

@@ -4,9 +4,11 @@ Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv
 v2"), PR description (absorbed attention over the e4m3 latent rows, scales
 hoisted out of the dots) and closing note (split-T).  Tolerance: max-abs error
 <= 2e-3 * max|out| per sequence for the CUDA-core kernel (f32 throughout) and
-<= 1e-2 * max|out| for the tensor-core kernel (reduced-precision MMA operands:
-q rounded to fp16 for the scores, the softmax weights as two e4m3 terms for the
-context; f32 accumulation); lse within 2e-3.
+<= 1e-2 * max|out| for the tensor-core kernels (reduced-precision MMA operands:
+the query as fp16 (one-CTA kernel) or two e4m3 terms (SM-pair kernel) for the
+scores, the softmax weights as two e4m3 terms for the context; f32
+accumulation); lse within 2e-3.  Every test runs the three kernels: CUDA-core,
+one-CTA tensor-core and SM-pair tensor-core (the last two forced at any H).
 Caches are filled by the library's quantizer and the oracle reads the same
 codes, so these tests isolate attention.
 """
@@ -21,7 +23,9 @@ from gpu_helpers import check, decode, upload_cache
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = {"simt": pkg.KV8_DECODE_SIMT, "tcgen05": pkg.KV8_DECODE_TCGEN05}
+VARIANTS = {"simt": pkg.KV8_DECODE_SIMT, "tc_cta": pkg.KV8_DECODE_TCGEN05_CTA,
+            "tc_pair": pkg.KV8_DECODE_TCGEN05_PAIR}
+TENSOR = (pkg.KV8_DECODE_TCGEN05_CTA, pkg.KV8_DECODE_TCGEN05_PAIR)
 
 
 def tc_ready():
@@ -42,7 +46,7 @@ def tc_ready():
 @pytest.fixture(params=list(VARIANTS))
 def variant(request):
     v = VARIANTS[request.param]
-    if v == pkg.KV8_DECODE_TCGEN05 and not tc_ready():
+    if v in TENSOR and not tc_ready():
         pytest.skip("tensor-core decode not built in this library")
     return v
 
@@ -201,8 +205,26 @@ def test_full_size_sampled(name, variant):
     assert np.isfinite(out).all()
 
 
+@pytest.mark.parametrize("H", [16, 64, 65, 128])
+def test_automatic_tensor_core_choice(H):
+    """TCGEN05 runs the SM-pair kernel for H > 64 and the one-CTA kernel otherwise:
+    bit for bit the forced kernel's result."""
+    if not tc_ready():
+        pytest.skip("tensor-core decode not built in this library")
+    w = workloads.make("batched", scale=0.02)
+    rng = np.random.default_rng(H)
+    w.H = H
+    w.q_lat = rng.standard_normal((w.B, H, 512)).astype(np.float32)
+    w.q_rope = rng.standard_normal((w.B, H, 64)).astype(np.float32)
+    codes, scales = upload_cache(w)
+    out_a, lse_a = decode(w, codes, scales, pkg.KV8_DECODE_TCGEN05)
+    forced = pkg.KV8_DECODE_TCGEN05_PAIR if H > 64 else pkg.KV8_DECODE_TCGEN05_CTA
+    out_f, lse_f = decode(w, codes, scales, forced)
+    assert np.array_equal(out_a.view(np.uint32), out_f.view(np.uint32))
+    assert np.array_equal(lse_a.view(np.uint32), lse_f.view(np.uint32))
+
+
 def test_report_worst_error():
     """Not a check: prints the worst err/max|out| seen per kernel in this session."""
-    from gpu_helpers import WORST
-    names = {1: "simt", 2: "tcgen05"}
-    print("worst err / max|out|: " + ", ".join(f"{names[k]} {v:.2e}" for k, v in sorted(WORST.items())))
+    from gpu_helpers import NAMES, WORST
+    print("worst err / max|out|: " + ", ".join(f"{NAMES[k]} {v:.2e}" for k, v in sorted(WORST.items())))
