@@ -22,15 +22,16 @@
 //             its Rc part in shared memory.  B = the e4m3 cache tile itself,
 //             loaded by TMA (five [128 tokens x 128 bytes] blocks: Lc 0..3 and Rc,
 //             whose box runs past column 576 into zero fill), never converted.
-//   softmax   eight warps; a thread owns one head (its TMEM lane) and one page
-//             (64 tokens) of the tile: z = c_h (sLc S_L + sRc S_R), tile maximum
-//             per head over both pages, lazy running maxima, running denominators
-//             of the exact weights p = 2^(z - m_h), and p as f16.  Each warp
-//             stages its 32 heads x 64 tokens of p, its heads' O rescale factors
-//             and its page's token weights w_t = sLc_t P_TOP / s_ref in shared
-//             memory and sends them with one bulk copy to the context CTA.
+//   softmax   sixteen warps, four per TMEM lane quarter; a thread owns one head
+//             (its TMEM lane) and one part (32 tokens) of the tile: z = c_h (sLc
+//             S_L + sRc S_R), tile maximum per head over the four parts, lazy
+//             running maxima, running denominators of the exact weights
+//             p = 2^(z - m_h), and p as f16.  Each warp stages its 32 heads x 32
+//             tokens of p, its heads' O rescale factors and its part's token
+//             weights w_t = sLc_t P_TOP / s_ref in shared memory and sends them
+//             with one bulk copy to the context CTA.
 // Context CTA (rank 1), per tile:
-//   eight warps turn the received p into the context operand in place,
+//   sixteen warps turn the received p into the context operand in place,
 //   P''[h][t] = p w_t (f16) as two e4m3 terms, hi + lo; zero the V rows without
 //   data; rescale the O rows of heads whose factor moved, one half of O while the
 //   MMAs of the other half run; and write the partial o at the end.
@@ -66,22 +67,25 @@ namespace {
 using namespace ptx;
 
 constexpr int HG = 128;                      // heads per work item
-constexpr int NTHREADS = 320;                // warp 0 TMA, warp 1 MMA, warps 2..9 lane workers
-constexpr int W_TMA = 0, W_MMA = 1, W_LANE = 2, N_LANE_WARPS = 8;
+constexpr int W_TMA = 0, W_MMA = 1, W_LANE = 2;
+constexpr int N_LANE_WARPS = 16;             // four per TMEM lane quarter
+constexpr int NTHREADS = (W_LANE + N_LANE_WARPS) * 32;
+constexpr int PART = TILE / 4;               // 32 tokens: a lane warp's share of a tile
 constexpr int KBLK = TILE * 128;             // 16 KB: [128 tokens x 128 bytes]
 constexpr int BLKS = 5;                      // K blocks per tile: Lc 0..3, Rc
 constexpr int NKS = 2 * BLKS;                // K-block ring slots (score CTA): two tiles
 constexpr int NSC = 4;                       // scale ring slots (score CTA), one tile each
 constexpr int VTILE = 4 * KBLK;              // 64 KB: the tile's Lc, four d-blocks
 constexpr int NVT = 2;                       // V ring slots (context CTA), one tile each
-// Payload of one tile, one chunk per softmax warp (chunk c = page * 4 + lane
-// quarter; the context CTA registers the bytes it expects on its own barrier): p as f16 for its 32 heads x 64 tokens (rows of 128 bytes, 16-byte
-// units swizzled by the row), the O rescale factors of its heads, the token
-// weights of its page, and s_ref.
-constexpr int C_P16 = 0, C_FCOL = 4096, C_W = C_FCOL + 32 * 4, C_EXTRA = C_W + 64 * 4;
-constexpr int CHUNK = C_EXTRA + 16;          // 4496 bytes
+// Payload of one tile, one chunk per lane warp (chunk c = part * 4 + lane
+// quarter; the context CTA registers the bytes it expects on its own barrier):
+// p as f16 for its 32 heads x 32 tokens (rows of 64 bytes, 16-byte units
+// swizzled by the row), the O rescale factors of its heads, the token weights of
+// its part (f16), and s_ref.
+constexpr int C_P16 = 0, C_FCOL = 32 * PART * 2, C_W = C_FCOL + 32 * 4, C_EXTRA = C_W + PART * 2;
+constexpr int CHUNK = C_EXTRA + 16;          // 2256 bytes
 constexpr int P_BYTES = N_LANE_WARPS * CHUNK;
-constexpr int P_STRIDE = 36 * 1024;
+constexpr int P_STRIDE = 37 * 1024;
 constexpr int L2_AHEAD = 3;                  // tiles prefetched into L2 ahead of the K loads
 constexpr float TAU = 1.0f;
 constexpr float TAU_S = 2.0f;
@@ -99,13 +103,13 @@ constexpr int B_KEMPTY = B_KT + 2;           // [NKS] score: K block consumed by
 constexpr int B_SCFULL = B_KEMPTY + NKS;     // [NSC] score: row scales of a tile loaded
 constexpr int B_SCEMPTY = B_SCFULL + NSC;    // [NSC] score: row scales read by the softmax
 constexpr int B_SFULL = B_SCEMPTY + NSC;     // score: S of a tile in TMEM
-constexpr int B_SEMPTY = B_SFULL + 1;        // score: S read and next tile's K loaded (8 arrivals)
-constexpr int B_PX = B_SEMPTY + 1;           // [4] score: the two warps of a lane quarter meet
+constexpr int B_SEMPTY = B_SFULL + 1;        // score: S read and next tile's K loaded (16 arrivals)
+constexpr int B_PX = B_SEMPTY + 1;           // [4] score: the four warps of a lane quarter meet
 constexpr int B_VT = B_PX + 4;               // [NVT] context: V tile loaded
 constexpr int B_VEMPTY = B_VT + NVT;         // [NVT] context: V tile consumed
 constexpr int B_PFULL = B_VEMPTY + NVT;      // [2] context: payload of a tile arrived (bulk-copy bytes)
-constexpr int B_CVT = B_PFULL + 2;           // context: the payload is read, its buffer may be overwritten (8 arrivals)
-constexpr int B_RS = B_CVT + 1;              // [2] context: operand, V rows and O half ready (8 arrivals)
+constexpr int B_CVT = B_PFULL + 2;           // context: the payload is read, its buffer may be overwritten (16 arrivals)
+constexpr int B_RS = B_CVT + 1;              // [2] context: operand, V rows and O half ready (16 arrivals)
 constexpr int B_ODONE = B_RS + 2;            // [2] context: MMAs of an O half done
 constexpr int B_DRAIN = B_ODONE + 2;
 constexpr int NBAR = B_DRAIN + 1;
@@ -113,15 +117,16 @@ constexpr int NBAR = B_DRAIN + 1;
 // shared memory (offsets from the 1024-aligned base)
 constexpr int OFF_BAR = 0;
 constexpr int OFF_FLAGS = 512;               // tmem base, abort flag
+constexpr int OFF_FACTS = OFF_FLAGS + 16;    // [4] page facts of the tiles in the scale / V ring
 constexpr int OFF_CS = 1024;                 // score: c_h per head
-constexpr int OFF_XMAX = OFF_CS + HG * 4;    // score: [2 tiles][2 pages][128] page maxima
-constexpr int OFF_XSM = OFF_XMAX + 4 * HG * 4;  // score: [2 tiles][2 pages][4] page row-scale maxima
-constexpr int OFF_XL = OFF_XSM + 64;         // score: [2 pages][128] denominators
-constexpr int OFF_XA = OFF_XL + 2 * HG * 4;  // score: [2 halves][128] query maxima
-constexpr int OFF_QR = 6144;                 // score: [128 heads x 128 bytes]: Rc query hi | lo
+constexpr int OFF_XMAX = OFF_CS + HG * 4;    // score: [2 tiles][4 parts][128] part maxima
+constexpr int OFF_XA = OFF_XMAX;             // score, before the first tile: [4 quarters][128] query maxima
+constexpr int OFF_XSM = OFF_XMAX + 8 * HG * 4;  // score: [2 tiles][4 parts][4] part row-scale maxima
+constexpr int OFF_XL = OFF_XSM + 32 * 4;     // score: [4 parts][128] denominators
+constexpr int OFF_QR = 8192;                 // score: [128 heads x 128 bytes]: Rc query hi | lo
 constexpr int OFF_KRING = OFF_QR + KBLK;
 constexpr int OFF_SCR = OFF_KRING + NKS * KBLK;  // [NSC][128 tokens][2] f32
-constexpr int OFF_STG = OFF_SCR + NSC * TILE * 8;  // [8 warps] staged payload chunks
+constexpr int OFF_STG = OFF_SCR + NSC * TILE * 8;  // [16 warps] staged payload chunks
 constexpr int TOTAL_S = OFF_STG + P_BYTES;
 constexpr int OFF_P = 4096;                  // context: 2 payloads / context operands
 constexpr int OFF_VRING = OFF_P + 2 * P_STRIDE;
@@ -130,8 +135,9 @@ constexpr int SMEM = (TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C) + 1024;
 // score CTA TMEM columns: S_L, S_R (one tile), then the Lc query's hi and lo terms
 // (e4m3, four channels per column) as the A operand of the score MMAs
 constexpr int T_SL = 0, T_SR = 128, T_QH = 256, T_QL = 384;
-static_assert(OFF_XA + 2 * HG * 4 <= OFF_QR, "score CTA scratch overlaps the Rc query");
-static_assert(NBAR * 8 <= OFF_FLAGS, "barriers overlap the flags");
+static_assert(OFF_XL + 4 * HG * 4 <= OFF_QR, "score CTA scratch overlaps the Rc query");
+static_assert(4 * HG * 4 <= 8 * HG * 4, "query maxima fit in the part maxima");
+static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + 16 <= OFF_CS, "barriers, flags and facts overlap");
 static_assert(P_BYTES <= P_STRIDE && (P_STRIDE % 1024) == 0 && (OFF_VRING % 1024) == 0,
               "payload layout");
 static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits in its payload buffer");
@@ -155,6 +161,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ uint32_t sw128(int r, int u) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
 }
+// byte offset of 16-byte unit u (0..3) of head row r of a payload chunk: rows of
+// 64 bytes, the unit index turned by the row so that the eight rows a quarter
+// warp touches at once fall on distinct banks
+__device__ __forceinline__ uint32_t prow(int r, int u) {
+  return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+}
 
 // Two e4m3 terms of four f32 values already on the head's scale: hi = e4m3(x),
 // lo = e4m3(x - hi) (the difference is exact in f32).
@@ -177,7 +189,40 @@ __device__ __forceinline__ void split_h2(__half2 x, uint16_t& hi, uint16_t& lo) 
   lo = f16x2_to_e4m3x2(__hsub2(x, *reinterpret_cast<const __half2*>(&d)));
 }
 
-// Per-tile page facts, the same in every warp that asks.
+// Packed pairs of f32 (element 0 in the low half) and the sm_100 two-lane f32
+// instructions; each lane is rounded exactly as the scalar instruction would be.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 up2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Per-tile page facts.
 struct TileRows {
   int64_t s0, s1;  // cache slot of the tile's first / second page, or -1 (absent or unmapped)
   int nv;          // tokens of the tile inside the item
@@ -191,6 +236,22 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int64_
   r.s0 = slot_of(a, b, tb);
   r.s1 = r.nv > PAGE ? slot_of(a, b, tb + PAGE) : -1;
   return r;
+}
+// The facts packed in a word the loading thread leaves in shared memory for the
+// lane warps: tokens inside the item (0..128) in bits 0..7, first / second page
+// present in bits 8 / 9.
+constexpr uint32_t FULL_TILE = TILE | 0x300u;
+__device__ __forceinline__ uint32_t pack_facts(const TileRows& r) {
+  return (uint32_t)r.nv | (r.s0 >= 0 ? 0x100u : 0u) | (r.s1 >= 0 ? 0x200u : 0u);
+}
+// tokens with data in part k (tokens [32 k, 32 k + 32)) of the tile
+__device__ __forceinline__ int part_tokens(uint32_t f, int k) {
+  const int n = (int)(f & 0xFFu) - PART * k;
+  return ((f >> (8 + (k >> 1))) & 1u) ? min(max(n, 0), PART) : 0;
+}
+// row r of the tile holds data
+__device__ __forceinline__ bool row_has(uint32_t f, int r) {
+  return r < (int)(f & 0xFFu) && ((f >> (8 + r / PAGE)) & 1u) != 0u;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
@@ -223,6 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_FLAGS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_FLAGS + 4);
+  uint32_t* facts = reinterpret_cast<uint32_t*>(sm + OFF_FACTS);
   auto fail = [&]() {
     *abort_flag = 1;
     atomicOr(a.err, ERR_TIMEOUT);
@@ -243,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(&bars[B_SFULL], 1);
     mbar_init(&bars[B_SEMPTY], N_LANE_WARPS);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PX + i], 2);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PX + i], N_LANE_WARPS / 4);
     for (int i = 0; i < NVT; ++i) {
       mbar_init(&bars[B_VT + i], 1);
       mbar_init(&bars[B_VEMPTY + i], 1);
@@ -268,69 +330,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   if (rank == 0 && warp >= W_LANE) {
     // Query -> two e4m3 terms with a per-head power-of-two scale that puts max|q|
     // in [128, 256); c_h undoes it and folds in sm_scale * log2(e).  Thread
-    // (head hh, half hf) converts Lc channels [256 hf, 256 hf + 256) into TMEM
+    // (head hh, quarter hf) converts Lc channels [128 hf, 128 hf + 128) into TMEM
     // lane hh (four channels per column, channel 4j in the low byte of column j),
-    // and half 0 also the 64 Rc channels into row hh of the Rc operand in shared
-    // memory (hi in bytes 0..63, lo in 64..127).
+    // and quarter 0 also the 64 Rc channels into row hh of the Rc operand in
+    // shared memory (hi in bytes 0..63, lo in 64..127).  The rows reach the
+    // threads through a per-warp transpose buffer (4 KB of the K ring, unused
+    // until the loads start): 32 channels of the warp's 32 heads per round, read
+    // from global memory 128 contiguous bytes per eight lanes.
     const uint32_t tm = *tmem_slot;
     const int q = warp & 3, hf = (warp - W_LANE) >> 2, hh = q * 32 + lane, h = h0 + hh;
     const bool real = h < a.H;
-    const float4* src = reinterpret_cast<const float4*>(a.q_lat + ((int64_t)b * a.H + h) * DL) + 64 * hf;
-    const float2* rsrc = reinterpret_cast<const float2*>(a.q_rope + ((int64_t)b * a.H + h) * DR);
+    float4* stage = reinterpret_cast<float4*>(sm + OFF_KRING + (warp - W_LANE) * 4096);
+    const int64_t row0 = (int64_t)b * a.H + h0 + q * 32;  // the warp's first head row
+    // stage channels [c0, c0 + 32) of the warp's heads from rows of `width` floats,
+    // then return this thread's eight float4 of them
+    auto round = [&](const float* base, int width, int c0, float4 (&x)[8]) {
+      __syncwarp();  // the previous round's reads are done
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3), u = lane & 7;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (h0 + q * 32 + r < a.H)
+          v = __ldg(reinterpret_cast<const float4*>(base + (row0 + r) * width + c0) + u);
+        stage[r * 8 + (u ^ (r & 7))] = v;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = stage[lane * 8 + (u ^ (lane & 7))];
+    };
     float* xa = reinterpret_cast<float*>(sm + OFF_XA);
     float amax = 0.f;
-    if (real) {
-      for (int k = 0; k < 64; ++k) {
-        const float4 x = __ldg(src + k);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-      }
-      if (hf == 0)
-        for (int k = 0; k < 32; ++k) {
-          const float2 y = __ldg(rsrc + k);
-          amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
-        }
+    float4 x[8];
+#pragma unroll 1
+    for (int k = 0; k < 4 + (hf == 0 ? 2 : 0); ++k) {
+      if (k < 4) round(a.q_lat, DL, 128 * hf + 32 * k, x);
+      else round(a.q_rope, DR, 32 * (k - 4), x);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
     }
     xa[hf * HG + hh] = amax;
     named_bar_sync(1, N_LANE_WARPS * 32);
-    amax = fmaxf(xa[hh], xa[HG + hh]);
+    amax = fmaxf(fmaxf(xa[hh], xa[HG + hh]), fmaxf(xa[2 * HG + hh], xa[3 * HG + hh]));
     int e = 0;
     if (amax > 0.f && isfinite(amax)) {
-      int x;
-      frexpf(amax, &x);
-      e = min(max(8 - x, -120), 120);
+      int ex;
+      frexpf(amax, &ex);
+      e = min(max(8 - ex, -120), 120);
     }
     const float sc = ldexpf(1.0f, e);
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    const uint32_t qr = smem_u32(sm + OFF_QR);
 #pragma unroll 1
-    for (int ch = 0; ch < 2; ++ch) {
-      uint32_t hw[32], lw[32];
+    for (int k = 0; k < 4 + (hf == 0 ? 2 : 0); ++k) {
+      if (k < 4) round(a.q_lat, DL, 128 * hf + 32 * k, x);
+      else round(a.q_rope, DR, 32 * (k - 4), x);
+      uint32_t hw[8], lw[8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float4 x = real ? __ldg(src + ch * 32 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float v[4] = {x.x * sc, x.y * sc, x.z * sc, x.w * sc};
-        split4(v, hw[j], lw[j]);
+      for (int u = 0; u < 8; ++u) {
+        const float v[4] = {x[u].x * sc, x[u].y * sc, x[u].z * sc, x[u].w * sc};
+        split4(v, hw[u], lw[u]);
       }
-      __syncwarp();
-      tmem_st32(tm + lane_addr + T_QH + hf * 64 + ch * 32, hw);
-      tmem_st32(tm + lane_addr + T_QL + hf * 64 + ch * 32, lw);
-    }
-    if (hf == 0) {
-      const uint32_t qr = smem_u32(sm + OFF_QR);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float2 y0 = real ? __ldg(rsrc + 8 * u + 2 * k) : make_float2(0.f, 0.f);
-          float2 y1 = real ? __ldg(rsrc + 8 * u + 2 * k + 1) : make_float2(0.f, 0.f);
-          const float v[4] = {y0.x * sc, y0.y * sc, y1.x * sc, y1.y * sc};
-          split4(v, hw[k], lw[k]);
-        }
-        sts128(qr + sw128(hh, u), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-        sts128(qr + sw128(hh, u + 4), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      if (k < 4) {
+        __syncwarp();
+        tmem_st8(tm + lane_addr + T_QH + hf * 32 + k * 8, hw);
+        tmem_st8(tm + lane_addr + T_QL + hf * 32 + k * 8, lw);
+      } else {
+        // Rc channels [32 (k - 4), +32): hi units 2 (k - 4) + {0, 1}, lo units 4 + those
+        const int u0 = 2 * (k - 4);
+        sts128(qr + sw128(hh, u0), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+        sts128(qr + sw128(hh, u0 + 1), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+        sts128(qr + sw128(hh, 4 + u0), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+        sts128(qr + sw128(hh, 4 + u0 + 1), make_uint4(lw[4], lw[5], lw[6], lw[7]));
       }
-      cs[hh] = real ? a.sm_scale * LOG2E / sc : 0.f;
     }
+    if (hf == 0) cs[hh] = real ? a.sm_scale * LOG2E / sc : 0.f;
     __syncwarp();
     tmem_wait_st();
     fence_proxy_async_smem();
@@ -369,6 +443,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
+          // the tile's page facts travel with its row scales (the arrive releases them)
+          facts[sc] = pack_facts(tr);
           mbar_arrive_expect_tx(&bars[B_SCFULL + sc], 512u * pages);
           if (tr.s0 >= 0) tma_load_1d(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
           if (tr.s1 >= 0)
@@ -377,6 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           // the tile's five blocks complete on one barrier; a slot is free once the
           // MMAs of the tile two before have read it
           uint64_t* kt = &bars[B_KT + (i & 1)];
+#pragma unroll 1
           for (int blk = 0; blk < BLKS; ++blk) {
             const int j = i * BLKS + blk, ks = j % NKS;
             if (!mbar_wait(&bars[B_KEMPTY + ks], ((j / NKS) & 1) ^ 1, abort_flag, WAIT_NS)) {
@@ -410,8 +487,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t idS = idesc_f16(128, 128, false, false);  // e4m3 x e4m3 (format 0)
         const uint64_t kdesc = smem_desc(kring, 16, 1024, SW128);
         const uint64_t qdesc = smem_desc(qr, 16, 1024, SW128);
-        // tile 0's K blocks; a later tile's are waited for by the softmax warps
-        // before they release S, so one barrier per tile gates these MMAs
+        // tile 0's K blocks; a later tile's are waited for by a softmax warp before
+        // it releases S, so one barrier per tile gates these MMAs
         bool ok = mbar_wait(&bars[B_KT], 0, abort_flag, WAIT_NS);
         for (int i = 0; ok && i < n_tiles; ++i) {
           if (!mbar_wait(&bars[B_SEMPTY], (i & 1) ^ 1, abort_flag, WAIT_NS)) {
@@ -451,13 +528,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     } else {
       // ---------------------------------------------------------- softmax
       const int q = warp & 3;                  // TMEM lane quarter
-      const int pg = (warp - W_LANE) >> 2;     // page of the tile: tokens [64 pg, 64 pg + 64)
+      const int part = (warp - W_LANE) >> 2;   // part of the tile: tokens [32 part, 32 part + 32)
       const int hh = q * 32 + lane;            // head of the group = TMEM lane
-      const int chunk = pg * 4 + q;            // this warp's payload chunk
+      const int chunk = part * 4 + q;          // this warp's payload chunk
       const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-      float* xmax = reinterpret_cast<float*>(sm + OFF_XMAX);  // [2][2][128]
-      float* xsm = reinterpret_cast<float*>(sm + OFF_XSM);    // [2][2][4]
-      float* xl = reinterpret_cast<float*>(sm + OFF_XL);      // [2][128]
+      float* xmax = reinterpret_cast<float*>(sm + OFF_XMAX);  // [2][4][128]
+      float* xsm = reinterpret_cast<float*>(sm + OFF_XSM);    // [2][4][4]
+      float* xl = reinterpret_cast<float*>(sm + OFF_XL);      // [4][128]
       uint8_t* stg_p = sm + OFF_STG + chunk * CHUNK;
       const uint32_t stg = smem_u32(stg_p);
       const float c = cs[hh];
@@ -467,79 +544,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       float mu = -INFINITY, mhi = -INFINITY, lsum = 0.f, sref = 0.f;
       int px_phase = 0;
       bool ok = true;
-      auto pair_sync = [&]() -> bool {
+      auto quarter_sync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_PX + q]);
         return mbar_wait_warp(&bars[B_PX + q], (px_phase++) & 1, abort_flag, WAIT_NS);
       };
       for (int i = 0; i < n_tiles; ++i) {
         const int buf = i & 1, sc = i % NSC, pb = i & 1;
-        const TileRows tr = tile_rows(a, b, t0, t_end, i);
-        const int64_t my_slot = pg ? tr.s1 : tr.s0;
-        const int my_n = (my_slot >= 0) ? min(max(tr.nv - pg * PAGE, 0), PAGE) : 0;
+        // the tile's row scales and S, and the next tile's K blocks (waited for here
+        // by every warp, so that the MMA thread's one wait per tile covers both)
         if (!mbar_wait_warp(&bars[B_SCFULL + sc], (i / NSC) & 1, abort_flag, WAIT_NS) ||
-            !mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag, WAIT_NS)) {
+            !mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag, WAIT_NS) ||
+            (i + 1 < n_tiles &&
+             !mbar_wait_warp(&bars[B_KT + ((i + 1) & 1)], ((i + 1) >> 1) & 1, abort_flag, WAIT_NS))) {
           ok = false;
           break;
         }
+        const int my_n = part_tokens(facts[sc], part);
         tc_fence_after();
         __syncwarp();  // the TMEM loads are warp-collective: every lane, converged
-        // u = sLc S_L + sRc S_R for this thread's head and page, from the TMEM
-        // accumulators in two halves of 32 tokens (the row scales by broadcast
-        // loads: every lane reads the same 16 bytes)
-        const float4* sc4 = reinterpret_cast<const float4*>(sm + OFF_SCR + sc * TILE * 8) + pg * (PAGE / 2);
-        float u[PAGE];
-        float umax = -INFINITY;
-        const bool full = (my_n == PAGE);  // warp-uniform: every token of the page has data
+        // u = sLc S_L + sRc S_R for this thread's head and the part's 32 tokens, in
+        // token pairs, S read from TMEM in two halves of 16 tokens (the row scales by
+        // broadcast loads: every lane reads the same 16 bytes).  S is released as
+        // soon as both halves are in registers: the next tile's score MMAs overwrite
+        // it while this tile's softmax runs.
+        const float4* sc4 = reinterpret_cast<const float4*>(sm + OFF_SCR + sc * TILE * 8) + part * (PART / 2);
+        uint64_t u2[PART / 2];
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          uint32_t rl[32], rr[32];
-          tmem_ld32(tmem + lane_addr + T_SL + pg * PAGE + hlf * 32, rl);
-          tmem_ld32(tmem + lane_addr + T_SR + pg * PAGE + hlf * 32, rr);
+        for (int hl = 0; hl < 2; ++hl) {
+          uint32_t rl[16], rr[16];
+          tmem_ld16(tmem + lane_addr + T_SL + part * PART + 16 * hl, rl);
+          tmem_ld16(tmem + lane_addr + T_SR + part * PART + 16 * hl, rr);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int t = hlf * 32 + j;
-            const float4 s4 = sc4[t / 2];  // (sLc, sRc) of tokens t and t + 1
-            u[t] = fmaf(s4.y, __uint_as_float(rr[j]), s4.x * __uint_as_float(rl[j]));
-            u[t + 1] = fmaf(s4.w, __uint_as_float(rr[j + 1]), s4.z * __uint_as_float(rl[j + 1]));
+          for (int j = 0; j < 8; ++j) {
+            const float4 s4 = sc4[8 * hl + j];  // (sLc, sRc) of tokens 2j and 2j + 1 of the half
+            u2[8 * hl + j] = fma2(pk2(s4.y, s4.w), pk2(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1])),
+                                  mul2(pk2(s4.x, s4.z), pk2(__uint_as_float(rl[2 * j]), __uint_as_float(rl[2 * j + 1]))));
           }
         }
-        if (full) {
-#pragma unroll
-          for (int t = 0; t < PAGE; ++t) umax = fmaxf(umax, u[t]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < PAGE; ++t) {
-            u[t] = (t < my_n) ? u[t] : -INFINITY;
-            umax = fmaxf(umax, u[t]);
-          }
-        }
-        // the page's largest row scale: lane l holds tokens l and l + 32
-        const float2 sa = reinterpret_cast<const float2*>(sc4)[lane];
-        const float2 sb = reinterpret_cast<const float2*>(sc4)[lane + 32];
-        float smax = fmaxf(lane < my_n ? sa.x : 0.f, lane + 32 < my_n ? sb.x : 0.f);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
         tc_fence_before();
-        // S is read; the next tile's K blocks are waited for here, so that the MMA
-        // thread's one wait per tile covers both
-        if (i + 1 < n_tiles &&
-            !mbar_wait_warp(&bars[B_KT + ((i + 1) & 1)], ((i + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
-          ok = false;
-          break;
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
-        // tile maxima (score of this head, and row scale) over both pages
-        xmax[(buf * 2 + pg) * HG + hh] = umax;
-        if (lane == 0) xsm[(buf * 2 + pg) * 4 + q] = smax;
-        if (!pair_sync()) {
+        // tokens without data (a suffix of the part) get -inf, branch-free
+        float umax = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < PART / 2; ++j) {
+          float2 v = up2(u2[j]);
+          v.x = 2 * j < my_n ? v.x : -INFINITY;
+          v.y = 2 * j + 1 < my_n ? v.y : -INFINITY;
+          u2[j] = pk2(v.x, v.y);
+          umax = max3(umax, v.x, v.y);
+        }
+        // the part's largest row scale: lane l holds token l of the part
+        const float2 sa = reinterpret_cast<const float2*>(sc4)[lane];
+        float smax = lane < my_n ? sa.x : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        // tile maxima (score of this head, and row scale) over the four parts
+        xmax[(buf * 4 + part) * HG + hh] = umax;
+        if (lane == 0) xsm[(buf * 4 + part) * 4 + q] = smax;
+        if (!quarter_sync()) {
           ok = false;
           break;
         }
-        const float umax_t = fmaxf(xmax[(buf * 2) * HG + hh], xmax[(buf * 2 + 1) * HG + hh]);
-        smax = fmaxf(xsm[(buf * 2) * 4 + q], xsm[(buf * 2 + 1) * 4 + q]);
+        const float* xm = xmax + buf * 4 * HG + hh;
+        const float umax_t = fmaxf(fmaxf(xm[0], xm[HG]), fmaxf(xm[2 * HG], xm[3 * HG]));
+        const float* xs = xsm + buf * 16 + q;
+        smax = fmaxf(fmaxf(xs[0], xs[4]), fmaxf(xs[8], xs[12]));
         const float tmax = (c > 0.f) ? c * umax_t : -INFINITY;
         float mn = mu;
         if (tmax > mu + TAU) {
@@ -556,25 +628,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const float fcol = alpha * beta;
         lsum *= alpha;
         const float wk = sref > 0.f ? P_TOP / sref : 0.f;
-        const float mneg = -fmaxf(mu, -3.0e38f);
-        // p = 2^(z - m) as f16 pairs (tokens without data, and padding heads, 0; u is
-        // -inf there, and c = 0 only for padding heads)
-        uint32_t ph[PAGE / 2];
-        float ls0 = 0.f, ls1 = 0.f;
+        // p = 2^(c u - m) as f16 pairs; a padding head takes c = 1 and m = +inf, so
+        // that its weights are 0 (as are those of tokens without data: u = -inf)
+        const uint64_t c2 = live ? pk2(c, c) : pk2(1.f, 1.f);
+        const float mneg = live ? -fmaxf(mu, -3.0e38f) : -INFINITY;
+        const uint64_t m2 = pk2(mneg, mneg);
+        uint32_t ph[PART / 2];
+        uint64_t ls2 = pk2(0.f, 0.f);  // running sums of the even and the odd tokens
 #pragma unroll
-        for (int t = 0; t < PAGE; t += 2) {
-          const float p0 = live ? ex2_approx(fmaf(c, u[t], mneg)) : 0.f;
-          const float p1 = live ? ex2_approx(fmaf(c, u[t + 1], mneg)) : 0.f;
-          ls0 += p0;
-          ls1 += p1;
+        for (int j = 0; j < PART / 2; ++j) {
+          const float2 z = up2(fma2(c2, u2[j], m2));
+          const float p0 = ex2_approx(z.x), p1 = ex2_approx(z.y);
+          ls2 = add2(ls2, pk2(p0, p1));
           const __half2 h2 = __floats2half2_rn(p0, p1);
-          ph[t / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+          ph[j] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        lsum += ls0 + ls1;
-        // this page's token weights w_t = sLc_t P_TOP / s_ref (0 without data):
-        // lane l takes tokens l and l + 32
-        const float w_lo = (lane < my_n) ? sa.x * wk : 0.f;
-        const float w_hi = (lane + 32 < my_n) ? sb.x * wk : 0.f;
+        {
+          const float2 ls = up2(ls2);
+          lsum += ls.x + ls.y;
+        }
+        // the part's token weights w_t = sLc_t P_TOP / s_ref (0 without data): lane l
+        // takes token l
+        const float wt = (lane < my_n) ? sa.x * wk : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_SCEMPTY + sc]);
         // the context CTA must be done with this payload buffer's previous tile
@@ -587,12 +662,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
 #pragma unroll
-        for (int u16 = 0; u16 < 8; ++u16)
-          sts128(stg + C_P16 + lane * 128 + ((u16 ^ (lane & 7)) << 4),
+        for (int u16 = 0; u16 < 4; ++u16)
+          sts128(stg + C_P16 + prow(lane, u16),
                  make_uint4(ph[4 * u16], ph[4 * u16 + 1], ph[4 * u16 + 2], ph[4 * u16 + 3]));
         reinterpret_cast<float*>(stg_p + C_FCOL)[lane] = fcol;
-        reinterpret_cast<float*>(stg_p + C_W)[lane] = w_lo;
-        reinterpret_cast<float*>(stg_p + C_W)[lane + 32] = w_hi;
+        reinterpret_cast<__half*>(stg_p + C_W)[lane] = __float2half_rn(wt);
         if (lane == 0)
           *reinterpret_cast<uint4*>(stg_p + C_EXTRA) = make_uint4(__float_as_uint(sref), 0u, 0u, 0u);
         fence_proxy_async_smem();
@@ -606,13 +680,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (!ok) {
         fail();
       } else {
-        // denominators over both pages; the partial's (m, l) per head
-        xl[pg * HG + hh] = lsum;
-        if (pair_sync()) {
-          if (pg == 0 && h0 + hh < a.H) {
+        // denominators over the four parts; the partial's (m, l) per head
+        xl[part * HG + hh] = lsum;
+        if (quarter_sync()) {
+          if (part == 0 && h0 + hh < a.H) {
             const int64_t base = item * HG;
             a.ws_m[base + hh] = mu;
-            a.ws_l[base + hh] = xl[hh] + xl[HG + hh];
+            a.ws_l[base + hh] = (xl[hh] + xl[HG + hh]) + (xl[2 * HG + hh] + xl[3 * HG + hh]);
           }
         } else {
           fail();
@@ -643,6 +717,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
+          facts[vs] = pack_facts(tr);  // released by the arrive below
           mbar_arrive_expect_tx(&bars[B_VT + vs],
                                 4u * ((tr.s0 >= 0 ? 8192u : 0u) + (tr.s1 >= 0 ? 8192u : 0u)));
           for (int m = 0; m < 4; ++m) {
@@ -699,9 +774,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       // ---------------------------------------------------------- operand, V rows,
       // O rescale and epilogue
       const int q = warp & 3;
-      const int sub = (warp - W_LANE) >> 2;    // page of the tile / 128 columns of an O half
+      const int part = (warp - W_LANE) >> 2;   // part of the tile / 64 columns of an O half
       const int hh = q * 32 + lane;
-      const int chunk = sub * 4 + q;           // the payload chunk of these heads and tokens
+      const int chunk = part * 4 + q;          // the payload chunk of these heads and tokens
       const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
       bool ok = true;
       float sref_fin = 0.f;
@@ -712,22 +787,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           ok = false;
           break;
         }
-        // this thread's row of the payload (p for 64 tokens of head hh), the head's
-        // rescale factor and the page's token weights (as f16 pairs)
+        // this thread's row of the payload (p for 32 tokens of head hh), the head's
+        // rescale factor and the part's token weights (as f16 pairs)
         const uint32_t cb = pbuf + pb * P_STRIDE + chunk * CHUNK;
         const uint8_t* cp = sm + OFF_P + pb * P_STRIDE + chunk * CHUNK;
-        uint4 pv[8];
+        uint4 pv[4];
 #pragma unroll
-        for (int u16 = 0; u16 < 8; ++u16) pv[u16] = lds128(cb + C_P16 + lane * 128 + ((u16 ^ (lane & 7)) << 4));
+        for (int u16 = 0; u16 < 4; ++u16) pv[u16] = lds128(cb + C_P16 + prow(lane, u16));
         const float f = reinterpret_cast<const float*>(cp + C_FCOL)[lane];
         if (i == n_tiles - 1) sref_fin = reinterpret_cast<const float*>(cp + C_EXTRA)[0];
-        uint32_t wh[PAGE / 2];
+        uint32_t wh[PART / 2];
 #pragma unroll
-        for (int t = 0; t < PAGE; t += 4) {
-          const float4 w4 = reinterpret_cast<const float4*>(cp + C_W)[t / 4];
-          const __half2 a2 = __floats2half2_rn(w4.x, w4.y), b2 = __floats2half2_rn(w4.z, w4.w);
-          wh[t / 2] = *reinterpret_cast<const uint32_t*>(&a2);
-          wh[t / 2 + 1] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int k = 0; k < PART / 8; ++k) {
+          const uint4 w8 = lds128(cb + C_W + 16 * k);  // f16 weights of tokens 8k .. 8k + 7
+          wh[4 * k] = w8.x;
+          wh[4 * k + 1] = w8.y;
+          wh[4 * k + 2] = w8.z;
+          wh[4 * k + 3] = w8.w;
         }
         const bool any = __any_sync(0xffffffffu, f != 1.f) && i > 0;
         // every warp has read this payload: its buffer may now take the operand
@@ -745,7 +821,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // (K-major, 128-byte swizzle) of the same buffer
         const uint32_t opnd = pbuf + pb * P_STRIDE;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 16 tokens per 16-byte unit
+        for (int j = 0; j < 2; ++j) {  // 16 tokens per 16-byte unit
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -762,26 +838,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             hw[k] = (uint32_t)h01 | ((uint32_t)h23 << 16);
             lw[k] = (uint32_t)l01 | ((uint32_t)l23 << 16);
           }
-          const uint32_t off = sw128(hh, sub * 4 + j);
+          const uint32_t off = sw128(hh, part * 2 + j);
           sts128(opnd + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
           sts128(opnd + KBLK + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
         }
         // V tile: rows without data (past the item, or a page that is absent or
         // unmapped) are zeroed so that their zero weights meet no NaN; warp w takes
-        // rows r = w (mod 8), a lane one 16-byte unit of one d-block
+        // rows r = w (mod 16), a lane one 16-byte unit of one d-block
         if (!mbar_wait_warp(&bars[B_VT + vs], (i / NVT) & 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
-        const TileRows tr = tile_rows(a, b, t0, t_end, i);
-        if (tr.s0 < 0 || tr.s1 < 0 || tr.nv < TILE) {
+        const uint32_t vf = facts[vs];
+        if (vf != FULL_TILE) {
           const uint32_t vb = vring + vs * VTILE;
-          for (int r = warp - W_LANE; r < TILE; r += N_LANE_WARPS) {
-            const bool has = r < tr.nv && (r < PAGE ? tr.s0 >= 0 : tr.s1 >= 0);
-            if (!has) sts128(vb + (lane >> 3) * KBLK + r * 128 + (lane & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
-          }
+          for (int r = warp - W_LANE; r < TILE; r += N_LANE_WARPS)
+            if (!row_has(vf, r))
+              sts128(vb + (lane >> 3) * KBLK + r * 128 + (lane & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
         }
         fence_proxy_async_smem();
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           if (any) {
             if (!mbar_wait_warp(&bars[B_ODONE + half], (i - 1) & 1, abort_flag, WAIT_NS)) {
@@ -790,20 +866,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
             tc_fence_after();
             __syncwarp();
-            const uint32_t col = tmem + lane_addr + half * 256 + sub * 128;
+            const uint32_t col = tmem + lane_addr + half * 256 + part * 64;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 64) {
-              uint32_t r0[32], r1[32];
-              tmem_ld32(col + c0, r0);
-              tmem_ld32(col + c0 + 32, r1);
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+              uint32_t r[16];
+              tmem_ld16(col + c0, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                r0[k] = __float_as_uint(__uint_as_float(r0[k]) * f);
-                r1[k] = __float_as_uint(__uint_as_float(r1[k]) * f);
-              }
-              tmem_st32(col + c0, r0);
-              tmem_st32(col + c0 + 32, r1);
+              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * f);
+              tmem_st16(col + c0, r);
             }
             __syncwarp();
             tmem_wait_st();
@@ -827,9 +898,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const bool mine = h0 + hh < a.H;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-          const int cbase = half * 256 + sub * 128;
+          const int cbase = half * 256 + part * 64;
 #pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+          for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r[32];
             __syncwarp();
             tmem_ld32(tmem + lane_addr + cbase + c0, r);
