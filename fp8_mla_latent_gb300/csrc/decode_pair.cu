@@ -101,8 +101,7 @@ constexpr int B_PFREE = 0;                   // [2] score: the context MMAs of t
 constexpr int B_KT = B_PFREE + 2;            // [2] score: all K blocks of a tile loaded (by tile parity)
 constexpr int B_KEMPTY = B_KT + 2;           // [NKS] score: K block consumed by the score MMAs
 constexpr int B_SCFULL = B_KEMPTY + NKS;     // [NSC] score: row scales of a tile loaded
-constexpr int B_SCEMPTY = B_SCFULL + NSC;    // [NSC] score: row scales read by the softmax
-constexpr int B_SFULL = B_SCEMPTY + NSC;     // score: S of a tile in TMEM
+constexpr int B_SFULL = B_SCFULL + NSC;      // score: S of a tile in TMEM
 constexpr int B_SEMPTY = B_SFULL + 1;        // score: S read and next tile's K loaded (16 arrivals)
 constexpr int B_PX = B_SEMPTY + 1;           // [4] score: the four warps of a lane quarter meet
 constexpr int B_VT = B_PX + 4;               // [NVT] context: V tile loaded
@@ -299,10 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars[B_ODONE + i], 1);
     }
     for (int i = 0; i < NKS; ++i) mbar_init(&bars[B_KEMPTY + i], 1);
-    for (int i = 0; i < NSC; ++i) {
-      mbar_init(&bars[B_SCFULL + i], 1);
-      mbar_init(&bars[B_SCEMPTY + i], N_LANE_WARPS);
-    }
+    for (int i = 0; i < NSC; ++i) mbar_init(&bars[B_SCFULL + i], 1);
     mbar_init(&bars[B_SFULL], 1);
     mbar_init(&bars[B_SEMPTY], N_LANE_WARPS);
     for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PX + i], N_LANE_WARPS / 4);
@@ -439,19 +435,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           const TileRows tr = tile_rows(a, b, t0, t_end, i);
           const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
           const int sc = i % NSC;
-          if (!mbar_wait(&bars[B_SCEMPTY + sc], ((i / NSC) & 1) ^ 1, abort_flag, WAIT_NS)) {
-            ok = false;
-            break;
-          }
-          // the tile's page facts travel with its row scales (the arrive releases them)
-          facts[sc] = pack_facts(tr);
-          mbar_arrive_expect_tx(&bars[B_SCFULL + sc], 512u * pages);
-          if (tr.s0 >= 0) tma_load_1d(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
-          if (tr.s1 >= 0)
-            tma_load_1d(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
-          ++nsc;
           // the tile's five blocks complete on one barrier; a slot is free once the
-          // MMAs of the tile two before have read it
+          // MMAs of the tile two before have read it.  Those MMAs started after the
+          // softmax warps had released tile i - 3, and a warp reads every row
+          // scale and page fact of a tile before it releases it, so the scale slot
+          // of tile i - 4 is free then too.
           uint64_t* kt = &bars[B_KT + (i & 1)];
 #pragma unroll 1
           for (int blk = 0; blk < BLKS; ++blk) {
@@ -461,6 +449,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
               break;
             }
             if (blk == 0) {
+              // the tile's page facts travel with its row scales (the arrive releases them)
+              facts[sc] = pack_facts(tr);
+              mbar_arrive_expect_tx(&bars[B_SCFULL + sc], 512u * pages);
+              if (tr.s0 >= 0) tma_load_1d(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
+              if (tr.s1 >= 0)
+                tma_load_1d(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
+              nsc = i + 1;
               mbar_arrive_expect_tx(kt, 8192u * pages * BLKS);
               nk = i + 1;
             }
@@ -562,13 +557,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         const int my_n = part_tokens(facts[sc], part);
         tc_fence_after();
-        __syncwarp();  // the TMEM loads are warp-collective: every lane, converged
+        // this warp's previous payload copy has read its staging chunk, whose first
+        // 256 bytes now take the part's row scales in planar order (sLc of the 32
+        // tokens, then sRc); lane l reads token l's pair
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        const float2 sa = reinterpret_cast<const float2*>(sm + OFF_SCR + sc * TILE * 8)[part * PART + lane];
+        reinterpret_cast<float*>(stg_p)[lane] = sa.x;
+        reinterpret_cast<float*>(stg_p)[PART + lane] = sa.y;
+        __syncwarp();  // also: the TMEM loads are warp-collective (every lane, converged)
         // u = sLc S_L + sRc S_R for this thread's head and the part's 32 tokens, in
-        // token pairs, S read from TMEM in two halves of 16 tokens (the row scales by
+        // token pairs, S read from TMEM in two halves of 16 tokens (the scales by
         // broadcast loads: every lane reads the same 16 bytes).  S is released as
         // soon as both halves are in registers: the next tile's score MMAs overwrite
         // it while this tile's softmax runs.
-        const float4* sc4 = reinterpret_cast<const float4*>(sm + OFF_SCR + sc * TILE * 8) + part * (PART / 2);
+        const float4* sl4 = reinterpret_cast<const float4*>(stg_p);
+        const float4* sr4 = reinterpret_cast<const float4*>(stg_p + PART * 4);
         uint64_t u2[PART / 2];
 #pragma unroll
         for (int hl = 0; hl < 2; ++hl) {
@@ -577,27 +581,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           tmem_ld16(tmem + lane_addr + T_SR + part * PART + 16 * hl, rr);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 s4 = sc4[8 * hl + j];  // (sLc, sRc) of tokens 2j and 2j + 1 of the half
-            u2[8 * hl + j] = fma2(pk2(s4.y, s4.w), pk2(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1])),
-                                  mul2(pk2(s4.x, s4.z), pk2(__uint_as_float(rl[2 * j]), __uint_as_float(rl[2 * j + 1]))));
+          for (int k = 0; k < 4; ++k) {  // tokens 16 hl + 4k .. + 3
+            const float4 l4 = sl4[4 * hl + k], r4 = sr4[4 * hl + k];
+            const int j = 2 * k;
+            u2[8 * hl + j] = fma2(pk2(r4.x, r4.y), pk2(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1])),
+                                  mul2(pk2(l4.x, l4.y), pk2(__uint_as_float(rl[2 * j]), __uint_as_float(rl[2 * j + 1]))));
+            u2[8 * hl + j + 1] = fma2(pk2(r4.z, r4.w), pk2(__uint_as_float(rr[2 * j + 2]), __uint_as_float(rr[2 * j + 3])),
+                                      mul2(pk2(l4.z, l4.w), pk2(__uint_as_float(rl[2 * j + 2]), __uint_as_float(rl[2 * j + 3]))));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
-        // tokens without data (a suffix of the part) get -inf, branch-free
+        // tokens without data (a suffix of the part, in a partial tile) get -inf
+        if (my_n < PART) {
+#pragma unroll
+          for (int j = 0; j < PART / 2; ++j) {
+            const float2 v = up2(u2[j]);
+            u2[j] = pk2(2 * j < my_n ? v.x : -INFINITY, 2 * j + 1 < my_n ? v.y : -INFINITY);
+          }
+        }
         float umax = -INFINITY;
 #pragma unroll
         for (int j = 0; j < PART / 2; ++j) {
-          float2 v = up2(u2[j]);
-          v.x = 2 * j < my_n ? v.x : -INFINITY;
-          v.y = 2 * j + 1 < my_n ? v.y : -INFINITY;
-          u2[j] = pk2(v.x, v.y);
+          const float2 v = up2(u2[j]);
           umax = max3(umax, v.x, v.y);
         }
         // the part's largest row scale: lane l holds token l of the part
-        const float2 sa = reinterpret_cast<const float2*>(sc4)[lane];
         float smax = lane < my_n ? sa.x : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
@@ -650,17 +660,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // the part's token weights w_t = sLc_t P_TOP / s_ref (0 without data): lane l
         // takes token l
         const float wt = (lane < my_n) ? sa.x * wk : 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_SCEMPTY + sc]);
         // the context CTA must be done with this payload buffer's previous tile
         if (i >= 2 &&
             !mbar_wait_warp(&bars[B_PFREE + pb], ((i >> 1) + 1) & 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
-        // this warp's previous bulk copy has read the staging chunk
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+        // the payload goes to the staging chunk (its previous copy was waited for
+        // at the top of the tile)
 #pragma unroll
         for (int u16 = 0; u16 < 4; ++u16)
           sts128(stg + C_P16 + prow(lane, u16),
@@ -857,13 +864,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
               sts128(vb + (lane >> 3) * KBLK + r * 128 + (lane & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
         }
         fence_proxy_async_smem();
+        // Each O half: the previous tile's MMAs on it are done (waited for on every
+        // tile, rescale or not: the operand-ready barrier of this half then runs at
+        // most one phase ahead of the MMA thread that waits on it), then the rows of
+        // heads whose factor moved are rescaled, then the half is released.
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
+          if (i > 0 &&
+              !mbar_wait_warp(&bars[B_ODONE + half], (i - 1) & 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
+          }
           if (any) {
-            if (!mbar_wait_warp(&bars[B_ODONE + half], (i - 1) & 1, abort_flag, WAIT_NS)) {
-              ok = false;
-              break;
-            }
             tc_fence_after();
             __syncwarp();
             const uint32_t col = tmem + lane_addr + half * 256 + part * 64;

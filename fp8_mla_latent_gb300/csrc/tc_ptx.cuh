@@ -40,33 +40,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait that suspends the thread (it issues nothing meanwhile) until the
-// phase completes or about `hint_ns` pass, whichever is first.
-constexpr uint32_t WAIT_SUSPEND_NS = 20000;
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
-                                                      uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time (or as soon as *abort is set by another warp) and
-// returns false; the caller then records the error and unwinds.  The waiting
-// thread is suspended between checks, so a waiting warp takes no issue slots
-// from the warps that share its SM sub-partition.
+// returns false; the caller then records the error and unwinds.  Each check is a
+// plain try_wait, which the hardware may suspend for a time of its own choosing,
+// so a waiting warp takes few issue slots from the warps beside it.
+//
+// A parity wait names a phase only modulo 2: every protocol built on these waits
+// keeps its arrivers at most one phase ahead of each waiter (a waiter whose
+// barrier has moved two phases on waits for a third that never comes).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, WAIT_SUSPEND_NS)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }
@@ -385,8 +373,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Wait by every lane of a converged warp (each suspends on the barrier until
-// the phase completes); true in every lane only if every lane saw it complete.
+// Wait by every lane of a converged warp (each waits on the barrier until the
+// phase completes); true in every lane only if every lane saw it complete.
 // (Leaving lanes parked at a warp barrier while one lane polls costs the other
 // warps of the SM sub-partition most of their issue rate.)
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
@@ -427,25 +415,12 @@ __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool try_wait_cluster_suspend(uint64_t* bar, uint32_t parity,
-                                                         uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait with a cluster-scope acquire, for barriers the peer CTA arrives on
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
                                                   const volatile int* abort, uint64_t limit_ns) {
   if (try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (try_wait_cluster_suspend(bar, parity, WAIT_SUSPEND_NS)) return true;
+    if (try_wait_cluster(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }
