@@ -329,9 +329,15 @@ def run_ours(args, rank, world, local_rank):
     else:
         kernel = "decode_simt"
         alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": flops / (ms_dec * 1e-3) / 1e12, "peak": alu_peak,
-                "unit": "TFLOP/s",
-                "peak_note": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}
+        t_alu = flops / (alu_peak * 1e12)
+        t_hbm = w.kv_bytes() / (peaks["hbm_gbs"] * 1e9)
+        if t_alu >= t_hbm:
+            roof = {"bound": "alu", "achieved": flops / (ms_dec * 1e-3) / 1e12, "peak": alu_peak,
+                    "unit": "TFLOP/s",
+                    "peak_note": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}
+        else:
+            roof = {"bound": "hbm", "achieved": w.kv_bytes() / (ms_dec * 1e-3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_note": f"{peaks['src']} copy"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic_for(kernel, args.workload)
     roof["kernel"] = kernel
@@ -342,8 +348,8 @@ def run_ours(args, rank, world, local_rank):
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f32 accum",
-        "data": "synthetic (seeded; shapes and value mix of the workload, see DESIGN.md)",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[plan_variant],
+        "data": "synthetic (seeded; the workload's shapes, page layout and value mix)",
         "token_heads_per_s": tok_heads / (ms_step * 1e-3),
         "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H,
                    "T_total": w.total_tokens, "kv_lora": 512, "qk_rope": 64,
@@ -360,6 +366,18 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed": t_wall,
     }
     return res, w
+
+
+# the decode configs, in the order of the lines; the long-context one, the headline,
+# comes last
+DECODE_ORDER = ("tiny", "single", "batched", "append", "long")
+
+# what each decode kernel computes in (the cache is e4m3 in every case)
+DTYPES = {
+    1: "e4m3 cache; f32 arithmetic on CUDA cores",
+    3: "e4m3 cache; fp16 query and two-term e4m3 weights on tcgen05; f32 accumulation",
+    4: "e4m3 cache; two-term e4m3 query and two-term e4m3 weights on tcgen05; f32 accumulation",
+}
 
 
 PRODUCE_METRIC = "fp8-latent fused producer (RMS norm + rotary + e4m3 quantize + paged write): GB/s"
@@ -436,7 +454,7 @@ def run_produce(args, rank, world, local_rank):
         "metric": PRODUCE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 in, e4m3 + f32 scales out",
-        "data": "synthetic (seeded; append-workload value mix, see DESIGN.md)",
+        "data": "synthetic (seeded; the append workload's value mix)",
         "rows_per_s": world * n / (ms * 1e-3),
         "config": {"workload": "produce", "rows": n, "max_pos": int(p.rope_cos.shape[0]),
                    "l2": "flushed between steps (256 MB write); rows > L2",
@@ -786,16 +804,20 @@ def tc_built(pkg, dev):
 
 
 # ----------------------------------------------------------------- oracle (CPU) arm
-def oracle_sample(w, budget_s, codes=None, scales=None):
-    """Time the f32 oracle (OpenMP, all cores) on a bounded sample of the workload:
-    sequence 0, the first n heads, n sized to about budget_s of wall time."""
+def oracle_sample(w, budget_s, codes=None, scales=None, n_threads=None):
+    """Time the f32 oracle (OpenMP over heads; all cores unless n_threads) on a
+    bounded sample of the workload: sequence 0, the first n heads, n sized to about
+    budget_s of wall time.  value is the sample's rate (KV bytes of the heads it
+    covered per second), the same rate the whole job would run at."""
     import oracle
     if codes is None:
         codes, scales = oracle.quantize_rows(w.cache_rows, dst_slot=w.cache_slots,
                                              n_slots=w.n_slots)
         if w.fresh_rows is not None:
             oracle.quantize_rows(w.fresh_rows, dst_slot=w.fresh_slots, codes=codes, scales=scales)
-    cores = oracle.max_threads()
+    # the thread count is always passed explicitly: the OpenMP setting a call makes
+    # outlives it, so asking the runtime after a one-core sample would answer 1
+    cores = len(os.sched_getaffinity(0)) if n_threads is None else int(n_threads)
     b = 0
     T = int(w.seq_lens[b])
 
@@ -812,13 +834,22 @@ def oracle_sample(w, budget_s, codes=None, scales=None):
     n2 = int(max(1, min(w.H, budget_s / max(per_head, 1e-6))))
     if n2 > nh:
         nh, t1 = n2, run(n2)
-    # full-job time: every (sequence, head) at the sample's per-head rate
+    # the rate: KV bytes per (token, head) share, over the sample's time
     per_tok_head = t1 / (nh * T)
     t_full = per_tok_head * w.total_tokens * w.H
     value = w.kv_bytes() / t_full / 1e9
     sample = f"sequence 0 ({T} tokens) x {nh} of {w.H} heads, f32 oracle, {t1:.2f} s wall"
     return {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-            "seconds": t1}, (codes, scales)
+            "seconds": t1, "projected_full_job_s": t_full}, (codes, scales)
+
+
+def cpu_baselines(w, budget_s):
+    """The oracle on all host cores (the reported value) and on one core."""
+    allc, cache = oracle_sample(w, budget_s)
+    one, _ = oracle_sample(w, budget_s, *cache, n_threads=1)
+    res = {k: allc[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    res["one_core"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
+    return res
 
 
 def run_reference(args, world):
@@ -872,24 +903,36 @@ def run_reference(args, world):
             "cpu_baseline": dict(vals[-1], value=value),
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
-    w = workloads.make(args.workload)
+    return ref_decode(args.workload, args, world, 1.0)
+
+
+def ref_decode(name, args, world, budget_s):
+    """The oracle arm on one decode workload: each step a bounded sample (sequence 0,
+    as many heads as fit in budget_s).  ms_per_step is the measured time of the
+    sample; value is its rate, which the whole job would run at."""
+    from fp8_mla_latent_gb300 import workloads
+    w = workloads.make(name)
     cache = None
     for _ in range(args.warmup):
-        _, cache = oracle_sample(w, 0.2, *(cache or (None, None)))
+        _, cache = oracle_sample(w, min(0.2, budget_s), *(cache or (None, None)))
     vals, secs = [], []
     cb = None
     for _ in range(args.steps):
-        cb, cache = oracle_sample(w, 1.0, *cache)
+        cb, cache = oracle_sample(w, budget_s, *cache)
         vals.append(cb["value"])
         secs.append(cb["seconds"])
     value = float(np.mean(vals))
-    ms = w.kv_bytes() / (value * 1e9) * 1e3
+    ms = float(np.mean(secs)) * 1e3
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; same workload as our arm)",
-        "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H, "T_total": w.total_tokens},
+        "config": {"workload": name, "scale": args.scale, "B": w.B, "H": w.H,
+                   "T_total": w.total_tokens},
+        "step": "a bounded sample of the workload: " + cb["sample"] +
+                "; ms_per_step is that sample's measured time",
+        "projected_full_job_ms": w.kv_bytes() / (value * 1e9) * 1e3,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
                          "sample": cb["sample"] + f"; {args.steps} steps"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -903,7 +946,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="long")
+    ap.add_argument("--workload", default="all",
+                    help="a decode workload, 'all' (one line per decode config, the long one "
+                         "last), or produce / wuv / prefill / persist")
     ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05", "tc_cta", "tc_pair"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -919,7 +964,12 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, world)), flush=True)
+            if args.workload == "all":
+                for name in DECODE_ORDER:
+                    print(json.dumps(ref_decode(name, args, world, 1.0 if name == "long" else 0.25)),
+                          flush=True)
+            else:
+                print(json.dumps(run_reference(args, world)), flush=True)
         return
 
     if world > 1:
@@ -950,14 +1000,20 @@ def main():
                 res["cpu_baseline"] = produce_cpu_baseline(p)
             print(json.dumps(res), flush=True)
     else:
-        r = run_ours(args, rank, world, local_rank)
-        if rank == 0:
-            res, w = r
-            if not args.no_cpu_baseline:
-                cb, _ = oracle_sample(w, 8.0)
-                cb.pop("seconds", None)
-                res["cpu_baseline"] = cb
-            print(json.dumps(res), flush=True)
+        import copy
+        import torch
+        names = DECODE_ORDER if args.workload == "all" else (args.workload,)
+        for name in names:
+            a = copy.copy(args)
+            a.workload = name
+            r = run_ours(a, rank, world, local_rank)
+            if rank == 0:
+                res, w = r
+                if not args.no_cpu_baseline:
+                    res["cpu_baseline"] = cpu_baselines(w, 6.0 if name == "long" else 3.0)
+                print(json.dumps(res), flush=True)
+            del r
+            torch.cuda.empty_cache()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

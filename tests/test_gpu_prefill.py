@@ -3,9 +3,11 @@
 KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"), PR
 description: the projection path dequantizes the cached Lc rows before the kv_b
 up-projection.  The tensor-core kernel uses bf16 operands (the e4m3 values are
-exact in bf16), f32 accumulation and a bf16 result: max-abs error <= 1e-2 *
-max|Y|.  Ragged token counts, slot maps, several column widths and the full
-size (4096 tokens x 32768 columns, sampled rows) are covered.
+exact in bf16, the row scale is applied in the f32 epilogue), f32 accumulation
+and a bf16 result.  Rounding Y to bf16 costs at most 2^-9 |Y| ~ 1.95e-3 |Y| and the
+f32 sums far less, so max-abs error <= 3e-3 * max|Y|.  Ragged token counts, slot
+maps, several column widths and the full size (4096 tokens x 32768 columns,
+sampled rows) are covered.
 """
 import numpy as np
 import pytest
@@ -36,7 +38,7 @@ def check(y, ref, rows=None):
     if rows is not None:
         got = got[rows]
     err = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
-    assert err <= 1e-2, err
+    assert err <= 3e-3, err
     return err
 
 
