@@ -47,6 +47,12 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   off = align_up(off + parts * 4, 256);
   p.off_o = off;
   off = align_up(off + parts * DL * 4, 256);
+  if (v == kTcPair) {
+    p.off_q8 = off;
+    off = align_up(off + (int64_t)B * H * Q8_BYTES, 256);
+    p.off_cq = off;
+    off = align_up(off + (int64_t)B * H * 4, 256);
+  }
   p.ws_bytes = off;
   return p;
 }
@@ -72,6 +78,8 @@ int bind_workspace(DecodeArgs& a, const void* workspace, int64_t workspace_bytes
   a.ws_m = reinterpret_cast<float*>(ws + a.plan.off_m);
   a.ws_l = reinterpret_cast<float*>(ws + a.plan.off_l);
   a.ws_o = reinterpret_cast<float*>(ws + a.plan.off_o);
+  a.q8 = a.plan.off_q8 ? reinterpret_cast<uint8_t*>(ws + a.plan.off_q8) : nullptr;
+  a.cq = a.plan.off_cq ? reinterpret_cast<float*>(ws + a.plan.off_cq) : nullptr;
   return KV8_OK;
 }
 

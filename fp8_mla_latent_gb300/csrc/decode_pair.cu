@@ -111,15 +111,14 @@ constexpr int B_CVT = B_PFULL + 2;           // context: the payload is read, it
 constexpr int B_RS = B_CVT + 1;              // [2] context: operand, V rows and O half ready (16 arrivals)
 constexpr int B_ODONE = B_RS + 2;            // [2] context: MMAs of an O half done
 constexpr int B_DRAIN = B_ODONE + 2;
-constexpr int NBAR = B_DRAIN + 1;
+constexpr int B_QREADY = B_DRAIN + 1;        // score: the query is in TMEM and shared memory (16 arrivals)
+constexpr int NBAR = B_QREADY + 1;
 
 // shared memory (offsets from the 1024-aligned base)
 constexpr int OFF_BAR = 0;
 constexpr int OFF_FLAGS = 512;               // tmem base, abort flag
 constexpr int OFF_FACTS = OFF_FLAGS + 16;    // [4] page facts of the tiles in the scale / V ring
-constexpr int OFF_CS = 1024;                 // score: c_h per head
-constexpr int OFF_XMAX = OFF_CS + HG * 4;    // score: [2 tiles][4 parts][128] part maxima
-constexpr int OFF_XA = OFF_XMAX;             // score, before the first tile: [4 quarters][128] query maxima
+constexpr int OFF_XMAX = 1024;               // score: [2 tiles][4 parts][128] part maxima
 constexpr int OFF_XSM = OFF_XMAX + 8 * HG * 4;  // score: [2 tiles][4 parts][4] part row-scale maxima
 constexpr int OFF_XL = OFF_XSM + 32 * 4;     // score: [4 parts][128] denominators
 constexpr int OFF_QR = 8192;                 // score: [128 heads x 128 bytes]: Rc query hi | lo
@@ -130,13 +129,14 @@ constexpr int TOTAL_S = OFF_STG + P_BYTES;
 constexpr int OFF_P = 4096;                  // context: 2 payloads / context operands
 constexpr int OFF_VRING = OFF_P + 2 * P_STRIDE;
 constexpr int TOTAL_C = OFF_VRING + NVT * VTILE;
-constexpr int SMEM = (TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C) + 1024;
+constexpr int PT_N = 256;                    // block-table entries of an item kept in shared memory
+constexpr int OFF_PT = TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C;  // both CTAs: [PT_N] int32
+constexpr int SMEM = OFF_PT + PT_N * 4 + 1024;
 // score CTA TMEM columns: S_L, S_R (one tile), then the Lc query's hi and lo terms
 // (e4m3, four channels per column) as the A operand of the score MMAs
 constexpr int T_SL = 0, T_SR = 128, T_QH = 256, T_QL = 384;
 static_assert(OFF_XL + 4 * HG * 4 <= OFF_QR, "score CTA scratch overlaps the Rc query");
-static_assert(4 * HG * 4 <= 8 * HG * 4, "query maxima fit in the part maxima");
-static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + 16 <= OFF_CS, "barriers, flags and facts overlap");
+static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + 16 <= OFF_XMAX, "barriers, flags and facts overlap");
 static_assert(P_BYTES <= P_STRIDE && (P_STRIDE % 1024) == 0 && (OFF_VRING % 1024) == 0,
               "payload layout");
 static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits in its payload buffer");
@@ -226,14 +226,39 @@ struct TileRows {
   int64_t s0, s1;  // cache slot of the tile's first / second page, or -1 (absent or unmapped)
   int nv;          // tokens of the tile inside the item
 };
+// Cache slot of token t of the item starting at token t0: its block-table entry
+// from the item's copy in shared memory (the first PT_N pages), else from global
+// memory; -1 (and the error bit) for an entry out of range.
+__device__ __forceinline__ int64_t item_slot(const DecodeArgs& a, int b, int64_t t, int64_t t0,
+                                             const int32_t* pt) {
+  if (a.block_table == nullptr) return t;
+  const int64_t k = (t >> 6) - (t0 >> 6);
+  const int32_t blk = k < PT_N ? pt[k] : __ldg(&a.block_table[(int64_t)b * a.max_blocks + (t >> 6)]);
+  if (blk < 0 || (int64_t)blk >= a.n_blocks) {
+    atomicOr(a.err, ERR_BLOCK_TABLE);
+    return -1;
+  }
+  return (int64_t)blk * PAGE + (t & (PAGE - 1));
+}
+// The item's first PT_N block-table entries into shared memory, by all lanes of
+// the calling warp (one round trip instead of a dependent lookup per page).
+__device__ __forceinline__ void load_page_table(const DecodeArgs& a, int b, int64_t t0,
+                                                int64_t t_end, int32_t* pt, int lane) {
+  if (a.block_table != nullptr) {
+    const int64_t p0 = t0 >> 6, np = ((t_end + PAGE - 1) >> 6) - p0;
+    for (int k = lane; k < PT_N && k < np; k += 32)
+      pt[k] = __ldg(&a.block_table[(int64_t)b * a.max_blocks + p0 + k]);
+  }
+  __syncwarp();
+}
 __device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int64_t t0, int64_t t_end,
-                                              int i) {
+                                              int i, const int32_t* pt) {
   TileRows r;
   const int64_t tb = t0 + (int64_t)i * TILE;
   const int64_t n = t_end - tb;
   r.nv = n < TILE ? (int)n : TILE;
-  r.s0 = slot_of(a, b, tb);
-  r.s1 = r.nv > PAGE ? slot_of(a, b, tb + PAGE) : -1;
+  r.s0 = item_slot(a, b, tb, t0, pt);
+  r.s1 = r.nv > PAGE ? item_slot(a, b, tb + PAGE, t0, pt) : -1;
   return r;
 }
 // The facts packed in a word the loading thread leaves in shared memory for the
@@ -308,6 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(&bars[B_CVT], N_LANE_WARPS);
     mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[B_QREADY], N_LANE_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the context CTA expects the payloads of its first two tiles (one per
@@ -321,90 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  float* cs = reinterpret_cast<float*>(sm + OFF_CS);
   __syncthreads();  // the TMEM base address is in shared memory
-  if (rank == 0 && warp >= W_LANE) {
-    // Query -> two e4m3 terms with a per-head power-of-two scale that puts max|q|
-    // in [128, 256); c_h undoes it and folds in sm_scale * log2(e).  Thread
-    // (head hh, quarter hf) converts Lc channels [128 hf, 128 hf + 128) into TMEM
-    // lane hh (four channels per column, channel 4j in the low byte of column j),
-    // and quarter 0 also the 64 Rc channels into row hh of the Rc operand in
-    // shared memory (hi in bytes 0..63, lo in 64..127).  The rows reach the
-    // threads through a per-warp transpose buffer (4 KB of the K ring, unused
-    // until the loads start): 32 channels of the warp's 32 heads per round, read
-    // from global memory 128 contiguous bytes per eight lanes.
-    const uint32_t tm = *tmem_slot;
-    const int q = warp & 3, hf = (warp - W_LANE) >> 2, hh = q * 32 + lane, h = h0 + hh;
-    const bool real = h < a.H;
-    float4* stage = reinterpret_cast<float4*>(sm + OFF_KRING + (warp - W_LANE) * 4096);
-    const int64_t row0 = (int64_t)b * a.H + h0 + q * 32;  // the warp's first head row
-    // stage channels [c0, c0 + 32) of the warp's heads from rows of `width` floats,
-    // then return this thread's eight float4 of them
-    auto round = [&](const float* base, int width, int c0, float4 (&x)[8]) {
-      __syncwarp();  // the previous round's reads are done
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + (lane >> 3), u = lane & 7;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (h0 + q * 32 + r < a.H)
-          v = __ldg(reinterpret_cast<const float4*>(base + (row0 + r) * width + c0) + u);
-        stage[r * 8 + (u ^ (r & 7))] = v;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = stage[lane * 8 + (u ^ (lane & 7))];
-    };
-    float* xa = reinterpret_cast<float*>(sm + OFF_XA);
-    float amax = 0.f;
-    float4 x[8];
-#pragma unroll 1
-    for (int k = 0; k < 4 + (hf == 0 ? 2 : 0); ++k) {
-      if (k < 4) round(a.q_lat, DL, 128 * hf + 32 * k, x);
-      else round(a.q_rope, DR, 32 * (k - 4), x);
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
-    }
-    xa[hf * HG + hh] = amax;
-    named_bar_sync(1, N_LANE_WARPS * 32);
-    amax = fmaxf(fmaxf(xa[hh], xa[HG + hh]), fmaxf(xa[2 * HG + hh], xa[3 * HG + hh]));
-    int e = 0;
-    if (amax > 0.f && isfinite(amax)) {
-      int ex;
-      frexpf(amax, &ex);
-      e = min(max(8 - ex, -120), 120);
-    }
-    const float sc = ldexpf(1.0f, e);
-    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    const uint32_t qr = smem_u32(sm + OFF_QR);
-#pragma unroll 1
-    for (int k = 0; k < 4 + (hf == 0 ? 2 : 0); ++k) {
-      if (k < 4) round(a.q_lat, DL, 128 * hf + 32 * k, x);
-      else round(a.q_rope, DR, 32 * (k - 4), x);
-      uint32_t hw[8], lw[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float v[4] = {x[u].x * sc, x[u].y * sc, x[u].z * sc, x[u].w * sc};
-        split4(v, hw[u], lw[u]);
-      }
-      if (k < 4) {
-        __syncwarp();
-        tmem_st8(tm + lane_addr + T_QH + hf * 32 + k * 8, hw);
-        tmem_st8(tm + lane_addr + T_QL + hf * 32 + k * 8, lw);
-      } else {
-        // Rc channels [32 (k - 4), +32): hi units 2 (k - 4) + {0, 1}, lo units 4 + those
-        const int u0 = 2 * (k - 4);
-        sts128(qr + sw128(hh, u0), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-        sts128(qr + sw128(hh, u0 + 1), make_uint4(hw[4], hw[5], hw[6], hw[7]));
-        sts128(qr + sw128(hh, 4 + u0), make_uint4(lw[0], lw[1], lw[2], lw[3]));
-        sts128(qr + sw128(hh, 4 + u0 + 1), make_uint4(lw[4], lw[5], lw[6], lw[7]));
-      }
-    }
-    if (hf == 0) cs[hh] = real ? a.sm_scale * LOG2E / sc : 0.f;
-    __syncwarp();
-    tmem_wait_st();
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrive or copy
   tc_fence_after();
@@ -416,6 +359,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t qr = smem_u32(sm + OFF_QR);
     const uint32_t scr = smem_u32(sm + OFF_SCR);
     if (warp == W_TMA) {
+      int32_t* pt = reinterpret_cast<int32_t*>(sm + OFF_PT);
+      load_page_table(a, b, t0, t_end, pt, lane);
       if (lane == 0) {
         bool ok = true;
         auto prefetch_tile = [&](int i) {
@@ -424,15 +369,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int64_t tk = tb + pg * PAGE;
             if (tk >= t_end) break;
             const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
-            const int64_t slot = slot_of(a, b, tk);
+            const int64_t slot = item_slot(a, b, tk, t0, pt);
             if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
           }
         };
         int nk = 0, nsc = 0;  // tiles whose K blocks / row scales were requested
-        for (int i = 0; i < L2_AHEAD && i < n_tiles; ++i) prefetch_tile(i);
         for (int i = 0; ok && i < n_tiles; ++i) {
-          if (i + L2_AHEAD < n_tiles) prefetch_tile(i + L2_AHEAD);
-          const TileRows tr = tile_rows(a, b, t0, t_end, i);
+          const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
           const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
           const int sc = i % NSC;
           // the tile's five blocks complete on one barrier; a slot is free once the
@@ -463,6 +406,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (tr.s0 >= 0) tma_load_2d(dst, &kmap, 128 * blk, (int)tr.s0, kt);
             if (tr.s1 >= 0) tma_load_2d(dst + 8192, &kmap, 128 * blk, (int)tr.s1, kt);
           }
+          // then the L2 prefetch of the tiles ahead (the next tile is loaded at once;
+          // after the first, the one L2_AHEAD tiles on)
+          for (int j = (i == 0 ? 2 : i + L2_AHEAD); ok && j <= i + L2_AHEAD && j < n_tiles; ++j)
+            prefetch_tile(j);
         }
         if (!ok) {
           // after an abort, let the loads already requested land before the CTA can
@@ -482,9 +429,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t idS = idesc_f16(128, 128, false, false);  // e4m3 x e4m3 (format 0)
         const uint64_t kdesc = smem_desc(kring, 16, 1024, SW128);
         const uint64_t qdesc = smem_desc(qr, 16, 1024, SW128);
-        // tile 0's K blocks; a later tile's are waited for by a softmax warp before
-        // it releases S, so one barrier per tile gates these MMAs
-        bool ok = mbar_wait(&bars[B_KT], 0, abort_flag, WAIT_NS);
+        // the query, and tile 0's K blocks; a later tile's are waited for by the
+        // softmax warps before they release S, so one barrier per tile gates these MMAs
+        bool ok = mbar_wait(&bars[B_QREADY], 0, abort_flag, WAIT_NS) &&
+                  mbar_wait(&bars[B_KT], 0, abort_flag, WAIT_NS);
         for (int i = 0; ok && i < n_tiles; ++i) {
           if (!mbar_wait(&bars[B_SEMPTY], (i & 1) ^ 1, abort_flag, WAIT_NS)) {
             ok = false;
@@ -532,7 +480,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       float* xl = reinterpret_cast<float*>(sm + OFF_XL);      // [4][128]
       uint8_t* stg_p = sm + OFF_STG + chunk * CHUNK;
       const uint32_t stg = smem_u32(stg_p);
-      const float c = cs[hh];
+      // The prepared query (two e4m3 terms on the head's power-of-two scale, c_h
+      // folding the scale back in with sm_scale * log2(e)): thread (head hh, part)
+      // puts Lc channels [128 part, 128 part + 128) of both terms into TMEM lane hh
+      // (four channels per column), part 0 also the Rc terms into row hh of the Rc
+      // operand in shared memory (hi in bytes 0..63, lo in 64..127).  Heads past H
+      // are zeros.  The loads overlap the first tiles' K loads.
+      const bool real = h0 + hh < a.H;
+      const float c = real ? __ldg(a.cq + (int64_t)b * a.H + h0 + hh) : 0.f;
+      {
+        const uint4* q8 = reinterpret_cast<const uint4*>(a.q8 + ((int64_t)b * a.H + h0 + hh) * Q8_BYTES);
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl) {  // 64 channels (16 columns) of each term at a time
+          uint32_t hw[16], lw[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int u = 8 * part + 4 * hl + k;
+            const uint4 vh = real ? __ldg(q8 + u) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 vl = real ? __ldg(q8 + 32 + u) : make_uint4(0u, 0u, 0u, 0u);
+            hw[4 * k] = vh.x; hw[4 * k + 1] = vh.y; hw[4 * k + 2] = vh.z; hw[4 * k + 3] = vh.w;
+            lw[4 * k] = vl.x; lw[4 * k + 1] = vl.y; lw[4 * k + 2] = vl.z; lw[4 * k + 3] = vl.w;
+          }
+          __syncwarp();
+          tmem_st16(tmem + lane_addr + T_QH + part * 32 + 16 * hl, hw);
+          tmem_st16(tmem + lane_addr + T_QL + part * 32 + 16 * hl, lw);
+        }
+        if (part == 0) {
+          const uint32_t qr = smem_u32(sm + OFF_QR);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            sts128(qr + sw128(hh, u), real ? __ldg(q8 + 64 + u) : make_uint4(0u, 0u, 0u, 0u));
+        }
+        __syncwarp();
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_QREADY]);
+      }
       const bool live = c > 0.f;               // a real head (padding heads have c = 0)
       const uint32_t prem = map_to(smem_u32(sm + OFF_P), 1) + chunk * CHUNK;  // partner's buffers
       const uint32_t pfull_rem = map_to(smem_u32(&bars[B_PFULL]), 1);
@@ -714,11 +699,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t pbuf = smem_u32(sm + OFF_P);
     const uint32_t vring = smem_u32(sm + OFF_VRING);
     if (warp == W_TMA) {
+      int32_t* pt = reinterpret_cast<int32_t*>(sm + OFF_PT);
+      load_page_table(a, b, t0, t_end, pt, lane);
       if (lane == 0) {
         bool ok = true;
         int nv = 0;  // tiles requested
         for (int i = 0; ok && i < n_tiles; ++i) {
-          const TileRows tr = tile_rows(a, b, t0, t_end, i);
+          const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
           const int vs = i % NVT;
           if (!mbar_wait(&bars[B_VEMPTY + vs], ((i / NVT) & 1) ^ 1, abort_flag, WAIT_NS)) {
             ok = false;
@@ -939,6 +926,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   if (warp == W_MMA) tmem_dealloc(tmem, 512);
 }
 
+// The queries in the score operand's form, one warp per (sequence, head): a
+// power-of-two scale 2^e puts max|q| over the 576 channels in [128, 256), each
+// scaled value becomes two e4m3 terms, hi = e4m3(x) and lo = e4m3(x - hi), and
+// c_h = sm_scale * log2(e) / 2^e undoes the scale in the softmax.  Bytes of a head:
+// Lc hi (channel order), Lc lo, Rc hi, Rc lo.
+__global__ void __launch_bounds__(256) prep_query_kernel(const DecodeArgs a) {
+  const int64_t head = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // b * H + h
+  if (head >= (int64_t)a.B * a.H) return;
+  const int lane = threadIdx.x & 31;
+  const float4* ql = reinterpret_cast<const float4*>(a.q_lat + head * DL);
+  const float4* qr = reinterpret_cast<const float4*>(a.q_rope + head * DR);
+  float4 x[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) x[k] = __ldg(ql + 32 * k + lane);  // channels 4 (32 k + lane) + 0..3
+  const float4 y = lane < 16 ? __ldg(qr + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float amax = fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w)));
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[k].x), fabsf(x[k].y)), fmaxf(fabsf(x[k].z), fabsf(x[k].w))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int e = 0;
+  if (amax > 0.f && isfinite(amax)) {
+    int ex;
+    frexpf(amax, &ex);
+    e = min(max(8 - ex, -120), 120);
+  }
+  const float sc = ldexpf(1.0f, e);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.q8 + head * Q8_BYTES);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float v[4] = {x[k].x * sc, x[k].y * sc, x[k].z * sc, x[k].w * sc};
+    uint32_t hi, lo;
+    split4(v, hi, lo);
+    dst[32 * k + lane] = hi;
+    dst[DL / 4 + 32 * k + lane] = lo;
+  }
+  if (lane < 16) {
+    const float v[4] = {y.x * sc, y.y * sc, y.z * sc, y.w * sc};
+    uint32_t hi, lo;
+    split4(v, hi, lo);
+    dst[2 * DL / 4 + lane] = hi;
+    dst[2 * DL / 4 + DR / 4 + lane] = lo;
+  }
+  if (lane == 0) a.cq[head] = a.sm_scale * LOG2E / sc;
+}
+
 // 1-D tensor map of the row scales (f32, two per slot): boxes of 128 floats (one
 // page); floats past the end read as zeros.
 cudaError_t make_scale_map(const DecodeArgs& a, CUtensorMap* map) {
@@ -991,6 +1025,9 @@ cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = make_scale_map(d, &smap);
   if (e != cudaSuccess) return e;
+  if (d.q8 == nullptr || d.cq == nullptr) return cudaErrorInvalidValue;  // not a pair plan
+  const int64_t heads = (int64_t)d.B * d.H;
+  if (heads > 0) prep_query_kernel<<<(unsigned)((heads + 7) / 8), 256, 0, s>>>(d);
   decode_pair_kernel<<<2 * d.plan.max_items, NTHREADS, SMEM, s>>>(d, kmap, smap);
   return cudaGetLastError();
 }

@@ -34,7 +34,14 @@ struct SplitPlan {
   // byte offsets inside the workspace; the header (error word, then the item
   // table) is cleared by every split launch
   int64_t hdr_bytes, off_seg, off_m, off_l, off_o;
+  // SM-pair kernel only (0 otherwise): the queries in the score operand's form,
+  // written by the query-prep launch: [B][H][Q8_BYTES] e4m3 terms, [B][H] f32 c_h
+  int64_t off_q8, off_cq;
 };
+
+// Bytes per (sequence, head) of the prepared query: the Lc channels' hi term (512),
+// their lo term (512), then the Rc channels' hi (64) and lo (64) terms.
+constexpr int Q8_BYTES = 2 * DL + 2 * DR;
 
 // Deterministic in its arguments (no device query), so the workspace-size call
 // and the decode call always agree.
@@ -58,6 +65,8 @@ struct DecodeArgs {
   float* ws_m;                 // [max_items][hg]   running max, log2 units
   float* ws_l;                 // [max_items][hg]   sum of exp2(z - m)
   float* ws_o;                 // [max_items][hg][512] unnormalised context
+  uint8_t* q8;                 // [B][H][Q8_BYTES] prepared queries (SM-pair kernel), or nullptr
+  float* cq;                   // [B][H] their scale factors c_h (SM-pair kernel), or nullptr
   SplitPlan plan;
 };
 
