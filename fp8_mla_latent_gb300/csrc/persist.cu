@@ -25,18 +25,19 @@
 
 #include <string>
 
+#include "cachefile.h"
 #include "fp8mla.h"
 #include "kv8_internal.h"
 
 namespace kv8 {
 namespace {
 
-constexpr int HDR = 64;
-constexpr int REC2 = D + 8;      // version-2 record: codes, then sLc and sRc
-constexpr int REC1 = D * 4;      // version-1 record: 576 f32
+using cachefile::HDR;
+using cachefile::read_at;
+using cachefile::REC1;
+using cachefile::REC2;
+using cachefile::write_at;
 constexpr int STAGE_ROW = REC1 + D + 8;  // f32 rows (or records) + codes + scales per staged row
-const char MAGIC2[8] = {'C', 'O', 'L', 'I', 'K', 'V', '2', 0};
-const char MAGIC1[8] = {'C', 'O', 'L', 'I', 'K', 'V', '1', 0};
 
 // One warp per record; a record is 73 eight-byte words (72 of codes, 1 of scales).
 __global__ void gather_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
@@ -80,38 +81,6 @@ __global__ void check_slots_kernel(const int64_t* __restrict__ slots, int64_t n,
   if (i < n && (slots[i] < 0 || slots[i] >= n_slots)) *reinterpret_cast<volatile int*>(flag) = 1;
 }
 
-void put_u32(uint8_t* p, uint32_t v) { memcpy(p, &v, 4); }
-void put_u64(uint8_t* p, uint64_t v) { memcpy(p, &v, 8); }
-uint32_t get_u32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
-uint64_t get_u64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
-
-void make_header(uint8_t* h, int version, int64_t n_rows) {
-  memset(h, 0, HDR);
-  memcpy(h, version == 2 ? MAGIC2 : MAGIC1, 8);
-  put_u32(h + 8, HDR);
-  put_u32(h + 12, version == 2 ? 2u : 1u);
-  put_u32(h + 16, D);
-  put_u32(h + 20, version == 2 ? REC2 : REC1);
-  put_u64(h + 24, (uint64_t)n_rows);
-}
-
-// Version of a header from its fields after the magic (0 if they fit neither).
-int version_of_fields(const uint8_t* h) {
-  if (get_u32(h + 8) != HDR || get_u32(h + 16) != D) return 0;
-  if (get_u32(h + 12) == 2 && get_u32(h + 20) == REC2) return 2;
-  if (get_u32(h + 12) == 1 && get_u32(h + 20) == REC1) return 1;
-  return 0;
-}
-
-bool write_at(FILE* f, int64_t off, const void* p, size_t n) {
-  if (fseeko(f, (off_t)off, SEEK_SET) != 0) return false;
-  return n == 0 || fwrite(p, 1, n, f) == n;
-}
-bool read_at(FILE* f, int64_t off, void* p, size_t n) {
-  if (fseeko(f, (off_t)off, SEEK_SET) != 0) return false;
-  return n == 0 || fread(p, 1, n, f) == n;
-}
-
 }  // namespace
 }  // namespace kv8
 
@@ -141,57 +110,40 @@ float* area_scales(kv8_disk* d, bool dev) {
 }
 
 int commit_rows(kv8_disk* d, int64_t n_rows) {
-  uint8_t h[HDR];
-  make_header(h, d->version, n_rows);
-  if (!write_at(d->f, 0, h, HDR) || fflush(d->f) != 0) return KV8_EIO;
-  d->n_rows = n_rows;
-  return KV8_OK;
+  const int st = cachefile::commit(d->f, d->version, n_rows);
+  if (st == KV8_OK) d->n_rows = n_rows;
+  return st;
 }
 
-// Version 1 -> 2: quantize the f32 rows chunk by chunk with the library's
-// quantizer into a new file beside the old one, then replace it.
-int convert_to_v2(kv8_disk* d, cudaStream_t s) {
-  const std::string tmp = d->path + ".v2tmp";
-  FILE* g = fopen(tmp.c_str(), "w+b");
-  if (g == nullptr) return KV8_EIO;
-  uint8_t h[HDR];
-  make_header(h, 2, 0);
-  int st = fwrite(h, 1, HDR, g) == HDR ? KV8_OK : KV8_EIO;
-  for (int64_t r0 = 0; st == KV8_OK && r0 < d->n_rows; r0 += d->staging_rows) {
-    const int64_t m = (d->n_rows - r0) < d->staging_rows ? (d->n_rows - r0) : d->staging_rows;
-    if (!read_at(d->f, HDR + r0 * REC1, area_rows(d, false), (size_t)(m * REC1))) { st = KV8_EIO; break; }
-    if (launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
-                        area_codes(d, true), area_scales(d, true), m, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
-      st = KV8_ECUDA;
-      break;
-    }
-    // interleave codes and scales into records over the (now free) f32 area
-    uint8_t* rec = area_rows(d, false);
-    const uint8_t* c = area_codes(d, false);
-    const float* sc = area_scales(d, false);
-    for (int64_t i = 0; i < m; ++i) {
-      memcpy(rec + i * REC2, c + i * D, D);
-      memcpy(rec + i * REC2 + D, sc + i * 2, 8);
-    }
-    if (fwrite(rec, 1, (size_t)(m * REC2), g) != (size_t)(m * REC2)) st = KV8_EIO;
+// Version 1 -> 2: the file's rewrite (cachefile.h) with the library's quantizer:
+// the staged f32 rows through the device view of the staging buffer, then codes
+// and scales interleaved into records over the (now free) f32 area.
+struct ConvertCtx {
+  kv8_disk* d;
+  cudaStream_t s;
+};
+int quantize_records(void* ctx, int64_t m, uint8_t* buf) {
+  kv8_disk* d = static_cast<ConvertCtx*>(ctx)->d;
+  cudaStream_t s = static_cast<ConvertCtx*>(ctx)->s;
+  if (buf != area_rows(d, false)) return KV8_EINVAL;
+  if (launch_quantize(reinterpret_cast<const float*>(area_rows(d, true)), m, D, nullptr,
+                      area_codes(d, true), area_scales(d, true), m, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return KV8_ECUDA;
+  const uint8_t* c = area_codes(d, false);
+  const float* sc = area_scales(d, false);
+  for (int64_t i = 0; i < m; ++i) {
+    memcpy(buf + i * REC2, c + i * D, D);
+    memcpy(buf + i * REC2 + D, sc + i * 2, 8);
   }
-  if (st == KV8_OK) {
-    make_header(h, 2, d->n_rows);
-    if (!write_at(g, 0, h, HDR) || fflush(g) != 0 || fsync(fileno(g)) != 0) st = KV8_EIO;
-  }
-  if (fclose(g) != 0 && st == KV8_OK) st = KV8_EIO;
-  if (st != KV8_OK) {
-    remove(tmp.c_str());
-    return st;
-  }
-  fclose(d->f);
-  d->f = nullptr;
-  if (rename(tmp.c_str(), d->path.c_str()) != 0) return KV8_EIO;
-  d->f = fopen(d->path.c_str(), "r+b");
-  if (d->f == nullptr) return KV8_EIO;
-  d->version = 2;
   return KV8_OK;
+}
+int convert_to_v2(kv8_disk* d, cudaStream_t s) {
+  ConvertCtx ctx{d, s};
+  const int st = cachefile::rewrite_v1_to_v2(d->path, &d->f, d->n_rows, d->staging_rows,
+                                             area_rows(d, false), quantize_records, &ctx);
+  if (st == KV8_OK) d->version = 2;
+  return st;
 }
 
 }  // namespace
@@ -226,33 +178,7 @@ int kv8_disk_open(const char* path, int64_t staging_rows, kv8_disk** out) {
   d->f = fopen(path, "r+b");
   if (d->f == nullptr && errno == ENOENT) d->f = fopen(path, "w+b");
   if (d->f == nullptr) st = KV8_EIO;
-  uint8_t h[HDR];
-  size_t got = 0;
-  if (st == KV8_OK) {
-    if (fseeko(d->f, 0, SEEK_SET) != 0) st = KV8_EIO;
-    else got = fread(h, 1, HDR, d->f);
-  }
-  if (st == KV8_OK && got < (size_t)HDR) {
-    // empty or torn at creation: a fresh version-2 file
-    if (ftruncate(fileno(d->f), 0) != 0) st = KV8_EIO;
-    else {
-      d->version = 2;
-      st = commit_rows(d, 0);
-    }
-  } else if (st == KV8_OK) {
-    const int v = version_of_fields(h);
-    if (v == 0) {
-      st = KV8_EFORMAT;
-    } else {
-      d->version = v;
-      d->n_rows = (int64_t)get_u64(h + 24);
-      if (memcmp(h, v == 2 ? MAGIC2 : MAGIC1, 8) != 0) st = commit_rows(d, d->n_rows);  // repair the magic
-      struct stat sb;
-      if (st == KV8_OK && (fstat(fileno(d->f), &sb) != 0 || d->n_rows < 0 ||
-                           (int64_t)sb.st_size < HDR + d->n_rows * (v == 2 ? REC2 : REC1)))
-        st = KV8_EFORMAT;  // fewer bytes than the committed rows
-    }
-  }
+  if (st == KV8_OK) st = cachefile::open_header(d->f, &d->version, &d->n_rows);
   if (st != KV8_OK) {
     kv8_disk_close(d);
     return st;
