@@ -273,10 +273,11 @@ def mla_absorb_decode_fp8(q_lat, q_rope, kv_codes, kv_scales, T, sm_scale, out=N
     return out
 
 
-def mla_absorb_decode_fp8_batch(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
-                                sm_scale, out=None, lse=None, workspace=None,
-                                variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK, stream=None):
-    """B queries (q_lat [B,H,512], q_rope [B,H,64]) over a paged cache -> out [B,H,512]."""
+def _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, out=None, lse=None,
+                  outputs=True):
+    """The checks every batched decode wrapper runs: dtypes, shapes and one row per
+    sequence (and of out / lse when the call writes them); returns (B, H, out), out
+    allocated if None."""
     _need(q_lat, "q_lat", torch.float32, 3)
     _need(q_rope, "q_rope", torch.float32, 3)
     _need(kv_codes, "kv_codes", torch.uint8, 2)
@@ -286,13 +287,29 @@ def mla_absorb_decode_fp8_batch(q_lat, q_rope, kv_codes, kv_scales, block_table,
     B, H = q_lat.shape[:2]
     if q_lat.shape[2] != KV8_DL or tuple(q_rope.shape) != (B, H, KV8_DR):
         raise ValueError("q_lat must be [B,H,512] and q_rope [B,H,64]")
+    if kv_codes.shape[1] != KV8_D or tuple(kv_scales.shape) != (kv_codes.shape[0], 2):
+        raise ValueError("kv_codes must be [slots,576] and kv_scales [slots,2]")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table and seq_lens need one row per sequence")
+    if not outputs:
+        return B, H, None
     if out is None:
         out = torch.empty((B, H, KV8_DL), dtype=torch.float32, device=q_lat.device)
     _need(out, "out", torch.float32, 3)
+    if tuple(out.shape) != (B, H, KV8_DL):
+        raise ValueError("out must be [B,H,512]")
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
+        if tuple(lse.shape) != (B, H):
+            raise ValueError("lse must be [B,H]")
+    return B, H, out
+
+
+def mla_absorb_decode_fp8_batch(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
+                                sm_scale, out=None, lse=None, workspace=None,
+                                variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK, stream=None):
+    """B queries (q_lat [B,H,512], q_rope [B,H,64]) over a paged cache -> out [B,H,512]."""
+    B, H, out = _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, out, lse)
     max_blocks = block_table.shape[1]
     n_blocks = kv_codes.shape[0] // block_size
     need = mla_absorb_decode_fp8_batch_workspace_size(B, H, max_blocks, block_size, variant)
@@ -312,7 +329,8 @@ def mla_absorb_decode_fp8_batch_partials(q_lat, q_rope, kv_codes, kv_scales, blo
                                          variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK,
                                          stream=None):
     """Split phase 1: the split-T kernel only; partials stay in ``workspace``."""
-    B, H = q_lat.shape[:2]
+    B, H, _ = _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
+                            outputs=False)
     st = lib().mla_absorb_decode_fp8_batch_partials(
         _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
         _ptr(seq_lens), B, H, block_table.shape[1], int(block_size),
@@ -341,11 +359,7 @@ def mla_absorb_decode_fp8_batch_noalloc(q_lat, q_rope, kv_codes, kv_scales, bloc
                                         block_size=KV8_BLOCK, stream=None):
     """The batched decode without a caller workspace (for callers that cannot
     allocate device memory): partials go to the library's static device scratch."""
-    _need(q_lat, "q_lat", torch.float32, 3)
-    _need(q_rope, "q_rope", torch.float32, 3)
-    B, H = q_lat.shape[:2]
-    if out is None:
-        out = torch.empty((B, H, KV8_DL), dtype=torch.float32, device=q_lat.device)
+    B, H, out = _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, out, lse)
     st = lib().mla_absorb_decode_fp8_batch_noalloc(
         _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
         _ptr(seq_lens), B, H, block_table.shape[1], int(block_size),

@@ -1,8 +1,8 @@
 // decode_simt.cu -- CUDA-core split-T absorbed MLA decode over the e4m3 cache.
 //
 // KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"),
-// PR description: the latent is both key and value; the score and context loops
-// dequantize inline with the per-row scale hoisted out of each dot; closing
+// PR description: the latent is key and value at once; the score and context
+// loops decode as they go, each row scale applied outside its dot product; closing
 // note: split-T kernels for long caches.
 //
 // One CTA per work item (sequence, head group of HG_SIMT heads, token range);
@@ -98,7 +98,7 @@ decode_simt_kernel(DecodeArgs a) {
       for (int k = 0; k < 16; ++k) dl = fmaf(qL[j][k], v[k], dl);
       dr = fmaf(qR[j][0], vr[0], dr);
       dr = fmaf(qR[j][1], vr[1], dr);
-      float z = sc.x * dl + sc.y * dr;  // scales hoisted out of the dots
+      float z = sc.x * dl + sc.y * dr;  // the row scales, outside the dot products
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       const float mn = fmaxf(m[j], z);

@@ -4,7 +4,7 @@
 // Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with
 // .coli_kv v2"), PR description: the latent Lc is both key and value of the
 // absorbed attention, the RoPE part Rc is key only, and each row's f32 scale is
-// hoisted out of its dot product; closing note: split-T kernels for long caches.
+// applied outside its dot product; closing note: split-T kernels for long caches.
 // Per (sequence b, head h):
 //   z_t = sm * ( sLc_t <q_lat, dec(Lc_t)> + sRc_t <q_rope, dec(Rc_t)> )
 //   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)

@@ -6,8 +6,8 @@
 // amax/448 scale for Lc and one for Rc.
 //
 // produce_rows_kernel is the fused producer in front of it (PR description,
-// attention_rows item: the producer quantizes the fresh normed/roped row): RMS
-// norm of Lc with a weight, rotation of the Rc pairs (2j, 2j+1) by the angle of
+// attention_rows item: the producer quantizes the new row once normalised and
+// rotated): RMS norm of Lc with a weight, rotation of the Rc pairs (2j, 2j+1) by the angle of
 // the row's position (cosine and sine tabulated by the caller), then the same
 // quantization.  Its f32 operations are rounded once each, in a fixed order (the
 // sum of squares: lane partial sums in index order, then an xor butterfly), so

@@ -2,7 +2,7 @@
 // the latent context to the value head, y[b][h][v] = sum_d o[b][h][d] W_UV[h][d][v].
 //
 // KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv v2"), PR
-// description: "the latent is both key and value in the absorbed attention", so
+// description: in the absorbed attention the latent is key and value at once, so
 // the attention's context is a latent vector per head and the value projection
 // follows it.
 //

@@ -77,9 +77,10 @@ typedef enum {
 } kv8_decode_variant;
 
 /* ---------------------------------------------------------------------------
- * kv8_quantize_rows -- KV8 page, PR description, c/kv_fp8.h item ("per-row
- * quantizer with a subnormal-amax guard") and attention_rows item (the producer
- * quantizes the fresh normed/roped row instead of copying f32).
+ * kv8_quantize_rows -- KV8 page, PR description, c/kv_fp8.h item (a per-row
+ * quantizer that guards rows with a subnormal amax) and attention_rows item (the
+ * producer quantizes the new row, once normalised and rotated, instead of keeping
+ * an f32 copy).
  *
  * For each source row r, and for each segment (Lc = floats 0..511, Rc = floats
  * 512..575) separately:
@@ -110,9 +111,9 @@ int kv8_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 
 /* ---------------------------------------------------------------------------
  * kv8_produce_rows -- KV8 page, PR description, attention_rows item: the
- * producer quantizes "the fresh normed/roped row" instead of an f32 copy.  The
- * fused form of that producer: from the raw latent rows to cache codes in one
- * pass.  The page names the steps; the formulas are our reading.  For each row r
+ * producer quantizes the new row after normalisation and rotation instead of
+ * keeping an f32 copy.  The fused form of that producer: from the raw latent rows
+ * to cache codes in one pass.  The page names the steps; the formulas are our reading.  For each row r
  * with position pos = positions[r]:
  *   Lc (floats 0..511):   ss  = sum of x_i^2 in a fixed order (32 partial sums
  *                         of x[16l..16l+15] in index order, then for o = 16, 8,
@@ -146,7 +147,7 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 
 /* ---------------------------------------------------------------------------
  * mla_wuv_epilogue -- the step after the absorbed attention (KV8 page, PR
- * description: "the latent is both key and value in the absorbed attention", so
+ * description: in the absorbed attention the latent is key and value at once, so
  * the attention's output is a latent context per head): the per-head value
  * projection
  *   y[b][h][v] = sum_{d<512} o[b][h][d] * W_UV[h][d][v]      (f32 accumulation)
@@ -209,10 +210,10 @@ int kv8_selftest_wait_timeout(void* workspace, int64_t workspace_bytes, int64_t 
                               void* stream);
 
 /* ---------------------------------------------------------------------------
- * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph ("the
- * latent is both key and value in the absorbed attention"), attention_rows item
- * (score and context loops dequantize inline "with the scale hoisted out of the
- * dot"), CUDA item (absorbed decode kernel over fp8 rows); the closing note's
+ * mla_absorb_decode_fp8 -- KV8 page, PR description, opening paragraph (the latent
+ * is key and value at once in the absorbed attention), attention_rows item (the
+ * score and context loops decode as they go, the row scale applied outside each
+ * dot product), CUDA item (absorbed decode kernel over fp8 rows); the closing note's
  * split-T kernels for long caches.
  *
  * One decode query (H heads) against one contiguous cache of T rows (slots

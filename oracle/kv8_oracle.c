@@ -18,8 +18,8 @@
 #endif
 
 /* ------------------------------------------------------------------------ */
-/* e4m3 decode.  KV8 page, PR description, c/kv_fp8.h item: "256-entry decode
- * LUT".  The table is filled from the closed form of the OCP e4m3fn format:
+/* e4m3 decode.  KV8 page, PR description, c/kv_fp8.h item: a decode table of
+ * all 256 codes.  The table is filled from the closed form of the OCP e4m3fn format:
  *   sign s = bit 7, exponent e = bits 6..3 (bias 7), mantissa m = bits 2..0;
  *   e = 15, m = 7        -> NaN (codes 0x7F and 0xFF; there is no infinity);
  *   e = 0                -> (-1)^s * m * 2^-9           (subnormals, and +-0);
@@ -53,9 +53,9 @@ void orc_e4m3_decode_table(float out[256]) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* e4m3 encode.  KV8 page, PR description, c/kv_fp8.h item: "RNE bit-math
- * encoder (saturating at +/-448, signed zero preserved, NaN stored as inert 0)".
- * Works on the f32 bit pattern with integer arithmetic only.                   */
+/* e4m3 encode.  KV8 page, PR description, c/kv_fp8.h item: an encoder on the bit
+ * pattern with round-to-nearest-even that saturates at +/-448, keeps the sign of
+ * zero and stores NaN as the code 0.  Works on the f32 bit pattern with integer arithmetic only.                   */
 uint8_t orc_e4m3_encode(float q) {
     uint32_t u;
     memcpy(&u, &q, sizeof u);
@@ -174,10 +174,9 @@ int64_t orc_e4m3_list_mismatches_nearest(const uint32_t* bits, int64_t n, uint32
 }
 
 /* ------------------------------------------------------------------------ */
-/* Per-row quantizer.  KV8 page, PR description: "per-row f32 amax/448 scale";
- * expanded summary: Lc and Rc get "one f32 amax/448 scale each"; c/kv_fp8.h
- * item: "per-row quantizer with a subnormal-amax guard (448/amax would overflow
- * to +inf)".  Steps, for each segment (Lc: 512 values, Rc: 64 values):
+/* Per-row quantizer.  KV8 page, PR description and expanded summary: each of Lc
+ * and Rc gets its own f32 scale amax/448; c/kv_fp8.h item: a guard for rows whose
+ * amax is so small (subnormal) that 448/amax overflows to +inf.  Steps, for each segment (Lc: 512 values, Rc: 64 values):
  *   1. amax = max |x_i| over the non-NaN entries (0 if there are none);
  *   2. s = amax / 448 (f32, rounded once) is the stored scale;
  *   3. inv = 448 / amax (f32, rounded once);
@@ -219,7 +218,7 @@ void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 
 /* ------------------------------------------------------------------------ */
 /* Fused producer.  KV8 page, PR description, attention_rows item: the producer
- * quantizes "the fresh normed/roped row".  The page names the steps but not
+ * quantizes the new row after its normalisation and rotation.  The page names the steps but not
  * their formulas; the readings (RMS norm with a weight over Lc, rotation of the
  * pairs (2j, 2j+1) of Rc by tabulated angles) and the fixed f32 order are in
  * kv8_oracle.h.  Each f32 operation goes through a volatile, so it is rounded
@@ -275,10 +274,10 @@ void orc_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Absorbed decode attention.  KV8 page, PR description, opening paragraph:
- * "the latent is both key and value in the absorbed attention"; attention_rows
- * item: the absorb "score/context loops LUT-dequant inline with the scale
- * hoisted out of the dot".  For one head with query (q_lat, q_rope):
+/* Absorbed decode attention.  KV8 page, PR description, opening paragraph: in the
+ * absorbed attention the latent serves as key and as value; attention_rows item:
+ * the score and context loops decode the codes as they go and apply the row scale
+ * outside each dot product.  For one head with query (q_lat, q_rope):
  *   z_t = sm_scale * ( sLc_t * sum_i q_lat[i] dec(Lc_t[i])
  *                    + sRc_t * sum_j q_rope[j] dec(Rc_t[j]) )
  *   M = max_t z_t,  p_t = exp(z_t - M),  l = sum_t p_t
@@ -385,7 +384,7 @@ void orc_attention_partial_f64(const float* q_lat, const float* q_rope, const ui
 
 /* Split-T merge (flash-decoding): with M = max_s m_s and w_s = exp(m_s - M),
  * out = sum_s w_s o_s / sum_s w_s l_s and lse = M + log(sum_s w_s l_s).  The
- * KV8 page's closing note names "split-T kernels" for long caches; this is the
+ * KV8 page's closing note names split-T kernels for long caches; this is the
  * standard exact recombination of softmax partials. */
 void orc_lse_merge_f64(int n_parts, int H, const double* o_parts, const double* m_parts,
                        const double* l_parts, double* out, double* lse) {

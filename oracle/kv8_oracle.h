@@ -49,7 +49,8 @@ void orc_quantize_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
                        const int64_t* dst_slot, uint8_t* codes, float* scales);
 
 /* ---- fused producer (KV8 page, PR description, attention_rows item: the
- * producer quantizes "the fresh normed/roped row" instead of an f32 copy) ----
+ * producer quantizes the new row after normalisation and rotation instead of
+ * keeping an f32 copy) ----
  * Our reading of the steps the page names but does not spell out:
  *   Lc: RMS norm with a weight, y_i = (x_i * inv) * w_i, inv = 1 / sqrt(ss/512 + eps);
  *   Rc: rotary embedding of the 32 pairs (x[2j], x[2j+1]) by the angle whose

@@ -1,9 +1,9 @@
 """GPU decode parity against the f64 oracle.
 
 Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv
-v2"), PR description (absorbed attention over the e4m3 latent rows, scales
-hoisted out of the dots) and closing note (split-T).  Tolerance: max-abs error
-<= 2e-3 * max|out| per sequence for the CUDA-core kernel (f32 throughout) and
+v2"), PR description (absorbed attention over the e4m3 latent rows, each row
+scale applied outside its dot product) and closing note (split-T).  Tolerance:
+max-abs error <= 2e-3 * max|out| per sequence for the CUDA-core kernel (f32 throughout) and
 <= 1e-2 * max|out| for the tensor-core kernels (reduced-precision MMA operands:
 the query as fp16 (one-CTA kernel) or two e4m3 terms (SM-pair kernel) for the
 scores, the softmax weights as two e4m3 terms for the context; f32

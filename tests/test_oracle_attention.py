@@ -1,10 +1,10 @@
 """Pins for the oracle's absorbed MLA decode attention (CPU only).
 
 Method: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv
-v2"), PR description: "the latent is both key and value in the absorbed
-attention"; attention_rows item: score and context loops dequantize inline
-"with the scale hoisted out of the dot"; Validation paragraph: the fp8 path is
-checked against a "dequantized-host reference".  The oracle is pinned to
+v2"), PR description: the latent is key and value at once in the absorbed
+attention; attention_rows item: the score and context loops decode the codes as
+they go, the row scale applied outside each dot product; Validation paragraph:
+the fp8 path is checked against a reference on the host over dequantized rows.  The oracle is pinned to
 torch's scaled-dot-product attention over explicitly dequantized rows (a
 library routine), closed forms (T = 1, identical rows, q = 0), invariants
 (permutation, split-T merge, paged layout) and its own f32/f64 agreement.

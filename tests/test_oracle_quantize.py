@@ -1,9 +1,9 @@
 """Pins for the oracle's per-row quantizer (CPU only).
 
 Rules: KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU + CUDA) with .coli_kv
-v2"), PR description: "per-row f32 amax/448 scale"; expanded summary: Lc and
-Rc get "one f32 amax/448 scale each"; c/kv_fp8.h item: "per-row quantizer with a
-subnormal-amax guard (448/amax would overflow to +inf)".  Checked against numpy's
+v2"), PR description and expanded summary: Lc and Rc each get an f32 scale
+amax/448; c/kv_fp8.h item: rows whose amax is subnormal (448/amax would overflow
+to +inf) are guarded.  Checked against numpy's
 f32 division, torch's e4m3fn cast, the format's spacing bound and invariants.
 """
 import os

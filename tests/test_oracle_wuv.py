@@ -1,8 +1,8 @@
 """Pins of the oracle's W_UV epilogue (CPU only).
 
 The absorbed attention of the KV8 page ("KV8=1: fp8 e4m3 latent KV cache (CPU +
-CUDA) with .coli_kv v2", PR description: "the latent is both key and value in
-the absorbed attention") leaves the context in latent space; the per-head
+CUDA) with .coli_kv v2", PR description: the latent is key and value at once in
+the absorbed attention) leaves the context in latent space; the per-head
 projection W_UV maps it to the value heads.  Pinned against the bf16 format's
 definition, a selection matrix, a brute-force triple loop and linearity, so a
 transposed weight or a swapped head index fails.
