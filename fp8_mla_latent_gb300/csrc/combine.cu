@@ -8,15 +8,13 @@
 // w_s = 2^(m_s - M):
 //   out = sum_s w_s o_s / sum_s w_s l_s,   lse = ln2 * (M + log2 sum_s w_s l_s).
 // Two forms.  With fewer than 1024 (sequence, head) pairs, one CTA of 256
-// threads per pair: the maxima and weights of the splits by block reductions,
-// weights kept in shared memory; thread i of half q sums channels 4i..4i+3 over
-// the splits s = q, q+2, ... in order, eight splits' loads in flight, and the two
-// halves are added (half 0 first).  Otherwise one warp per pair, eight per CTA,
-// no block barriers: the warp takes M by a butterfly over its lanes' strided
-// maxima, then walks the splits in order, every lane computing the same weight
-// w_s and running denominator (so the sum order is fixed and no reduction is
-// needed) while it accumulates its 16 channels (four 16-byte pieces, 512 B per
-// warp load, coalesced); the splits' loads go out two splits ahead of their use.
+// threads per pair (described above the kernel).  Otherwise one warp per pair,
+// eight per CTA, no block barriers: the warp takes M by a butterfly over its
+// lanes' strided maxima, then walks the splits in order, every lane computing the
+// same weight w_s and running denominator (so the sum order is fixed and no
+// reduction is needed) while it accumulates its 16 channels (four 16-byte pieces,
+// 512 B per warp load, coalesced); the splits' loads go out two splits ahead of
+// their use.
 // Both forms are deterministic.
 #include "kv8_common.cuh"
 
@@ -31,25 +29,23 @@ constexpr int AHEAD = 2;                // splits whose loads are in flight per 
 // flight.  Many pairs come with few splits: one warp per pair.
 constexpr int64_t WARP_PATH_MIN = 1024;
 
-constexpr int WCHUNK = 1024;    // split weights held in shared memory at a time
+// CTA form: 256 threads, two groups of 128; thread i of group q holds channels
+// 4i..4i+3 of the splits s = q (mod 2).  Each pass takes up to PASS splits: all
+// of a thread's partial loads (PASS / 2 of them) and the splits' (m, l) go out
+// together, then the block maximum, the weights 2^(m_s - M) and the denominator
+// (thread 0, in split order) come from shared memory, each group sums its splits
+// in order, and the two groups are added in order.  Two CTAs fit on an SM, so
+// 128 heads of two sequences run in one wave.  Deterministic.
+constexpr int CT4 = 256;
+constexpr int PASS = 40;
+constexpr int PER = PASS / 2;   // partial loads per thread per pass
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  const float r = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
-                        fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
-  __syncthreads();
-  return r;
-}
-
-__global__ void __launch_bounds__(CT) combine_cta_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(CT4) combine_cta_kernel(DecodeArgs a) {
   const int h = blockIdx.x, b = blockIdx.y;
   __shared__ long long s_first, s_count;
-  __shared__ float red[8];
-  __shared__ float4 half1[128];
-  __shared__ float wsh[WCHUNK];
+  __shared__ float red[16];
+  __shared__ float ms[PASS], ls[PASS], wsh[PASS];
+  __shared__ float4 grp[128];
   if (threadIdx.x == 0) {
     const int64_t* e = a.seg + ((int64_t)b * a.plan.n_hg + h / a.plan.hg) * 2;
     s_first = e[0];
@@ -59,55 +55,60 @@ __global__ void __launch_bounds__(CT) combine_cta_kernel(DecodeArgs a) {
   const int64_t first = s_first, ns = s_count;
   const int hl = h % a.plan.hg, hg = a.plan.hg;
   auto part = [&](int64_t s) -> int64_t { return (first + s) * hg + hl; };
+  const int q = threadIdx.x >> 7, i = threadIdx.x & 127;  // group, channel quad
+  const float4* o = reinterpret_cast<const float4*>(a.ws_o) + i;
 
+  // the maximum over every split first (one pass over m)
   float M = -INFINITY;
-  for (int64_t s = threadIdx.x; s < ns; s += CT) M = fmaxf(M, a.ws_m[part(s)]);
-  M = block_max(M, red);
+  for (int64_t s = threadIdx.x; s < ns; s += CT4) M = fmaxf(M, a.ws_m[part(s)]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int k = 1; k < CT4 / 32; ++k) M = fmaxf(M, red[k]);
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Lsum = 0.f;  // thread 0's running denominator, in split order
-  if (M != -INFINITY) {
-    for (int64_t c0 = 0; c0 < ns; c0 += WCHUNK) {
-      const int n = (int)((ns - c0) < WCHUNK ? (ns - c0) : WCHUNK);
-      for (int s = threadIdx.x; s < n; s += CT) {
-        const float ms = a.ws_m[part(c0 + s)];
-        wsh[s] = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0)
-        for (int s = 0; s < n; ++s) Lsum += wsh[s] * a.ws_l[part(c0 + s)];
-      const int q = threadIdx.x >> 7;
-      const float4* o = reinterpret_cast<const float4*>(a.ws_o) + (threadIdx.x & 127);
-      int s = q;
-      for (; s + 14 < n; s += 16) {
-        float4 v[8];
+  float L = 0.f;  // thread 0's denominator, in split order
+  for (int64_t c0 = 0; M != -INFINITY && c0 < ns; c0 += PASS) {
+    const int n = (int)((ns - c0) < PASS ? (ns - c0) : PASS);
+    float4 v[PER];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = o[part(c0 + s + 2 * k) * (DL / 4)];
+    for (int k = 0; k < PER; ++k) {
+      const int s = q + 2 * k;
+      v[k] = s < n ? o[part(c0 + s) * (DL / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();  // the previous pass is done with ms / ls / wsh
+    if (threadIdx.x < n) {
+      ms[threadIdx.x] = a.ws_m[part(c0 + threadIdx.x)];
+      ls[threadIdx.x] = a.ws_l[part(c0 + threadIdx.x)];
+    }
+    __syncthreads();
+    if (threadIdx.x < n) wsh[threadIdx.x] = ms[threadIdx.x] == -INFINITY ? 0.f : exp2f(ms[threadIdx.x] - M);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int s = 0; s < n; ++s) L += wsh[s] * ls[s];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float w = wsh[s + 2 * k];
-          acc.x += w * v[k].x; acc.y += w * v[k].y; acc.z += w * v[k].z; acc.w += w * v[k].w;
-        }
-      }
-      for (; s < n; s += 2) {
+    for (int k = 0; k < PER; ++k) {
+      const int s = q + 2 * k;
+      if (s < n) {
         const float w = wsh[s];
-        const float4 v = o[part(c0 + s) * (DL / 4)];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+        acc.x += w * v[k].x; acc.y += w * v[k].y; acc.z += w * v[k].z; acc.w += w * v[k].w;
       }
-      __syncthreads();
     }
   }
-  if (threadIdx.x >= 128) half1[threadIdx.x - 128] = acc;
-  if (threadIdx.x == 0) red[0] = Lsum;
+  if (q > 0) grp[i] = acc;
+  if (threadIdx.x == 0) red[0] = L;
   __syncthreads();
-  if (threadIdx.x >= 128) return;
-  const float4 a1 = half1[threadIdx.x];
-  acc.x += a1.x; acc.y += a1.y; acc.z += a1.z; acc.w += a1.w;
-  const float L = red[0];
+  if (q > 0) return;
+  const float4 x = grp[i];
+  acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+  L = red[0];
   const float inv = (L > 0.f) ? 1.0f / L : 0.f;
-  float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  reinterpret_cast<float4*>(a.out + ((int64_t)b * a.H + h) * DL)[threadIdx.x] = r;
-  if (a.lse != nullptr && threadIdx.x == 0)
+  reinterpret_cast<float4*>(a.out + ((int64_t)b * a.H + h) * DL)[i] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (a.lse != nullptr && i == 0)
     a.lse[(int64_t)b * a.H + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
@@ -179,7 +180,7 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s) {
     combine_warp_kernel<<<(unsigned)((warps + WPC - 1) / WPC), CT, 0, s>>>(a);
   } else {
     dim3 grid(a.H, a.B);
-    combine_cta_kernel<<<grid, CT, 0, s>>>(a);
+    combine_cta_kernel<<<grid, CT4, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
