@@ -61,7 +61,8 @@ def source_hash(files):
 
 
 KERNEL_SOURCES = {
-    "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "decode_tc": ["fp8_mla_latent_gb300/csrc/decode_tc.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh",
+                  "fp8_mla_latent_gb300/csrc/tc_ptx.cuh"],
     "decode_pair": ["fp8_mla_latent_gb300/csrc/decode_pair.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh",
                     "fp8_mla_latent_gb300/csrc/tc_ptx.cuh"],
     "produce_rows": ["fp8_mla_latent_gb300/csrc/quantize.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
