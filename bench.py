@@ -339,8 +339,8 @@ def run_ours(args, rank, world, local_rank):
     value = kv_bytes / (ms_step * 1e-3) / 1e9
     peaks = load_peaks()
     flops = FLOP_PER_TOKEN_HEAD * w.total_tokens * w.H
-    if plan_variant == pkg.KV8_DECODE_TCGEN05_PAIR:
-        kernel = "decode_pair"
+    if plan_variant in (pkg.KV8_DECODE_TCGEN05_PAIR, pkg.KV8_DECODE_TCGEN05_CTA):
+        kernel = "decode_pair" if plan_variant == pkg.KV8_DECODE_TCGEN05_PAIR else "decode_tc"
         # both contractions on e4m3 operands: the e4m3 tensor peak is twice the measured
         # bf16 dense peak (the nominal fp8 / bf16 ratio)
         p8 = 2 * peaks["bf16_tflops"] * 1e12
@@ -354,26 +354,6 @@ def run_ours(args, rank, world, local_rank):
             roof = {"bound": "hbm", "achieved": w.kv_bytes() / (ms_dec * 1e-3) / 1e9,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_note": f"{peaks['src']} copy",
                     "tensor_frac": flops / (ms_dec * 1e-3) / p8}
-    elif plan_variant == pkg.KV8_DECODE_TCGEN05_CTA:
-        kernel = "decode_tc"
-        # two contractions, two operand types: the scores (2*576*H FLOP per token) on fp16
-        # operands at the measured bf16 rate, the context (2*512*H) on e4m3 operands at twice
-        # it (the nominal fp8 / bf16 ratio); the peak is the FLOP-weighted one of the two
-        f16_flops = 2 * 576 * w.total_tokens * w.H
-        f8_flops = flops - f16_flops
-        p16 = peaks["bf16_tflops"] * 1e12
-        t_tensor = f16_flops / p16 + f8_flops / (2 * p16)
-        t_hbm = w.kv_bytes() / (peaks["hbm_gbs"] * 1e9)
-        if t_tensor >= t_hbm:
-            roof = {"bound": "tensor", "achieved": flops / (ms_dec * 1e-3) / 1e12,
-                    "peak": flops / t_tensor / 1e12, "unit": "TFLOP/s",
-                    "peak_note": f"{peaks['src']} bf16 dense burst for the fp16 score FLOPs, twice "
-                                 "it for the e4m3 context FLOPs, weighted by FLOPs",
-                    "frac_of_bf16_peak": flops / (ms_dec * 1e-3) / p16,
-                    "flops_by_operand": {"fp16": f16_flops, "e4m3": f8_flops}}
-        else:
-            roof = {"bound": "hbm", "achieved": w.kv_bytes() / (ms_dec * 1e-3) / 1e9,
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "peak_note": f"{peaks['src']} copy"}
     else:
         kernel = "decode_simt"
         alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
@@ -411,10 +391,10 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        # per step: the fresh rows' quantizer (append), the query prep (SM-pair kernel
-        # only), the decode kernel and the combine kernel
+        # per step: the fresh rows' quantizer (append), the query prep (tensor-core
+        # kernels), the decode kernel and the combine kernel
         "gpu_launches": args.steps * ((1 if fresh is not None else 0) +
-                                     (2 if plan_variant == pkg.KV8_DECODE_TCGEN05_PAIR else 1) + 1),
+                                     (1 if plan_variant == pkg.KV8_DECODE_SIMT else 2) + 1),
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }
@@ -428,7 +408,7 @@ DECODE_ORDER = ("tiny", "single", "batched", "append", "long")
 # what each decode kernel computes in (the cache is e4m3 in every case)
 DTYPES = {
     1: "e4m3 cache; f32 arithmetic on CUDA cores",
-    3: "e4m3 cache; fp16 query and two-term e4m3 weights on tcgen05; f32 accumulation",
+    3: "e4m3 cache; two-term e4m3 query and two-term e4m3 weights on tcgen05; f32 accumulation",
     4: "e4m3 cache; two-term e4m3 query and two-term e4m3 weights on tcgen05; f32 accumulation",
 }
 

@@ -24,7 +24,7 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   if (v == kTcPair) {
     p.hg = 128;  // MMA M = heads of the item, on a pair of SMs
   } else if (v == kTcCta) {
-    p.hg = H <= 16 ? 16 : (H <= 32 ? 32 : 64);  // MMA N = heads per CTA
+    p.hg = H <= 16 ? 16 : 32;  // heads per CTA (the MMA N is twice that: hi and lo terms)
   } else {
     p.hg = 4;
   }
@@ -47,7 +47,7 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   off = align_up(off + parts * 4, 256);
   p.off_o = off;
   off = align_up(off + parts * DL * 4, 256);
-  if (v == kTcPair) {
+  if (v == kTcPair || v == kTcCta) {
     p.off_q8 = off;
     off = align_up(off + (int64_t)B * H * Q8_BYTES, 256);
     p.off_cq = off;

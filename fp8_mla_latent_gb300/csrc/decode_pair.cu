@@ -129,9 +129,8 @@ constexpr int TOTAL_S = OFF_STG + P_BYTES;
 constexpr int OFF_P = 4096;                  // context: 2 payloads / context operands
 constexpr int OFF_VRING = OFF_P + 2 * P_STRIDE;
 constexpr int TOTAL_C = OFF_VRING + NVT * VTILE;
-constexpr int PT_N = 256;                    // block-table entries of an item kept in shared memory
-constexpr int OFF_PT = TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C;  // both CTAs: [PT_N] int32
-constexpr int SMEM = OFF_PT + PT_N * 4 + 1024;
+constexpr int OFF_PT = TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C;  // both CTAs: [PT_PAGES] int32
+constexpr int SMEM = OFF_PT + PT_PAGES * 4 + 1024;
 // score CTA TMEM columns: S_L, S_R (one tile), then the Lc query's hi and lo terms
 // (e4m3, four channels per column) as the A operand of the score MMAs
 constexpr int T_SL = 0, T_SR = 128, T_QH = 256, T_QL = 384;
@@ -143,23 +142,6 @@ static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits i
 static_assert((CHUNK % 16) == 0 && (OFF_STG % 16) == 0, "bulk-copied chunks");
 static_assert(SMEM <= 232448, "shared memory above the per-CTA limit");
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-// byte offset of 16-byte unit u of row r in a 128-byte-swizzled K-major atom
-__device__ __forceinline__ uint32_t sw128(int r, int u) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
-}
 // byte offset of 16-byte unit u (0..3) of head row r of a payload chunk: rows of
 // 64 bytes, the unit index turned by the row so that the eight rows a quarter
 // warp touches at once fall on distinct banks
@@ -221,61 +203,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Per-tile page facts.
-struct TileRows {
-  int64_t s0, s1;  // cache slot of the tile's first / second page, or -1 (absent or unmapped)
-  int nv;          // tokens of the tile inside the item
-};
-// Cache slot of token t of the item starting at token t0: its block-table entry
-// from the item's copy in shared memory (the first PT_N pages), else from global
-// memory; -1 (and the error bit) for an entry out of range.
-__device__ __forceinline__ int64_t item_slot(const DecodeArgs& a, int b, int64_t t, int64_t t0,
-                                             const int32_t* pt) {
-  if (a.block_table == nullptr) return t;
-  const int64_t k = (t >> 6) - (t0 >> 6);
-  const int32_t blk = k < PT_N ? pt[k] : __ldg(&a.block_table[(int64_t)b * a.max_blocks + (t >> 6)]);
-  if (blk < 0 || (int64_t)blk >= a.n_blocks) {
-    atomicOr(a.err, ERR_BLOCK_TABLE);
-    return -1;
-  }
-  return (int64_t)blk * PAGE + (t & (PAGE - 1));
-}
-// The item's first PT_N block-table entries into shared memory, by all lanes of
-// the calling warp (one round trip instead of a dependent lookup per page).
-__device__ __forceinline__ void load_page_table(const DecodeArgs& a, int b, int64_t t0,
-                                                int64_t t_end, int32_t* pt, int lane) {
-  if (a.block_table != nullptr) {
-    const int64_t p0 = t0 >> 6, np = ((t_end + PAGE - 1) >> 6) - p0;
-    for (int k = lane; k < PT_N && k < np; k += 32)
-      pt[k] = __ldg(&a.block_table[(int64_t)b * a.max_blocks + p0 + k]);
-  }
-  __syncwarp();
-}
-__device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int64_t t0, int64_t t_end,
-                                              int i, const int32_t* pt) {
-  TileRows r;
-  const int64_t tb = t0 + (int64_t)i * TILE;
-  const int64_t n = t_end - tb;
-  r.nv = n < TILE ? (int)n : TILE;
-  r.s0 = item_slot(a, b, tb, t0, pt);
-  r.s1 = r.nv > PAGE ? item_slot(a, b, tb + PAGE, t0, pt) : -1;
-  return r;
-}
-// The facts packed in a word the loading thread leaves in shared memory for the
-// lane warps: tokens inside the item (0..128) in bits 0..7, first / second page
-// present in bits 8 / 9.
-constexpr uint32_t FULL_TILE = TILE | 0x300u;
-__device__ __forceinline__ uint32_t pack_facts(const TileRows& r) {
-  return (uint32_t)r.nv | (r.s0 >= 0 ? 0x100u : 0u) | (r.s1 >= 0 ? 0x200u : 0u);
-}
 // tokens with data in part k (tokens [32 k, 32 k + 32)) of the tile
 __device__ __forceinline__ int part_tokens(uint32_t f, int k) {
   const int n = (int)(f & 0xFFu) - PART * k;
   return ((f >> (8 + (k >> 1))) & 1u) ? min(max(n, 0), PART) : 0;
-}
-// row r of the tile holds data
-__device__ __forceinline__ bool row_has(uint32_t f, int r) {
-  return r < (int)(f & 0xFFu) && ((f >> (8 + r / PAGE)) & 1u) != 0u;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
@@ -973,23 +904,14 @@ __global__ void __launch_bounds__(256) prep_query_kernel(const DecodeArgs a) {
   if (lane == 0) a.cq[head] = a.sm_scale * LOG2E / sc;
 }
 
-// 1-D tensor map of the row scales (f32, two per slot): boxes of 128 floats (one
-// page); floats past the end read as zeros.
-cudaError_t make_scale_map(const DecodeArgs& a, CUtensorMap* map) {
-  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
-  if (rows < 1 || a.scales == nullptr) {
-    memset(map, 0, sizeof(*map));
-    return cudaSuccess;
-  }
-  if (2 * rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
-  const cuuint64_t dims[1] = {(cuuint64_t)(2 * rows)};
-  const cuuint64_t strides[1] = {(cuuint64_t)(2 * rows) * 4};  // unused for one dimension
-  const cuuint32_t box[1] = {2 * PAGE};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(a.scales), dims,
-                      strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 }  // namespace
+
+cudaError_t launch_prep_query(const DecodeArgs& a, cudaStream_t s) {
+  if (a.q8 == nullptr || a.cq == nullptr) return cudaErrorInvalidValue;  // no room planned for them
+  const int64_t heads = (int64_t)a.B * a.H;
+  if (heads > 0) prep_query_kernel<<<(unsigned)((heads + 7) / 8), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 // Pairs that can be resident at once (clusters of two on this device).
 cudaError_t pair_capacity(int* pairs) {
@@ -1025,9 +947,8 @@ cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = make_scale_map(d, &smap);
   if (e != cudaSuccess) return e;
-  if (d.q8 == nullptr || d.cq == nullptr) return cudaErrorInvalidValue;  // not a pair plan
-  const int64_t heads = (int64_t)d.B * d.H;
-  if (heads > 0) prep_query_kernel<<<(unsigned)((heads + 7) / 8), 256, 0, s>>>(d);
+  e = launch_prep_query(d, s);
+  if (e != cudaSuccess) return e;
   decode_pair_kernel<<<2 * d.plan.max_items, NTHREADS, SMEM, s>>>(d, kmap, smap);
   return cudaGetLastError();
 }

@@ -189,4 +189,82 @@ __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkIt
   });
 }
 
+// ---------------------------------------------------------------------------
+// Pages of a work item, for the tensor-core kernels: the item's block-table
+// entries are read once into shared memory, and every tile's two pages become
+// cache slots (or -1) from there.
+
+constexpr int PT_PAGES = 256;  // block-table entries of an item kept in shared memory
+
+// Per-tile page facts.
+struct TileRows {
+  int64_t s0, s1;  // cache slot of the tile's first / second page, or -1 (absent or unmapped)
+  int nv;          // tokens of the tile inside the item
+};
+// Cache slot of token t of the item starting at token t0: its block-table entry
+// from the item's copy in shared memory (the first PT_PAGES pages), else from global
+// memory; -1 (and the error bit) for an entry out of range.
+__device__ __forceinline__ int64_t item_slot(const DecodeArgs& a, int b, int64_t t, int64_t t0,
+                                             const int32_t* pt) {
+  if (a.block_table == nullptr) return t;
+  const int64_t k = (t >> 6) - (t0 >> 6);
+  const int32_t blk = k < PT_PAGES ? pt[k] : __ldg(&a.block_table[(int64_t)b * a.max_blocks + (t >> 6)]);
+  if (blk < 0 || (int64_t)blk >= a.n_blocks) {
+    atomicOr(a.err, ERR_BLOCK_TABLE);
+    return -1;
+  }
+  return (int64_t)blk * PAGE + (t & (PAGE - 1));
+}
+// The item's first PT_PAGES block-table entries into shared memory, by all lanes of
+// the calling warp (one round trip instead of a dependent lookup per page).
+__device__ __forceinline__ void load_page_table(const DecodeArgs& a, int b, int64_t t0,
+                                                int64_t t_end, int32_t* pt, int lane) {
+  if (a.block_table != nullptr) {
+    const int64_t p0 = t0 >> 6, np = ((t_end + PAGE - 1) >> 6) - p0;
+    for (int k = lane; k < PT_PAGES && k < np; k += 32)
+      pt[k] = __ldg(&a.block_table[(int64_t)b * a.max_blocks + p0 + k]);
+  }
+  __syncwarp();
+}
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int64_t t0, int64_t t_end,
+                                              int i, const int32_t* pt) {
+  TileRows r;
+  const int64_t tb = t0 + (int64_t)i * TILE;
+  const int64_t n = t_end - tb;
+  r.nv = n < TILE ? (int)n : TILE;
+  r.s0 = item_slot(a, b, tb, t0, pt);
+  r.s1 = r.nv > PAGE ? item_slot(a, b, tb + PAGE, t0, pt) : -1;
+  return r;
+}
+// The facts packed in a word the loading thread leaves in shared memory for the
+// warps that read the tile: tokens inside the item (0..128) in bits 0..7, first /
+// second page present in bits 8 / 9.
+constexpr uint32_t FULL_TILE = TILE | 0x300u;
+__device__ __forceinline__ uint32_t pack_facts(const TileRows& r) {
+  return (uint32_t)r.nv | (r.s0 >= 0 ? 0x100u : 0u) | (r.s1 >= 0 ? 0x200u : 0u);
+}
+// row r of the tile holds data
+__device__ __forceinline__ bool row_has(uint32_t f, int r) {
+  return r < (int)(f & 0xFFu) && ((f >> (8 + r / PAGE)) & 1u) != 0u;
+}
+
+// 16-byte shared-memory stores and loads.
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// Byte offset of 16-byte unit u of row r in a 128-byte-swizzled K-major atom.
+__device__ __forceinline__ uint32_t sw128(int r, int u) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
+}
+
 }  // namespace kv8

@@ -34,8 +34,8 @@ struct SplitPlan {
   // byte offsets inside the workspace; the header (error word, then the item
   // table) is cleared by every split launch
   int64_t hdr_bytes, off_seg, off_m, off_l, off_o;
-  // SM-pair kernel only (0 otherwise): the queries in the score operand's form,
-  // written by the query-prep launch: [B][H][Q8_BYTES] e4m3 terms, [B][H] f32 c_h
+  // tensor-core kernels only (0 otherwise): the queries in the score operand's
+  // form, written by the query-prep launch: [B][H][Q8_BYTES] e4m3 terms, [B][H] f32 c_h
   int64_t off_q8, off_cq;
 };
 
@@ -65,8 +65,8 @@ struct DecodeArgs {
   float* ws_m;                 // [max_items][hg]   running max, log2 units
   float* ws_l;                 // [max_items][hg]   sum of exp2(z - m)
   float* ws_o;                 // [max_items][hg][512] unnormalised context
-  uint8_t* q8;                 // [B][H][Q8_BYTES] prepared queries (SM-pair kernel), or nullptr
-  float* cq;                   // [B][H] their scale factors c_h (SM-pair kernel), or nullptr
+  uint8_t* q8;                 // [B][H][Q8_BYTES] prepared queries (tensor-core kernels), or nullptr
+  float* cq;                   // [B][H] their scale factors c_h (tensor-core kernels), or nullptr
   SplitPlan plan;
 };
 
@@ -93,15 +93,19 @@ inline cudaError_t per_device(std::atomic<int> (&memo)[MAX_DEVICES], F&& make, i
 }
 
 // Tensor maps for TMA loads (decode_tc.cu): a tiled map of `rank` dimensions
-// (row strides in bytes, rows past the extent read as zeros), and the e4m3
-// cache's map (boxes of one 64-row page x 128 bytes, 128-byte swizzle).
+// (row strides in bytes, rows past the extent read as zeros), the e4m3 cache's
+// map (boxes of one 64-row page x 128 bytes, 128-byte swizzle) and the row
+// scales' map (1-D, boxes of one page's 128 floats).
 cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, unsigned rank, void* base,
                          const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
                          CUtensorMapSwizzle swizzle);
 cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map);
+cudaError_t make_scale_map(const DecodeArgs& a, CUtensorMap* map);
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s);
+// The queries of both tensor-core kernels in their score operand's form (a.q8, a.cq).
+cudaError_t launch_prep_query(const DecodeArgs& a, cudaStream_t s);
 cudaError_t pair_capacity(int* pairs);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);

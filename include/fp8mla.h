@@ -59,14 +59,13 @@ typedef enum {
  *   SIMT     f32 operands:                      <= 2e-3 * max|out|
  *   TCGEN05  reduced-precision MMA operands on e4m3 tensor cores: the query as
  *            two e4m3 terms on a per-head power-of-two scale (about 8 significant
- *            bits) against the cache's e4m3 values for the scores (the one-CTA
- *            kernel rounds the query to fp16 instead), and the softmax weights as
- *            two e4m3 terms on one scale for the context, which reads the e4m3
- *            cache values as they are:         <= 1e-2 * max|out|
+ *            bits) against the cache's e4m3 values for the scores, and the softmax
+ *            weights as two e4m3 terms on one scale for the context; both read
+ *            the e4m3 cache values as they are:  <= 1e-2 * max|out|
  * (see the test report for the measured worst case of each kernel).
  * TCGEN05 runs the SM-pair kernel (a cluster of two CTAs per work item: one
  * computes scores and softmax, the other the context, for 128 heads) when
- * H > 64, and the one-CTA kernel (16, 32 or 64 heads per CTA) otherwise;
+ * H > 64, and the one-CTA kernel (16 or 32 heads per CTA) otherwise;
  * TCGEN05_CTA and TCGEN05_PAIR force one of the two at any H.              */
 typedef enum {
     KV8_DECODE_AUTO = 0,         /* TCGEN05 when H >= 16, else SIMT              */
