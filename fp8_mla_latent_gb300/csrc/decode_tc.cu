@@ -31,8 +31,9 @@
 // Warp roles (11 warps):
 //   warp 0      loads the item's page table, then per tile the row scales, the Rc
 //               block and the four Lc blocks by TMA (a block as soon as its ring
-//               slot is free), and asks the bulk-copy engine to prefetch the tile
-//               L2_AHEAD tiles on into L2; it owns TMEM.
+//               slot is free); it owns TMEM.  (An L2 prefetch of the tiles ahead
+//               was measured: its bulk requests delay the loads behind them, and
+//               the loop ran 10 % slower with it.)
 //   warp 1      issues the score MMAs of each tile once its blocks are in and its
 //               S buffer is free (S is double-buffered).
 //   warp 2      zeroes the Lc rows that hold no data, then issues the context MMAs
@@ -67,7 +68,6 @@ constexpr int W_TMA = 0, W_MMA = 1, W_CTX = 2, W_SOFT = 3;
 constexpr int NSOFT = 8;
 constexpr int NTHREADS = (W_SOFT + NSOFT) * 32;
 constexpr int NTF = 4;                       // tile-loaded barriers, scale slots, page facts
-constexpr int L2_AHEAD = 4;                  // tiles prefetched into L2 ahead of the TMA loads
 // Lazy rescaling thresholds.  The e4m3 weights P'' = 2^(z - m) (sLc / s_ref)
 // P_TOP are at most 2^TAU * TAU_S * P_TOP = 256 <= 448, and with this little
 // headroom the largest weights of a tile sit near the top of the e4m3 range,
@@ -223,16 +223,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     *abort_flag = 1;
     atomicOr(a.err, ERR_TIMEOUT);
   };
-  auto prefetch_tile = [&](int i) {
-    const int64_t tb = t0 + (int64_t)i * TILE;
-    for (int pg = 0; pg < 2; ++pg) {
-      const int64_t tk = tb + pg * PAGE;
-      if (tk >= t_end) break;
-      const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
-      const int64_t slot = item_slot(a, b, tk, t0, pt);
-      if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
-    }
-  };
+
 
   // ------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
@@ -254,9 +245,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
     load_page_table(a, b, t0, t_end, pt, lane);
-    // the first tiles' lines: ask the bulk-copy engine for them up front
-    if (lane == 0)
-      for (int i = 0; i < L2_AHEAD && i < n_tiles; ++i) prefetch_tile(i);
   } else if (warp >= W_SOFT) {
     // The query of the group's heads in the score MMA's B form: K-block k (Lc
     // channels 128k.., k = 4: Rc) holds NB rows of 128 bytes, row h the hi term of
@@ -293,31 +281,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Per tile: the row scales (one 128-float box per page), then the Rc block
     // and Lc blocks 0..3, each page a 64-row box; all complete on the tile's
     // barrier, armed once with the tile's bytes.  A block's slot is free once the
-    // MMAs that last read it are done.  The whole warp walks the loop; lane 0
-    // issues.
-    bool ok = true;
-    int n_req = 0;  // tiles whose barrier has been armed
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
-      const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
-      const int tf = i % NTF, rs = i % RR;
-      if (!mbar_wait_warp(&bars[C::B_REMPTY + rs], ((i / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
-        ok = false;
-        break;
-      }
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        const int j = 4 * i + blk, ls = j % RL;
-        if (!mbar_wait_warp(&bars[C::B_LEMPTY + ls], ((j / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
+    // MMAs that last read it are done.  Lane 0 alone walks the loop.
+    if (lane == 0) {
+      bool ok = true;
+      int n_req = 0;  // tiles whose barrier has been armed
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
+        const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
+        const int tf = i % NTF, rs = i % RR;
+        uint64_t* tb = &bars[C::B_TFULL + tf];
+        if (!mbar_wait(&bars[C::B_REMPTY + rs], ((i / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          uint64_t* tb = &bars[C::B_TFULL + tf];
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          const int j = 4 * i + blk, ls = j % RL;
+          if (!mbar_wait(&bars[C::B_LEMPTY + ls], ((j / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
+          }
           if (blk == 0) {
             // the tile's page facts travel with its loads (the arrive releases them)
             facts[tf] = pack_facts(tr);
             mbar_arrive_expect_tx(tb, pages * (2u * PAGE * 4u + 5u * PAGE * 128u));
+            n_req = i + 1;
             const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * KBLK;
             if (tr.s0 >= 0) {
               tma_load_1d(sd, &smap, (int)(2 * tr.s0), tb);
@@ -332,20 +320,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (tr.s0 >= 0) tma_load_2d(ld, &kmap, 128 * blk, (int)tr.s0, tb);
           if (tr.s1 >= 0) tma_load_2d(ld + PAGE * 128, &kmap, 128 * blk, (int)tr.s1, tb);
         }
-        if (blk == 0) n_req = i + 1;
-        __syncwarp();
       }
-      if (ok && lane == 0 && i + L2_AHEAD < n_tiles) prefetch_tile(i + L2_AHEAD);
-      __syncwarp();
-    }
-    if (!ok) {
-      // after an abort, let the loads already requested land before the CTA can
-      // leave (a tile requested in part never completes its barrier: that wait
-      // then ends at its bound, after those loads have landed)
-      if (lane == 0) fail();
-      const int zero = 0;
-      for (int i = (n_req > NTF ? n_req - NTF : 0); i < n_req; ++i)
-        (void)mbar_wait(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, &zero, WAIT_NS);
+      if (!ok) {
+        // after an abort, let the loads already requested land before the CTA can
+        // leave (a tile requested in part never completes its barrier: that wait
+        // then ends at its bound, after those loads have landed)
+        fail();
+        const int zero = 0;
+        for (int i = (n_req > NTF ? n_req - NTF : 0); i < n_req; ++i)
+          (void)mbar_wait(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, &zero, WAIT_NS);
+      }
     }
     __syncwarp();
   } else if (warp == W_MMA) {

@@ -90,67 +90,113 @@ __device__ __forceinline__ void record_segment(const DecodeArgs& a, int64_t k, c
   }
 }
 
-__device__ __forceinline__ int64_t tiles_of(const DecodeArgs& a, int b) {
-  return (seq_len_of(a, b) + TILE - 1) / TILE;
+__device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b) {
+  // a length is at most max_blocks * PAGE (or the contiguous cache's rows, below
+  // 2^31), so the count of 128-token tiles fits 32 bits
+  return (uint32_t)((seq_len_of(a, b) + TILE - 1) / TILE);
 }
 
-// Warp-wide (all 32 lanes): number of items if every sequence is cut into
-// pieces of st tiles, times the head groups.
-__device__ __forceinline__ int64_t count_items(const DecodeArgs& a, int64_t st) {
+// Tile counts of the sequences, held in registers: lane l keeps sequences l,
+// l + 32, ... (SEQ_CACHE of them).  With more than 32 * SEQ_CACHE sequences
+// nothing is kept and the counts are read again from seq_lens at every use.
+// (The item plan is found by a search that counts items for several lengths:
+// from registers, in 32-bit arithmetic, that costs each CTA about a microsecond
+// at the start of a call instead of several.)
+constexpr int SEQ_CACHE = 8;
+struct SeqTiles {
+  uint32_t t[SEQ_CACHE];
+  bool cached;
+};
+
+// Warp-wide (all 32 lanes).
+__device__ __forceinline__ void load_tiles(const DecodeArgs& a, SeqTiles& c) {
   const int lane = threadIdx.x & 31;
-  int64_t n = 0;
-  for (int b0 = 0; b0 < a.B; b0 += 32) {
-    const int64_t t = (b0 + lane < a.B) ? tiles_of(a, b0 + lane) : 0;
-    int64_t c = (t + st - 1) / st;
+  c.cached = a.B <= 32 * SEQ_CACHE;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    n += c;
+  for (int k = 0; k < SEQ_CACHE; ++k) {
+    const int b = lane + 32 * k;
+    c.t[k] = (c.cached && b < a.B) ? tiles_of(a, b) : 0u;
   }
-  return n * a.plan.n_hg;
 }
 
-// Warp-wide (all 32 lanes): tiles per item for this call.
-__device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a) {
-  const int lane = threadIdx.x & 31;
-  int64_t total = 0, tmax = 0;
-  for (int b0 = 0; b0 < a.B; b0 += 32) {
-    int64_t t = (b0 + lane < a.B) ? tiles_of(a, b0 + lane) : 0;
-    int64_t m = t;
+// Tiles of sequence 32 k + lane (0 past the last sequence).
+__device__ __forceinline__ uint32_t tiles_at(const DecodeArgs& a, const SeqTiles& c, int k) {
+  if (c.cached) {
+    uint32_t v = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      t += __shfl_xor_sync(0xffffffffu, t, o);
-      const int64_t mo = __shfl_xor_sync(0xffffffffu, m, o);
-      m = mo > m ? mo : m;
+    for (int j = 0; j < SEQ_CACHE; ++j) v = (j == k) ? c.t[j] : v;
+    return v;
+  }
+  const int b = 32 * k + (int)(threadIdx.x & 31);
+  return b < a.B ? tiles_of(a, b) : 0u;
+}
+
+__device__ __forceinline__ uint64_t warp_sum64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Warp-wide: number of items if every sequence is cut into pieces of st tiles
+// (1 <= st < 2^31), times the head groups.
+__device__ __forceinline__ int64_t count_items(const DecodeArgs& a, const SeqTiles& c, uint32_t st) {
+  uint64_t n = 0;
+  if (c.cached) {
+#pragma unroll
+    for (int k = 0; k < SEQ_CACHE; ++k) {
+      if (32 * k >= a.B) break;
+      n += (c.t[k] + (st - 1u)) / st;
     }
+  } else {
+    for (int k = 0; 32 * k < a.B; ++k) {
+      const uint32_t t = tiles_at(a, c, k);
+      n += (t + (st - 1u)) / st;
+    }
+  }
+  return (int64_t)warp_sum64(n) * a.plan.n_hg;
+}
+
+// Warp-wide: tiles per item for this call.
+__device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a, const SeqTiles& c) {
+  uint64_t total = 0;
+  uint32_t tmax = 0;
+  for (int k = 0; 32 * k < a.B; ++k) {
+    const uint32_t t = tiles_at(a, c, k);
     total += t;
+    tmax = t > tmax ? t : tmax;
+  }
+  total = warp_sum64(total);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t m = __shfl_xor_sync(0xffffffffu, tmax, o);
     tmax = m > tmax ? m : tmax;
   }
-  const int64_t jobs = total * a.plan.n_hg;
+  const int64_t jobs = (int64_t)total * a.plan.n_hg;
   int64_t lo = (jobs + a.plan.target - 1) / a.plan.target;
   if (lo < 1) lo = 1;
-  if (tmax <= lo || count_items(a, lo) <= a.plan.target) return lo;
-  if (count_items(a, tmax) > a.plan.target) return lo;  // more pairs than one wave holds
-  int64_t hi = tmax;  // invariant: count(lo) > target >= count(hi); count falls as st grows
-  while (lo + 1 < hi) {
-    const int64_t mid = lo + (hi - lo) / 2;
-    if (count_items(a, mid) <= a.plan.target) hi = mid;
-    else lo = mid;
+  if ((int64_t)tmax <= lo || count_items(a, c, (uint32_t)lo) <= a.plan.target) return lo;
+  if (count_items(a, c, tmax) > a.plan.target) return lo;  // more pairs than one wave holds
+  // invariant: count(lo) > target >= count(hi); the count falls as st grows
+  uint32_t l = (uint32_t)lo, h = tmax;
+  while (l + 1 < h) {
+    const uint32_t mid = l + (h - l) / 2;
+    if (count_items(a, c, mid) <= a.plan.target) h = mid;
+    else l = mid;
   }
-  return hi;
+  return h;
 }
 
-// Warp-wide: walks the sequences 32 at a time with the inclusive scan of their
-// item counts and calls f(b, first item of b, items per head group, st) in every
-// lane for the sequence holding item k (k >= 0) or for sequence want_b (k < 0).
-// Returns false if no sequence matched.
-template <typename F>
-__device__ __forceinline__ bool scan_items(const DecodeArgs& a, int64_t k, int want_b, F&& f) {
+// Warp-wide: the work item with index k; false if k is past the last item.  The
+// sequences are walked 32 at a time with the inclusive scan of their item counts.
+__device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it) {
   const int lane = threadIdx.x & 31;
-  const int64_t st = item_tiles(a);
+  SeqTiles c;
+  load_tiles(a, c);
+  const int64_t st = item_tiles(a, c);
   int64_t base = 0;
-  for (int b0 = 0; b0 < a.B; b0 += 32) {
-    const int b = b0 + lane;
-    const int64_t tiles = (b < a.B) ? tiles_of(a, b) : 0;
+  for (int kk = 0; 32 * kk < a.B; ++kk) {
+    const int b = 32 * kk + lane;
+    const int64_t tiles = tiles_at(a, c, kk);
     const int64_t ns = (tiles + st - 1) / st;
     const int64_t cnt = ns * a.plan.n_hg;
     int64_t inc = cnt;
@@ -160,33 +206,28 @@ __device__ __forceinline__ bool scan_items(const DecodeArgs& a, int64_t k, int w
       if (lane >= o) inc += v;
     }
     const int64_t first = base + inc - cnt;
-    const bool mine = (b < a.B) && (k >= 0 ? (k >= first && k < first + cnt) : (b == want_b));
+    const bool mine = (b < a.B) && k >= first && k < first + cnt;
     const unsigned m = __ballot_sync(0xffffffffu, mine);
     if (m) {
       const int src = __ffs(m) - 1;
-      f(__shfl_sync(0xffffffffu, b, src), __shfl_sync(0xffffffffu, first, src),
-        __shfl_sync(0xffffffffu, ns, src), st);
+      const int bb = __shfl_sync(0xffffffffu, b, src);
+      const int64_t fb = __shfl_sync(0xffffffffu, first, src);
+      const int64_t nsb = __shfl_sync(0xffffffffu, ns, src);
+      const int64_t r = k - fb;
+      const int64_t s = r % nsb;
+      it.b = bb;
+      it.g = (int)(r / nsb);
+      it.t0 = s * st * TILE;
+      const int64_t T = seq_len_of(a, bb);
+      const int64_t e = (s + 1) * st * TILE;
+      it.t1 = e < T ? e : T;
+      it.first = fb + (int64_t)it.g * nsb;
+      it.count = nsb;
       return true;
     }
     base += __shfl_sync(0xffffffffu, inc, 31);
   }
   return false;
-}
-
-// Warp-wide: the work item with index k; false if k is past the last item.
-__device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it) {
-  return scan_items(a, k, -1, [&](int b, int64_t first, int64_t ns, int64_t st) {
-    const int64_t r = k - first;
-    const int64_t s = r % ns;
-    it.b = b;
-    it.g = (int)(r / ns);
-    it.t0 = s * st * TILE;
-    const int64_t T = seq_len_of(a, b);
-    const int64_t e = (s + 1) * st * TILE;
-    it.t1 = e < T ? e : T;
-    it.first = first + (int64_t)it.g * ns;
-    it.count = ns;
-  });
 }
 
 // ---------------------------------------------------------------------------
