@@ -290,114 +290,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t qr = smem_u32(sm + OFF_QR);
     const uint32_t scr = smem_u32(sm + OFF_SCR);
     if (warp == W_TMA) {
+      // The whole warp walks the loop and waits; one elected lane issues.
       int32_t* pt = reinterpret_cast<int32_t*>(sm + OFF_PT);
       load_page_table(a, b, t0, t_end, pt, lane);
-      if (lane == 0) {
-        bool ok = true;
-        auto prefetch_tile = [&](int i) {
-          const int64_t tb = t0 + (int64_t)i * TILE;
-          for (int pg = 0; pg < 2; ++pg) {
-            const int64_t tk = tb + pg * PAGE;
-            if (tk >= t_end) break;
-            const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
-            const int64_t slot = item_slot(a, b, tk, t0, pt);
-            if (slot >= 0) prefetch_l2(a.codes + slot * D, (uint32_t)(nt * D));
-          }
-        };
-        int nk = 0, nsc = 0;  // tiles whose K blocks / row scales were requested
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
-          const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
-          const int sc = i % NSC;
-          // the tile's five blocks complete on one barrier; a slot is free once the
-          // MMAs of the tile two before have read it.  Those MMAs started after the
-          // softmax warps had released tile i - 3, and a warp reads every row
-          // scale and page fact of a tile before it releases it, so the scale slot
-          // of tile i - 4 is free then too.
-          uint64_t* kt = &bars[B_KT + (i & 1)];
+      bool ok = true;
+      auto prefetch_tile = [&](int i) {
+        const int64_t tb = t0 + (int64_t)i * TILE;
+        for (int pg = 0; pg < 2; ++pg) {
+          const int64_t tk = tb + pg * PAGE;
+          if (tk >= t_end) break;
+          const int64_t nt = (t_end - tk < PAGE) ? t_end - tk : PAGE;
+          const int64_t slot = item_slot(a, b, tk, t0, pt);
+          if (slot >= 0) prefetch_l2_warp(a.codes + slot * D, (uint32_t)(nt * D));
+        }
+      };
+      int nk = 0, nsc = 0;  // tiles whose K blocks / row scales were requested
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
+        const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
+        const int sc = i % NSC;
+        // the tile's five blocks complete on one barrier; a slot is free once the
+        // MMAs of the tile two before have read it.  Those MMAs started after the
+        // softmax warps had released tile i - 3, and a warp reads every row
+        // scale and page fact of a tile before it releases it, so the scale slot
+        // of tile i - 4 is free then too.
+        uint64_t* kt = &bars[B_KT + (i & 1)];
 #pragma unroll 1
-          for (int blk = 0; blk < BLKS; ++blk) {
-            const int j = i * BLKS + blk, ks = j % NKS;
-            if (!mbar_wait(&bars[B_KEMPTY + ks], ((j / NKS) & 1) ^ 1, abort_flag, WAIT_NS)) {
-              ok = false;
-              break;
-            }
-            if (blk == 0) {
-              // the tile's page facts travel with its row scales (the arrive releases them)
-              facts[sc] = pack_facts(tr);
-              mbar_arrive_expect_tx(&bars[B_SCFULL + sc], 512u * pages);
-              if (tr.s0 >= 0) tma_load_1d(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
-              if (tr.s1 >= 0)
-                tma_load_1d(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
-              nsc = i + 1;
-              mbar_arrive_expect_tx(kt, 8192u * pages * BLKS);
-              nk = i + 1;
-            }
-            const uint32_t dst = kring + ks * KBLK;
-            if (tr.s0 >= 0) tma_load_2d(dst, &kmap, 128 * blk, (int)tr.s0, kt);
-            if (tr.s1 >= 0) tma_load_2d(dst + 8192, &kmap, 128 * blk, (int)tr.s1, kt);
-          }
-          // then the L2 prefetch of the tiles ahead (the next tile is loaded at once;
-          // after the first, the one L2_AHEAD tiles on)
-          for (int j = (i == 0 ? 2 : i + L2_AHEAD); ok && j <= i + L2_AHEAD && j < n_tiles; ++j)
-            prefetch_tile(j);
-        }
-        if (!ok) {
-          // after an abort, let the loads already requested land before the CTA can
-          // leave (a tile requested in part never completes its barrier: the wait
-          // then ends at its bound, after those loads have landed)
-          fail();
-          const int zero = 0;
-          for (int i = (nk > 2 ? nk - 2 : 0); i < nk; ++i)
-            (void)mbar_wait(&bars[B_KT + (i & 1)], (i >> 1) & 1, &zero, WAIT_NS);
-          for (int i = (nsc > NSC ? nsc - NSC : 0); i < nsc; ++i)
-            (void)mbar_wait(&bars[B_SCFULL + i % NSC], (i / NSC) & 1, &zero, WAIT_NS);
-        }
-      }
-      __syncwarp();
-    } else if (warp == W_MMA) {
-      if (lane == 0) {
-        const uint32_t idS = idesc_f16(128, 128, false, false);  // e4m3 x e4m3 (format 0)
-        const uint64_t kdesc = smem_desc(kring, 16, 1024, SW128);
-        const uint64_t qdesc = smem_desc(qr, 16, 1024, SW128);
-        // the query, and tile 0's K blocks; a later tile's are waited for by the
-        // softmax warps before they release S, so one barrier per tile gates these MMAs
-        bool ok = mbar_wait(&bars[B_QREADY], 0, abort_flag, WAIT_NS) &&
-                  mbar_wait(&bars[B_KT], 0, abort_flag, WAIT_NS);
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          if (!mbar_wait(&bars[B_SEMPTY], (i & 1) ^ 1, abort_flag, WAIT_NS)) {
+        for (int blk = 0; blk < BLKS; ++blk) {
+          const int j = i * BLKS + blk, ks = j % NKS;
+          if (!mbar_wait_warp(&bars[B_KEMPTY + ks], ((j / NKS) & 1) ^ 1, abort_flag, WAIT_NS)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-#pragma unroll 1
-          for (int blk = 0; blk < BLKS; ++blk) {
-            const int ks = (i * BLKS + blk) % NKS;
-            const uint64_t bd = kdesc + (uint64_t)((ks * KBLK) >> 4);
-            if (blk < 4) {
-              // A = the Lc query from TMEM: 8 columns (32 channels) per MMA
-              const uint32_t ah = tmem + T_QH + blk * 32, al = tmem + T_QL + blk * 32;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                mma_f8_ts(tmem + T_SL, ah + kk * 8, bd + 2 * kk, idS, (blk | kk) != 0);
-                mma_f8_ts(tmem + T_SL, al + kk * 8, bd + 2 * kk, idS, 1u);
-              }
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                mma_f8(tmem + T_SR, qdesc + 2 * kk, bd + 2 * kk, idS, kk != 0);
-                mma_f8(tmem + T_SR, qdesc + 4 + 2 * kk, bd + 2 * kk, idS, 1u);
-              }
-            }
-            mma_commit(&bars[B_KEMPTY + ks]);
+          if (blk == 0) {
+            // the tile's page facts travel with its row scales (the arrive releases
+            // them; every lane stores the same word, the elected one among them)
+            facts[sc] = pack_facts(tr);
+            mbar_arrive_expect_tx_warp(&bars[B_SCFULL + sc], 512u * pages);
+            if (tr.s0 >= 0) tma_load_1d_warp(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
+            if (tr.s1 >= 0)
+              tma_load_1d_warp(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
+            nsc = i + 1;
+            mbar_arrive_expect_tx_warp(kt, 8192u * pages * BLKS);
+            nk = i + 1;
           }
-          mma_commit(&bars[B_SFULL]);
+          const uint32_t dst = kring + ks * KBLK;
+          if (tr.s0 >= 0) tma_load_2d_warp(dst, &kmap, 128 * blk, (int)tr.s0, kt);
+          if (tr.s1 >= 0) tma_load_2d_warp(dst + 8192, &kmap, 128 * blk, (int)tr.s1, kt);
         }
-        if (!ok) fail();
-        const int zero = 0;
-        mma_commit(&bars[B_DRAIN]);
-        (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+        // then the L2 prefetch of the tiles ahead (the next tile is loaded at once;
+        // after the first, the one L2_AHEAD tiles on)
+        for (int j = (i == 0 ? 2 : i + L2_AHEAD); ok && j <= i + L2_AHEAD && j < n_tiles; ++j)
+          prefetch_tile(j);
       }
+      if (!ok) {
+        // after an abort, let the loads already requested land before the CTA can
+        // leave (a tile requested in part never completes its barrier: the wait
+        // then ends at its bound, after those loads have landed)
+        if (lane == 0) fail();
+        const int zero = 0;
+        for (int i = (nk > 2 ? nk - 2 : 0); i < nk; ++i)
+          (void)mbar_wait(&bars[B_KT + (i & 1)], (i >> 1) & 1, &zero, WAIT_NS);
+        for (int i = (nsc > NSC ? nsc - NSC : 0); i < nsc; ++i)
+          (void)mbar_wait(&bars[B_SCFULL + i % NSC], (i / NSC) & 1, &zero, WAIT_NS);
+      }
+      __syncwarp();
+    } else if (warp == W_MMA) {
+      // The whole warp walks the loop and waits; one elected lane issues.
+      const uint32_t idS = idesc_f16(128, 128, false, false);  // e4m3 x e4m3 (format 0)
+      const uint64_t kdesc = smem_desc(kring, 16, 1024, SW128);
+      const uint64_t qdesc = smem_desc(qr, 16, 1024, SW128);
+      // the query, and tile 0's K blocks; a later tile's are waited for by the
+      // softmax warps before they release S, so one barrier per tile gates these MMAs
+      bool ok = mbar_wait_warp(&bars[B_QREADY], 0, abort_flag, WAIT_NS) &&
+                mbar_wait_warp(&bars[B_KT], 0, abort_flag, WAIT_NS);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        if (!mbar_wait_warp(&bars[B_SEMPTY], (i & 1) ^ 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int blk = 0; blk < BLKS; ++blk) {
+          const int ks = (i * BLKS + blk) % NKS;
+          const uint64_t bd = kdesc + (uint64_t)((ks * KBLK) >> 4);
+          if (blk < 4) {
+            // A = the Lc query from TMEM: 8 columns (32 channels) per MMA
+            const uint32_t ah = tmem + T_QH + blk * 32, al = tmem + T_QL + blk * 32;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma_f8_ts_warp(tmem + T_SL, ah + kk * 8, bd + 2 * kk, idS, (blk | kk) != 0);
+              mma_f8_ts_warp(tmem + T_SL, al + kk * 8, bd + 2 * kk, idS, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              mma_f8_warp(tmem + T_SR, qdesc + 2 * kk, bd + 2 * kk, idS, kk != 0);
+              mma_f8_warp(tmem + T_SR, qdesc + 4 + 2 * kk, bd + 2 * kk, idS, 1u);
+            }
+          }
+          mma_commit_warp(&bars[B_KEMPTY + ks]);
+        }
+        mma_commit_warp(&bars[B_SFULL]);
+      }
+      if (!ok && lane == 0) fail();
+      const int zero = 0;
+      mma_commit_warp(&bars[B_DRAIN]);
+      (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
       __syncwarp();
     } else {
       // ---------------------------------------------------------- softmax
@@ -473,42 +472,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         const int my_n = part_tokens(facts[sc], part);
         tc_fence_after();
-        // this warp's previous payload copy has read its staging chunk, whose first
-        // 256 bytes now take the part's row scales in planar order (sLc of the 32
-        // tokens, then sRc); lane l reads token l's pair
+        // S for this thread's head and the part's 32 tokens: both loads in flight at
+        // once, and S released as soon as they land (the next tile's score MMAs
+        // overwrite it while this tile's softmax runs)
+        uint32_t rl[PART], rr[PART];
+        tmem_ld32(tmem + lane_addr + T_SL + part * PART, rl);
+        tmem_ld32(tmem + lane_addr + T_SR + part * PART, rr);
+        // meanwhile: this warp's previous payload copy has read its staging chunk,
+        // whose first 256 bytes now take the part's row scales in planar order (sLc
+        // of the 32 tokens, then sRc); lane l reads token l's pair
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
         const float2 sa = reinterpret_cast<const float2*>(sm + OFF_SCR + sc * TILE * 8)[part * PART + lane];
         reinterpret_cast<float*>(stg_p)[lane] = sa.x;
         reinterpret_cast<float*>(stg_p)[PART + lane] = sa.y;
-        __syncwarp();  // also: the TMEM loads are warp-collective (every lane, converged)
-        // u = sLc S_L + sRc S_R for this thread's head and the part's 32 tokens, in
-        // token pairs, S read from TMEM in two halves of 16 tokens (the scales by
-        // broadcast loads: every lane reads the same 16 bytes).  S is released as
-        // soon as both halves are in registers: the next tile's score MMAs overwrite
-        // it while this tile's softmax runs.
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
+        // u = sLc S_L + sRc S_R in token pairs (the scales by broadcast loads: every
+        // lane reads the same 16 bytes)
         const float4* sl4 = reinterpret_cast<const float4*>(stg_p);
         const float4* sr4 = reinterpret_cast<const float4*>(stg_p + PART * 4);
         uint64_t u2[PART / 2];
 #pragma unroll
-        for (int hl = 0; hl < 2; ++hl) {
-          uint32_t rl[16], rr[16];
-          tmem_ld16(tmem + lane_addr + T_SL + part * PART + 16 * hl, rl);
-          tmem_ld16(tmem + lane_addr + T_SR + part * PART + 16 * hl, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // tokens 16 hl + 4k .. + 3
-            const float4 l4 = sl4[4 * hl + k], r4 = sr4[4 * hl + k];
-            const int j = 2 * k;
-            u2[8 * hl + j] = fma2(pk2(r4.x, r4.y), pk2(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1])),
-                                  mul2(pk2(l4.x, l4.y), pk2(__uint_as_float(rl[2 * j]), __uint_as_float(rl[2 * j + 1]))));
-            u2[8 * hl + j + 1] = fma2(pk2(r4.z, r4.w), pk2(__uint_as_float(rr[2 * j + 2]), __uint_as_float(rr[2 * j + 3])),
-                                      mul2(pk2(l4.z, l4.w), pk2(__uint_as_float(rl[2 * j + 2]), __uint_as_float(rl[2 * j + 3]))));
-          }
+        for (int k = 0; k < PART / 4; ++k) {  // tokens 4k .. 4k + 3
+          const float4 l4 = sl4[k], r4 = sr4[k];
+          const int j = 2 * k;
+          u2[j] = fma2(pk2(r4.x, r4.y), pk2(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1])),
+                       mul2(pk2(l4.x, l4.y), pk2(__uint_as_float(rl[2 * j]), __uint_as_float(rl[2 * j + 1]))));
+          u2[j + 1] = fma2(pk2(r4.z, r4.w), pk2(__uint_as_float(rr[2 * j + 2]), __uint_as_float(rr[2 * j + 3])),
+                           mul2(pk2(l4.z, l4.w), pk2(__uint_as_float(rl[2 * j + 2]), __uint_as_float(rl[2 * j + 3]))));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
         // tokens without data (a suffix of the part, in a partial tile) get -inf
         if (my_n < PART) {
 #pragma unroll
@@ -630,70 +625,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t pbuf = smem_u32(sm + OFF_P);
     const uint32_t vring = smem_u32(sm + OFF_VRING);
     if (warp == W_TMA) {
+      // The whole warp walks the loop and waits; one elected lane issues.
       int32_t* pt = reinterpret_cast<int32_t*>(sm + OFF_PT);
       load_page_table(a, b, t0, t_end, pt, lane);
-      if (lane == 0) {
-        bool ok = true;
-        int nv = 0;  // tiles requested
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
-          const int vs = i % NVT;
-          if (!mbar_wait(&bars[B_VEMPTY + vs], ((i / NVT) & 1) ^ 1, abort_flag, WAIT_NS)) {
-            ok = false;
-            break;
-          }
-          facts[vs] = pack_facts(tr);  // released by the arrive below
-          mbar_arrive_expect_tx(&bars[B_VT + vs],
-                                4u * ((tr.s0 >= 0 ? 8192u : 0u) + (tr.s1 >= 0 ? 8192u : 0u)));
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t dst = vring + vs * VTILE + m * KBLK;
-            if (tr.s0 >= 0) tma_load_2d(dst, &kmap, 128 * m, (int)tr.s0, &bars[B_VT + vs]);
-            if (tr.s1 >= 0) tma_load_2d(dst + 8192, &kmap, 128 * m, (int)tr.s1, &bars[B_VT + vs]);
-          }
-          ++nv;
+      bool ok = true;
+      int nv = 0;  // tiles requested
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
+        const int vs = i % NVT;
+        if (!mbar_wait_warp(&bars[B_VEMPTY + vs], ((i / NVT) & 1) ^ 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
         }
-        if (!ok) {
-          fail();
-          const int zero = 0;
-          for (int i = (nv > NVT ? nv - NVT : 0); i < nv; ++i)
-            (void)mbar_wait(&bars[B_VT + i % NVT], (i / NVT) & 1, &zero, WAIT_NS);
+        facts[vs] = pack_facts(tr);  // released by the arrive below (every lane, one word)
+        mbar_arrive_expect_tx_warp(&bars[B_VT + vs],
+                                   4u * ((tr.s0 >= 0 ? 8192u : 0u) + (tr.s1 >= 0 ? 8192u : 0u)));
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t dst = vring + vs * VTILE + m * KBLK;
+          if (tr.s0 >= 0) tma_load_2d_warp(dst, &kmap, 128 * m, (int)tr.s0, &bars[B_VT + vs]);
+          if (tr.s1 >= 0) tma_load_2d_warp(dst + 8192, &kmap, 128 * m, (int)tr.s1, &bars[B_VT + vs]);
         }
+        ++nv;
+      }
+      if (!ok) {
+        if (lane == 0) fail();
+        const int zero = 0;
+        for (int i = (nv > NVT ? nv - NVT : 0); i < nv; ++i)
+          (void)mbar_wait(&bars[B_VT + i % NVT], (i / NVT) & 1, &zero, WAIT_NS);
       }
       __syncwarp();
     } else if (warp == W_MMA) {
-      if (lane == 0) {
-        const uint32_t idV = idesc_f16(128, 256, false, true);  // A = P'' K-major, B = V MN-major
-        const uint64_t pdesc = smem_desc(pbuf, 16, 1024, SW128);
-        const uint64_t vdesc = smem_desc(vring, KBLK, 1024, SW128);
-        bool ok = true;
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          const int pb = i & 1, vs = i % NVT;
-          for (int half = 0; half < 2; ++half) {
-            // operand, V rows and this O half ready (the lane workers' barrier)
-            if (!mbar_wait(&bars[B_RS + half], i & 1, abort_flag, WAIT_NS)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t ad = pdesc + (uint64_t)((pb * P_STRIDE) >> 4);
-            const uint64_t bd = vdesc + (uint64_t)((vs * VTILE + half * 2 * KBLK) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // A: 32 tokens of the hi / lo atom (32 bytes in); B: 32 token rows of V (4 KB in)
-              mma_f8(tmem + half * 256, ad + 2 * kk, bd + 256 * kk, idV, (i > 0 || kk > 0) ? 1u : 0u);
-              mma_f8(tmem + half * 256, ad + (KBLK >> 4) + 2 * kk, bd + 256 * kk, idV, 1u);
-            }
-            mma_commit(&bars[B_ODONE + half]);
+      // The whole warp walks the loop and waits; one elected lane issues.
+      const uint32_t idV = idesc_f16(128, 256, false, true);  // A = P'' K-major, B = V MN-major
+      const uint64_t pdesc = smem_desc(pbuf, 16, 1024, SW128);
+      const uint64_t vdesc = smem_desc(vring, KBLK, 1024, SW128);
+      bool ok = true;
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int pb = i & 1, vs = i % NVT;
+        for (int half = 0; half < 2; ++half) {
+          // operand, V rows and this O half ready (the lane workers' barrier)
+          if (!mbar_wait_warp(&bars[B_RS + half], i & 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          mma_commit(&bars[B_VEMPTY + vs]);
-          mma_commit_mc(&bars[B_PFREE + pb], (uint16_t)0x3);
+          tc_fence_after();
+          const uint64_t ad = pdesc + (uint64_t)((pb * P_STRIDE) >> 4);
+          const uint64_t bd = vdesc + (uint64_t)((vs * VTILE + half * 2 * KBLK) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 32 tokens of the hi / lo atom (32 bytes in); B: 32 token rows of V (4 KB in)
+            mma_f8_warp(tmem + half * 256, ad + 2 * kk, bd + 256 * kk, idV, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_f8_warp(tmem + half * 256, ad + (KBLK >> 4) + 2 * kk, bd + 256 * kk, idV, 1u);
+          }
+          mma_commit_warp(&bars[B_ODONE + half]);
         }
-        if (!ok) fail();
-        const int zero = 0;
-        mma_commit(&bars[B_DRAIN]);
-        (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
+        if (!ok) break;
+        mma_commit_warp(&bars[B_VEMPTY + vs]);
+        mma_commit_mc_warp(&bars[B_PFREE + pb], (uint16_t)0x3);
       }
+      if (!ok && lane == 0) fail();
+      const int zero = 0;
+      mma_commit_warp(&bars[B_DRAIN]);
+      (void)mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_NS);
       __syncwarp();
     } else {
       // ---------------------------------------------------------- operand, V rows,

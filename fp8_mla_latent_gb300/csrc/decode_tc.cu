@@ -281,55 +281,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Per tile: the row scales (one 128-float box per page), then the Rc block
     // and Lc blocks 0..3, each page a 64-row box; all complete on the tile's
     // barrier, armed once with the tile's bytes.  A block's slot is free once the
-    // MMAs that last read it are done.  Lane 0 alone walks the loop.
-    if (lane == 0) {
-      bool ok = true;
-      int n_req = 0;  // tiles whose barrier has been armed
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
-        const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
-        const int tf = i % NTF, rs = i % RR;
-        uint64_t* tb = &bars[C::B_TFULL + tf];
-        if (!mbar_wait(&bars[C::B_REMPTY + rs], ((i / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
+    // MMAs that last read it are done.  The whole warp walks the loop and waits;
+    // one elected lane issues.
+    bool ok = true;
+    int n_req = 0;  // tiles whose barrier has been armed
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
+      const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
+      const int tf = i % NTF, rs = i % RR;
+      uint64_t* tb = &bars[C::B_TFULL + tf];
+      if (!mbar_wait_warp(&bars[C::B_REMPTY + rs], ((i / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
+        ok = false;
+        break;
+      }
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        const int j = 4 * i + blk, ls = j % RL;
+        if (!mbar_wait_warp(&bars[C::B_LEMPTY + ls], ((j / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          const int j = 4 * i + blk, ls = j % RL;
-          if (!mbar_wait(&bars[C::B_LEMPTY + ls], ((j / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
-            ok = false;
-            break;
+        if (blk == 0) {
+          // the tile's page facts travel with its loads (the arrive releases them;
+          // every lane stores the same word, the elected one among them)
+          facts[tf] = pack_facts(tr);
+          mbar_arrive_expect_tx_warp(tb, pages * (2u * PAGE * 4u + 5u * PAGE * 128u));
+          n_req = i + 1;
+          const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * KBLK;
+          if (tr.s0 >= 0) {
+            tma_load_1d_warp(sd, &smap, (int)(2 * tr.s0), tb);
+            tma_load_2d_warp(rd, &kmap, DL, (int)tr.s0, tb);
           }
-          if (blk == 0) {
-            // the tile's page facts travel with its loads (the arrive releases them)
-            facts[tf] = pack_facts(tr);
-            mbar_arrive_expect_tx(tb, pages * (2u * PAGE * 4u + 5u * PAGE * 128u));
-            n_req = i + 1;
-            const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * KBLK;
-            if (tr.s0 >= 0) {
-              tma_load_1d(sd, &smap, (int)(2 * tr.s0), tb);
-              tma_load_2d(rd, &kmap, DL, (int)tr.s0, tb);
-            }
-            if (tr.s1 >= 0) {
-              tma_load_1d(sd + 2 * PAGE * 4, &smap, (int)(2 * tr.s1), tb);
-              tma_load_2d(rd + PAGE * 128, &kmap, DL, (int)tr.s1, tb);
-            }
+          if (tr.s1 >= 0) {
+            tma_load_1d_warp(sd + 2 * PAGE * 4, &smap, (int)(2 * tr.s1), tb);
+            tma_load_2d_warp(rd + PAGE * 128, &kmap, DL, (int)tr.s1, tb);
           }
-          const uint32_t ld = lring + ls * KBLK;
-          if (tr.s0 >= 0) tma_load_2d(ld, &kmap, 128 * blk, (int)tr.s0, tb);
-          if (tr.s1 >= 0) tma_load_2d(ld + PAGE * 128, &kmap, 128 * blk, (int)tr.s1, tb);
         }
+        const uint32_t ld = lring + ls * KBLK;
+        if (tr.s0 >= 0) tma_load_2d_warp(ld, &kmap, 128 * blk, (int)tr.s0, tb);
+        if (tr.s1 >= 0) tma_load_2d_warp(ld + PAGE * 128, &kmap, 128 * blk, (int)tr.s1, tb);
       }
-      if (!ok) {
-        // after an abort, let the loads already requested land before the CTA can
-        // leave (a tile requested in part never completes its barrier: that wait
-        // then ends at its bound, after those loads have landed)
-        fail();
-        const int zero = 0;
-        for (int i = (n_req > NTF ? n_req - NTF : 0); i < n_req; ++i)
-          (void)mbar_wait(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, &zero, WAIT_NS);
-      }
+    }
+    if (!ok) {
+      // after an abort, let the loads already requested land before the CTA can
+      // leave (a tile requested in part never completes its barrier: that wait
+      // then ends at its bound, after those loads have landed)
+      if (lane == 0) fail();
+      const int zero = 0;
+      for (int i = (n_req > NTF ? n_req - NTF : 0); i < n_req; ++i)
+        (void)mbar_wait(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, &zero, WAIT_NS);
     }
     __syncwarp();
   } else if (warp == W_MMA) {

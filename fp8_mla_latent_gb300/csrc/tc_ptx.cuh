@@ -232,6 +232,21 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// kind::f8f6f4 MMA with A in TMEM (as mma_f8_ts), issued by a whole converged
+// warp through elect.sync.  (A thread issuing alone, its other lanes parked,
+// falls behind the tensor pipe when the SM sub-partition's other warps run
+// arithmetic: measured 99 against 64 cycles per M128 N128 K32 MMA.)
+__device__ __forceinline__ void mma_f8_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Commit issued by the calling thread alone that arrives on the barrier at this
 // shared-memory offset in every CTA of `cta_mask` once its MMAs so far are done.
 __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
@@ -306,6 +321,37 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* tmap, int 
   asm volatile(
       "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
       "{%2}], [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same three, issued by a whole converged warp through elect.sync (one
+// elected lane issues; the warp stays converged).  A producer warp whose lane 0
+// runs alone, its other lanes parked, gets few issue slots beside arithmetic-heavy
+// warps of its SM sub-partition.
+__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_warp(uint32_t dst, const void* tmap, int x, int y,
+                                                 uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_1d_warp(uint32_t dst, const void* tmap, int x,
+                                                 uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2}], [%3];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(smem_u32(bar))
       : "memory");
 }
@@ -511,6 +557,14 @@ __device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src
 // L2 prefetch of a contiguous byte range by the bulk-copy engine (no smem).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// The same, issued by a whole converged warp (one elected lane).
+__device__ __forceinline__ void prefetch_l2_warp(const void* p, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.L2.global [%0], %1;\n\t}" ::"l"(p),
+      "r"(bytes)
+      : "memory");
 }
 
 }  // namespace ptx
