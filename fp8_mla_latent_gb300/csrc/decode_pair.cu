@@ -99,8 +99,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 // the same offset in both CTAs: the context CTA's commit multicasts to it)
 constexpr int B_PFREE = 0;                   // [2] score: the context MMAs of the payload buffer's last tile are done
 constexpr int B_KT = B_PFREE + 2;            // [2] score: all K blocks of a tile loaded (by tile parity)
-constexpr int B_KEMPTY = B_KT + 2;           // [NKS] score: K block consumed by the score MMAs
-constexpr int B_SCFULL = B_KEMPTY + NKS;     // [NSC] score: row scales of a tile loaded
+constexpr int B_KEMPTY = B_KT + 2;           // [2] score: a tile's K blocks consumed by its score MMAs (by tile parity)
+constexpr int B_SCFULL = B_KEMPTY + 2;       // [NSC] score: row scales of a tile loaded
 constexpr int B_SFULL = B_SCFULL + NSC;      // score: S of a tile in TMEM
 constexpr int B_SEMPTY = B_SFULL + 1;        // score: S read and next tile's K loaded (16 arrivals)
 constexpr int B_PX = B_SEMPTY + 1;           // [4] score: the four warps of a lane quarter meet
@@ -253,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars[B_RS + i], N_LANE_WARPS);
       mbar_init(&bars[B_ODONE + i], 1);
     }
-    for (int i = 0; i < NKS; ++i) mbar_init(&bars[B_KEMPTY + i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bars[B_KEMPTY + i], 1);
     for (int i = 0; i < NSC; ++i) mbar_init(&bars[B_SCFULL + i], 1);
     mbar_init(&bars[B_SFULL], 1);
     mbar_init(&bars[B_SEMPTY], N_LANE_WARPS);
@@ -309,32 +309,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
         const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
         const int sc = i % NSC;
-        // the tile's five blocks complete on one barrier; a slot is free once the
-        // MMAs of the tile two before have read it.  Those MMAs started after the
-        // softmax warps had released tile i - 3, and a warp reads every row
-        // scale and page fact of a tile before it releases it, so the scale slot
-        // of tile i - 4 is free then too.
+        // the tile's five blocks complete on one barrier and take the slots of the
+        // tile two before, free once that tile's score MMAs are done (one wait per
+        // tile, then every load at once).  Those MMAs started after the softmax
+        // warps had released tile i - 3, and a warp reads every row scale and page
+        // fact of a tile before it releases it, so the scale slot of tile i - 4 is
+        // free then too.
         uint64_t* kt = &bars[B_KT + (i & 1)];
+        if (!mbar_wait_warp(&bars[B_KEMPTY + (i & 1)], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
+          ok = false;
+          break;
+        }
+        // the tile's page facts travel with its row scales (the arrive releases them;
+        // every lane stores the same word, the elected one among them)
+        facts[sc] = pack_facts(tr);
+        mbar_arrive_expect_tx_warp(&bars[B_SCFULL + sc], 512u * pages);
+        if (tr.s0 >= 0) tma_load_1d_warp(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
+        if (tr.s1 >= 0)
+          tma_load_1d_warp(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
+        nsc = i + 1;
+        mbar_arrive_expect_tx_warp(kt, 8192u * pages * BLKS);
+        nk = i + 1;
 #pragma unroll 1
         for (int blk = 0; blk < BLKS; ++blk) {
-          const int j = i * BLKS + blk, ks = j % NKS;
-          if (!mbar_wait_warp(&bars[B_KEMPTY + ks], ((j / NKS) & 1) ^ 1, abort_flag, WAIT_NS)) {
-            ok = false;
-            break;
-          }
-          if (blk == 0) {
-            // the tile's page facts travel with its row scales (the arrive releases
-            // them; every lane stores the same word, the elected one among them)
-            facts[sc] = pack_facts(tr);
-            mbar_arrive_expect_tx_warp(&bars[B_SCFULL + sc], 512u * pages);
-            if (tr.s0 >= 0) tma_load_1d_warp(scr + sc * TILE * 8, &smap, (int)(2 * tr.s0), &bars[B_SCFULL + sc]);
-            if (tr.s1 >= 0)
-              tma_load_1d_warp(scr + sc * TILE * 8 + 512, &smap, (int)(2 * tr.s1), &bars[B_SCFULL + sc]);
-            nsc = i + 1;
-            mbar_arrive_expect_tx_warp(kt, 8192u * pages * BLKS);
-            nk = i + 1;
-          }
-          const uint32_t dst = kring + ks * KBLK;
+          const uint32_t dst = kring + ((i & 1) * BLKS + blk) * KBLK;
           if (tr.s0 >= 0) tma_load_2d_warp(dst, &kmap, 128 * blk, (int)tr.s0, kt);
           if (tr.s1 >= 0) tma_load_2d_warp(dst + 8192, &kmap, 128 * blk, (int)tr.s1, kt);
         }
@@ -372,8 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int blk = 0; blk < BLKS; ++blk) {
-          const int ks = (i * BLKS + blk) % NKS;
-          const uint64_t bd = kdesc + (uint64_t)((ks * KBLK) >> 4);
+          const uint64_t bd = kdesc + (uint64_t)((((i & 1) * BLKS + blk) * KBLK) >> 4);
           if (blk < 4) {
             // A = the Lc query from TMEM: 8 columns (32 channels) per MMA
             const uint32_t ah = tmem + T_QH + blk * 32, al = tmem + T_QL + blk * 32;
@@ -389,8 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
               mma_f8_warp(tmem + T_SR, qdesc + 4 + 2 * kk, bd + 2 * kk, idS, 1u);
             }
           }
-          mma_commit_warp(&bars[B_KEMPTY + ks]);
         }
+        mma_commit_warp(&bars[B_KEMPTY + (i & 1)]);
         mma_commit_warp(&bars[B_SFULL]);
       }
       if (!ok && lane == 0) fail();
