@@ -32,10 +32,11 @@ SplitPlan plan_decode(int B, int H, int64_t max_len, int variant) {
   (void)max_len;
   // One wave: the one-CTA tensor-core kernel holds a whole SM per CTA, the pair
   // kernel two SMs per item (the launch lowers this to the pairs the device
-  // holds at once), the SIMT kernel runs about four CTAs per SM.  Cutting every
+  // holds at once), and the SIMT kernel one CTA per SM as well (its 256 threads
+  // keep four tokens' rows in registers: over 200 registers each).  Cutting every
   // (sequence, head group) into items of ceil(jobs / target) tiles gives at most
   // target + B * n_hg items.
-  p.target = v == kTcPair ? NUM_SMS / 2 : NUM_SMS * (v == kTcCta ? 1 : 4);
+  p.target = v == kTcPair ? NUM_SMS / 2 : NUM_SMS;
   p.max_items = p.target + B * p.n_hg;
   const int64_t parts = (int64_t)p.max_items * p.hg;
   p.off_seg = 64;  // header: error word, then the item table of the split

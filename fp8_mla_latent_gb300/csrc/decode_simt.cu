@@ -24,7 +24,7 @@ constexpr int HG_SIMT = 4;
 constexpr int SWARPS = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(SWARPS * 32)
+__global__ void __launch_bounds__(SWARPS * 32, 1)
 decode_simt_kernel(DecodeArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ WorkItem s_it;
@@ -76,39 +76,56 @@ decode_simt_kernel(DecodeArgs a) {
     for (int k = 0; k < 16; ++k) o[j][k] = 0.f;
   }
 
-  for (int64_t t = t0 + warp; t < t1; t += SWARPS) {
-    const int64_t slot = slot_of(a, b, t);
-    if (slot < 0) continue;  // bad page: counted in the error word, read as empty
-    const uint8_t* row = a.codes + slot * D;
-    const uint4 cl = __ldg(reinterpret_cast<const uint4*>(row) + lane);
-    const uint16_t cr = __ldg(reinterpret_cast<const uint16_t*>(row + DL) + lane);
-    const float2 sc = __ldg(reinterpret_cast<const float2*>(a.scales + slot * 2));
-    float v[16], vr[2];
-    e4m3x4_to_f32(cl.x, v); e4m3x4_to_f32(cl.y, v + 4);
-    e4m3x4_to_f32(cl.z, v + 8); e4m3x4_to_f32(cl.w, v + 12);
-    {
-      const uint32_t h2 = e4m3x2_to_f16x2(cr);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      vr[0] = f.x; vr[1] = f.y;
+  // Tokens t0 + warp, + 8, + 16, ... in that order, four at a time: the four rows'
+  // loads are in flight together (one row at a time is a chain of dependent loads).
+  constexpr int AHEAD = 4;
+  for (int64_t tb = t0 + warp; tb < t1; tb += AHEAD * SWARPS) {
+    uint4 cl[AHEAD];
+    uint16_t cr[AHEAD];
+    float2 sc[AHEAD];
+    bool have[AHEAD];
+#pragma unroll
+    for (int u = 0; u < AHEAD; ++u) {
+      const int64_t t = tb + u * SWARPS;
+      const int64_t slot = t < t1 ? slot_of(a, b, t) : -1;  // a bad page reads as empty
+      have[u] = slot >= 0;
+      if (have[u]) {
+        const uint8_t* row = a.codes + slot * D;
+        cl[u] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+        cr[u] = __ldg(reinterpret_cast<const uint16_t*>(row + DL) + lane);
+        sc[u] = __ldg(reinterpret_cast<const float2*>(a.scales + slot * 2));
+      }
     }
 #pragma unroll
-    for (int j = 0; j < HG_SIMT; ++j) {
-      float dl = 0.f, dr = 0.f;
+    for (int u = 0; u < AHEAD; ++u) {
+      if (!have[u]) continue;
+      float v[16], vr[2];
+      e4m3x4_to_f32(cl[u].x, v); e4m3x4_to_f32(cl[u].y, v + 4);
+      e4m3x4_to_f32(cl[u].z, v + 8); e4m3x4_to_f32(cl[u].w, v + 12);
+      {
+        const uint32_t h2 = e4m3x2_to_f16x2(cr[u]);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        vr[0] = f.x; vr[1] = f.y;
+      }
 #pragma unroll
-      for (int k = 0; k < 16; ++k) dl = fmaf(qL[j][k], v[k], dl);
-      dr = fmaf(qR[j][0], vr[0], dr);
-      dr = fmaf(qR[j][1], vr[1], dr);
-      float z = sc.x * dl + sc.y * dr;  // the row scales, outside the dot products
+      for (int j = 0; j < HG_SIMT; ++j) {
+        float dl = 0.f, dr = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      const float mn = fmaxf(m[j], z);
-      const float alpha = exp2f(m[j] - mn);  // 0 on the first token (m = -inf)
-      const float p = exp2f(z - mn);
-      l[j] = l[j] * alpha + p;
-      const float w = p * sc.x;
+        for (int k = 0; k < 16; ++k) dl = fmaf(qL[j][k], v[k], dl);
+        dr = fmaf(qR[j][0], vr[0], dr);
+        dr = fmaf(qR[j][1], vr[1], dr);
+        float z = sc[u].x * dl + sc[u].y * dr;  // the row scales, outside the dot products
 #pragma unroll
-      for (int k = 0; k < 16; ++k) o[j][k] = fmaf(w, v[k], o[j][k] * alpha);
-      m[j] = mn;
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        const float mn = fmaxf(m[j], z);
+        const float alpha = exp2f(m[j] - mn);  // 0 on the first token (m = -inf)
+        const float p = exp2f(z - mn);
+        l[j] = l[j] * alpha + p;
+        const float w = p * sc[u].x;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[j][k] = fmaf(w, v[k], o[j][k] * alpha);
+        m[j] = mn;
+      }
     }
   }
 
