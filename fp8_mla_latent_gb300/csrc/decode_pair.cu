@@ -139,6 +139,7 @@ static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + 16 <= OFF_XMAX, "barriers, fl
 static_assert(P_BYTES <= P_STRIDE && (P_STRIDE % 1024) == 0 && (OFF_VRING % 1024) == 0,
               "payload layout");
 static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits in its payload buffer");
+static_assert(N_LANE_WARPS * 32 * 33 * 4 <= 2 * P_STRIDE, "the epilogue's staging fits in the payload buffers");
 static_assert((CHUNK % 16) == 0 && (OFF_STG % 16) == 0, "bulk-copied chunks");
 static_assert(SMEM <= 232448, "shared memory above the per-CTA limit");
 
@@ -810,12 +811,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
              mbar_wait_warp(&bars[B_ODONE + 1], (n_tiles - 1) & 1, abort_flag, WAIT_NS);
       }
       if (ok) {
-        // epilogue: the partial's unnormalised o = acc * s_ref / P_TOP
+        // epilogue: the partial's unnormalised o = acc * s_ref / P_TOP.  A thread's
+        // TMEM lane is one head, so each warp turns its 32 heads x 32 columns
+        // around in shared memory (the payload buffers, free now; rows padded to 33
+        // floats, no bank conflicts either way) and stores one head's 32 columns
+        // per instruction: 128 contiguous bytes instead of 32 rows 2 KB apart.
         tc_fence_after();
         __syncwarp();
         const float oscale = sref_fin * (1.0f / P_TOP);
-        float* dst = a.ws_o + (item * HG + hh) * DL;
-        const bool mine = h0 + hh < a.H;
+        float* stage = reinterpret_cast<float*>(sm + OFF_P) + (warp - W_LANE) * (32 * 33);
+        float* dst = a.ws_o + (item * HG + q * 32) * DL;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           const int cbase = half * 256 + part * 64;
@@ -825,13 +830,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             tmem_ld32(tmem + lane_addr + cbase + c0, r);
             tmem_wait_ld();
-            if (mine) {
 #pragma unroll
-              for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(dst + cbase + c0 + k) =
-                    make_float4(__uint_as_float(r[k]) * oscale, __uint_as_float(r[k + 1]) * oscale,
-                                __uint_as_float(r[k + 2]) * oscale, __uint_as_float(r[k + 3]) * oscale);
-            }
+            for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = __uint_as_float(r[k]) * oscale;
+            __syncwarp();
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j)
+              if (h0 + q * 32 + j < a.H) dst[(int64_t)j * DL + cbase + c0 + lane] = stage[j * 33 + lane];
           }
         }
       } else {
