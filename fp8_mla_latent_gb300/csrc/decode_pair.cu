@@ -415,6 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       // operand in shared memory (hi in bytes 0..63, lo in 64..127).  Heads past H
       // are zeros.  The loads overlap the first tiles' K loads.
       const bool real = h0 + hh < a.H;
+      grid_dependency_wait();  // the query-prep launch has completed
       const float c = real ? __ldg(a.cq + (int64_t)b * a.H + h0 + hh) : 0.f;
       {
         const uint4* q8 = reinterpret_cast<const uint4*>(a.q8 + ((int64_t)b * a.H + h0 + hh) * Q8_BYTES);
@@ -857,6 +858,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 // c_h = sm_scale * log2(e) / 2^e undoes the scale in the softmax.  Bytes of a head:
 // Lc hi (channel order), Lc lo, Rc hi, Rc lo.
 __global__ void __launch_bounds__(256) prep_query_kernel(const DecodeArgs a) {
+  grid_dependents_launch();  // the decode kernel's set-up may overlap this launch
   const int64_t head = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // b * H + h
   if (head >= (int64_t)a.B * a.H) return;
   const int lane = threadIdx.x & 31;
@@ -943,8 +945,7 @@ cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = launch_prep_query(d, s);
   if (e != cudaSuccess) return e;
-  decode_pair_kernel<<<2 * d.plan.max_items, NTHREADS, SMEM, s>>>(d, kmap, smap);
-  return cudaGetLastError();
+  return launch_after_prep(decode_pair_kernel, 2 * d.plan.max_items, NTHREADS, SMEM, s, d, kmap, smap);
 }
 
 }  // namespace kv8

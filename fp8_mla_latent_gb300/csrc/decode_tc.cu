@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
     load_page_table(a, b, t0, t_end, pt, lane);
   } else if (warp >= W_SOFT) {
+    grid_dependency_wait();  // the query-prep launch has completed
     // The query of the group's heads in the score MMA's B form: K-block k (Lc
     // channels 128k.., k = 4: Rc) holds NB rows of 128 bytes, row h the hi term of
     // head h and row N + h its lo term (Rc rows use their first 64 bytes).  Heads
@@ -684,8 +685,8 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = launch_prep_query(a, s);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<N><<<a.plan.max_items, NTHREADS, Cfg<N>::SMEM, s>>>(a, kmap, smap);
-  return cudaGetLastError();
+  return launch_after_prep(decode_tc_kernel<N>, a.plan.max_items, NTHREADS, Cfg<N>::SMEM, s, a, kmap,
+                           smap);
 }
 
 }  // namespace

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace kv8 {
 
@@ -106,6 +107,25 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s);
 // The queries of both tensor-core kernels in their score operand's form (a.q8, a.cq).
 cudaError_t launch_prep_query(const DecodeArgs& a, cudaStream_t s);
+
+// Launch of a decode kernel right after the query-prep launch on the same stream,
+// as its programmatic dependent: the kernel's set-up overlaps the prep launch, and
+// its threads wait (griddepcontrol.wait) before they read the prepared queries.
+template <typename... P, typename... A>
+cudaError_t launch_after_prep(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 cudaError_t pair_capacity(int* pairs);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);

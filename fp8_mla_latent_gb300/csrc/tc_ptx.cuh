@@ -60,6 +60,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch.  A primary grid lets the grid launched after it
+// (with the programmatic-serialization attribute) start early; that grid's
+// threads wait, before they read what the primary wrote, until the primary has
+// completed and its memory operations are visible.  Without the attribute the
+// wait returns at once.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
