@@ -10,10 +10,10 @@
 //   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)
 //
 // One CTA = one work item (sequence, group of N heads, range of 128-token tiles).
-// Every byte of a tile is loaded once, by TMA, into a ring of [128 tokens x 128
-// bytes] blocks (128-byte swizzle): the four Lc blocks and the Rc block (whose
-// box runs past column 576 into zero fill).  Both contractions read those bytes
-// as they are, with e4m3 operands and f32 accumulators in TMEM:
+// Every byte of a tile is loaded once, by TMA: the four Lc blocks into a ring of
+// [128 tokens x 128 bytes] slots (128-byte swizzle), the Rc block into a ring of
+// [128 tokens x 64 bytes] slots (64-byte swizzle).  Both contractions read those
+// bytes as they are, with e4m3 operands and f32 accumulators in TMEM:
 //   S[t][h]   = K_t . Q_h      kind::f8f6f4, M = 128 tokens, N = 2N' columns
 //                              (the query's hi terms, then its lo terms: one MMA
 //                              reads the tile once for both), K = 512 (S_L) and 64
@@ -63,7 +63,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int KBLK = TILE * 128;             // 16 KB: [128 tokens x 128 bytes]
+constexpr int KBLK = TILE * 128;             // 16 KB: [128 tokens x 128 bytes] (an Lc block)
+constexpr int RBLK = TILE * 64;              // 8 KB: [128 tokens x 64 bytes] (the Rc block)
 constexpr int W_TMA = 0, W_MMA = 1, W_CTX = 2, W_SOFT = 3;
 constexpr int NSOFT = 8;
 constexpr int NTHREADS = (W_SOFT + NSOFT) * 32;
@@ -93,7 +94,7 @@ struct Cfg {
   // ring slots: the Lc blocks (freed by the context MMAs), the Rc blocks (freed
   // by the score MMAs); a block of tile i reuses a slot of tile i - 3 at the
   // oldest while RL <= 12, which keeps the NTF tile barriers exact
-  static constexpr int RL = N <= 16 ? 9 : 8;
+  static constexpr int RL = N <= 16 ? 10 : 9;
   static constexpr int RR = 2;
   static_assert(RL >= 5 && RL <= 12, "Lc ring size");
   // barriers
@@ -126,7 +127,7 @@ struct Cfg {
   static constexpr int OFF_P = OFF_Q + 5 * NB * 128;       // [2][NB rows x 128 tokens]
   static constexpr int OFF_LRING = align1k(OFF_P + 2 * NB * 128);
   static constexpr int OFF_RRING = OFF_LRING + RL * KBLK;
-  static constexpr int TOTAL = OFF_RRING + RR * KBLK;
+  static constexpr int TOTAL = OFF_RRING + RR * RBLK;
   static constexpr int SMEM = TOTAL + 1024;          // slack for the 1024-byte alignment
   static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + NTF * 4 <= OFF_CS, "barriers and flags");
   static_assert(OFF_CS + N * 4 <= OFF_LS && OFF_LS + 4 * N * 4 <= OFF_RS, "scratch");
@@ -181,7 +182,7 @@ __device__ __forceinline__ void sts8(uint32_t addr, uint32_t v) {
 template <int N>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap smap) {
+                     const __grid_constant__ CUtensorMap rmap, const __grid_constant__ CUtensorMap smap) {
   using C = Cfg<N>;
   constexpr int NB = C::NB, NH = C::NH, RL = C::RL, RR = C::RR;
   constexpr int LOG2_NH = NH == 8 ? 3 : 4;
@@ -306,16 +307,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // the tile's page facts travel with its loads (the arrive releases them;
           // every lane stores the same word, the elected one among them)
           facts[tf] = pack_facts(tr);
-          mbar_arrive_expect_tx_warp(tb, pages * (2u * PAGE * 4u + 5u * PAGE * 128u));
+          mbar_arrive_expect_tx_warp(tb, pages * (2u * PAGE * 4u + 4u * PAGE * 128u + PAGE * 64u));
           n_req = i + 1;
-          const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * KBLK;
+          const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * RBLK;
           if (tr.s0 >= 0) {
             tma_load_1d_warp(sd, &smap, (int)(2 * tr.s0), tb);
-            tma_load_2d_warp(rd, &kmap, DL, (int)tr.s0, tb);
+            tma_load_2d_warp(rd, &rmap, DL, (int)tr.s0, tb);
           }
           if (tr.s1 >= 0) {
             tma_load_1d_warp(sd + 2 * PAGE * 4, &smap, (int)(2 * tr.s1), tb);
-            tma_load_2d_warp(rd + PAGE * 128, &kmap, DL, (int)tr.s1, tb);
+            tma_load_2d_warp(rd + PAGE * 64, &rmap, DL, (int)tr.s1, tb);
           }
         }
         const uint32_t ld = lring + ls * KBLK;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < 4; ++kk) mma_f8_warp(dL, ad + 2 * kk, bd + 2 * kk, idS, (blk | kk) != 0);
       }
       {
-        const uint64_t ad = smem_desc(rring + (i % RR) * KBLK, 16, 1024, SW128);
+        const uint64_t ad = smem_desc(rring + (i % RR) * RBLK, 16, 512, SW64);
         const uint64_t bd = smem_desc(qb + 4 * NB * 128, 16, 1024, SW128);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) mma_f8_warp(dR, ad + 2 * kk, bd + 2 * kk, idS, kk != 0);
@@ -678,15 +679,17 @@ cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
                                 Cfg<N>::SMEM);
   }, &done);
   if (e != cudaSuccess) return e;
-  CUtensorMap kmap, smap;
+  CUtensorMap kmap, rmap, smap;
   e = make_cache_map(a, &kmap);
+  if (e != cudaSuccess) return e;
+  e = make_rc_map(a, &rmap);
   if (e != cudaSuccess) return e;
   e = make_scale_map(a, &smap);
   if (e != cudaSuccess) return e;
   e = launch_prep_query(a, s);
   if (e != cudaSuccess) return e;
   return launch_after_prep(decode_tc_kernel<N>, a.plan.max_items, NTHREADS, Cfg<N>::SMEM, s, a, kmap,
-                           smap);
+                           rmap, smap);
 }
 
 }  // namespace
@@ -731,6 +734,22 @@ cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map) {
   const cuuint32_t box[2] = {128, PAGE};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.codes), dims,
                       strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Tensor map of the cache's Rc bytes (columns 512..575): boxes of 64 rows x 64
+// bytes, 64-byte swizzle, for the one-CTA kernel's 8 KB Rc slots.
+cudaError_t make_rc_map(const DecodeArgs& a, CUtensorMap* map) {
+  const int64_t rows = a.block_table != nullptr ? a.n_blocks * PAGE : a.T_contig;
+  if (rows < 1 || a.codes == nullptr) {
+    memset(map, 0, sizeof(*map));
+    return cudaSuccess;
+  }
+  if (rows >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D};
+  const cuuint32_t box[2] = {64, PAGE};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.codes), dims,
+                      strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // 1-D tensor map of the row scales (f32, two per slot): boxes of 128 floats (one

@@ -102,6 +102,7 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, unsigned ra
                          CUtensorMapSwizzle swizzle);
 cudaError_t make_cache_map(const DecodeArgs& a, CUtensorMap* map);
 cudaError_t make_scale_map(const DecodeArgs& a, CUtensorMap* map);
+cudaError_t make_rc_map(const DecodeArgs& a, CUtensorMap* map);
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t s);

@@ -157,6 +157,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 constexpr uint32_t SW128 = 2;
+constexpr uint32_t SW64 = 4;   // 64-byte swizzle (8-row atoms of 512 bytes)
 
 // Instruction descriptor for kind::f16 with f16 A/B and f32 accumulate.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
