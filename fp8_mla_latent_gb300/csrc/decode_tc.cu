@@ -94,7 +94,7 @@ struct Cfg {
   // ring slots: the Lc blocks (freed by the context MMAs), the Rc blocks (freed
   // by the score MMAs); a block of tile i reuses a slot of tile i - 3 at the
   // oldest while RL <= 12, which keeps the NTF tile barriers exact
-  static constexpr int RL = N <= 16 ? 10 : 9;
+  static constexpr int RL = N <= 16 ? 11 : 9;
   static constexpr int RR = 2;
   static_assert(RL >= 5 && RL <= 12, "Lc ring size");
   // barriers
@@ -115,25 +115,28 @@ struct Cfg {
   static constexpr int TMEM_COLS = 16 * N;
   // shared memory (offsets from the 1024-aligned base)
   static constexpr int OFF_BAR = 0;
-  static constexpr int OFF_FLAGS = 512;              // tmem base, abort flag
-  static constexpr int OFF_FACTS = 528;              // [NTF] page facts of the tiles in flight
-  static constexpr int OFF_CS = 640;                 // [N] c_h
-  static constexpr int OFF_LS = 768;                 // [4][N] denominators per warp
-  static constexpr int OFF_RS = 1280;                // [2][2][4] warp maxima of sLc
-  static constexpr int OFF_RMAX = 2048;              // [2][4][N] warp tile maxima per head
-  static constexpr int OFF_SCR = 3072;               // [NTF][128 tokens][2] f32 row scales
+  static constexpr int OFF_FLAGS = 256;              // tmem base, abort flag
+  static constexpr int OFF_FACTS = 272;              // [NTF] page facts of the tiles in flight
+  static constexpr int OFF_RS = 288;                 // [2][2][4] warp maxima of sLc
+  static constexpr int OFF_CS = 384;                 // [N] c_h
+  static constexpr int OFF_LS = 512;                 // [4][N] denominators per warp
+  static constexpr int OFF_RMAX = 1024;              // [2][4][N] warp tile maxima per head
+  static constexpr int OFF_SCR = 2048;               // [NTF][128 tokens][2] f32 row scales
   static constexpr int OFF_PT = OFF_SCR + NTF * TILE * 8;  // [PT_PAGES] block-table entries
-  static constexpr int OFF_Q = align1k(OFF_PT + PT_PAGES * 4);  // [5 K-blocks][NB rows x 128 B]
-  static constexpr int OFF_P = OFF_Q + 5 * NB * 128;       // [2][NB rows x 128 tokens]
+  // the query: [4 Lc K-blocks][NB rows x 128 B] (128-byte swizzle), then the Rc
+  // K-block [NB rows x 64 B] (64-byte swizzle)
+  static constexpr int OFF_Q = align1k(OFF_PT + PT_PAGES * 4);
+  static constexpr int OFF_P = OFF_Q + 4 * NB * 128 + NB * 64;  // [2][NB rows x 128 tokens]
   static constexpr int OFF_LRING = align1k(OFF_P + 2 * NB * 128);
   static constexpr int OFF_RRING = OFF_LRING + RL * KBLK;
   static constexpr int TOTAL = OFF_RRING + RR * RBLK;
   static constexpr int SMEM = TOTAL + 1024;          // slack for the 1024-byte alignment
-  static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + NTF * 4 <= OFF_CS, "barriers and flags");
-  static_assert(OFF_CS + N * 4 <= OFF_LS && OFF_LS + 4 * N * 4 <= OFF_RS, "scratch");
-  static_assert(OFF_RS + 64 <= OFF_RMAX && OFF_RMAX + 8 * N * 4 <= OFF_SCR, "scratch");
+  static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + NTF * 4 <= OFF_RS, "barriers and flags");
+  static_assert(OFF_RS + 64 <= OFF_CS && OFF_CS + N * 4 <= OFF_LS, "scratch");
+  static_assert(OFF_LS + 4 * N * 4 <= OFF_RMAX && OFF_RMAX + 8 * N * 4 <= OFF_SCR, "scratch");
   static_assert(SMEM <= 232448, "shared memory above the per-CTA limit");
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation");
+  static_assert(OFF_P % 1024 == 0 && (OFF_Q + 4 * NB * 128) % 512 == 0, "operand alignment");
 };
 
 // Transposed warp reduction of NV <= 32 values per lane: afterwards lane holds
@@ -173,6 +176,12 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&v)[NV], int
     }
   }
   return t[0];
+}
+
+// Byte offset of 16-byte unit u (0..3) of row r in a 64-byte-swizzled K-major
+// atom (8 rows of 64 bytes; the unit index turned by bits 1..2 of the row).
+__device__ __forceinline__ uint32_t sw64(int r, int u) {
+  return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((u ^ ((r >> 1) & 3)) << 4));
 }
 
 __device__ __forceinline__ void sts8(uint32_t addr, uint32_t v) {
@@ -250,7 +259,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     grid_dependency_wait();  // the query-prep launch has completed
     // The query of the group's heads in the score MMA's B form: K-block k (Lc
     // channels 128k.., k = 4: Rc) holds NB rows of 128 bytes, row h the hi term of
-    // head h and row N + h its lo term (Rc rows use their first 64 bytes).  Heads
+    // head h and row N + h its lo term (the Rc block has rows of 64 bytes).  Heads
     // past H get zeros and c_h = 0.
     for (int k = threadIdx.x - W_SOFT * 32; k < N * 72; k += NSOFT * 32) {
       const int hh = k / 72, u = k % 72;
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else {
         blk = 4; uu = u - 68; r = N + hh;
       }
-      sts128(qb + blk * NB * 128 + sw128(r, uu), v);
+      sts128(qb + blk * NB * 128 + (blk < 4 ? sw128(r, uu) : sw64(r, uu)), v);
     }
     const int st = threadIdx.x - W_SOFT * 32;
     if (st < N) cs[st] = (h0 + st < a.H) ? __ldg(&a.cq[(int64_t)b * a.H + h0 + st]) : 0.f;
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       {
         const uint64_t ad = smem_desc(rring + (i % RR) * RBLK, 16, 512, SW64);
-        const uint64_t bd = smem_desc(qb + 4 * NB * 128, 16, 1024, SW128);
+        const uint64_t bd = smem_desc(qb + 4 * NB * 128, 16, 512, SW64);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) mma_f8_warp(dR, ad + 2 * kk, bd + 2 * kk, idS, kk != 0);
       }
