@@ -102,7 +102,7 @@ __device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b) {
 // (The item plan is found by a search that counts items for several lengths:
 // from registers, in 32-bit arithmetic, that costs each CTA about a microsecond
 // at the start of a call instead of several.)
-constexpr int SEQ_CACHE = 8;
+constexpr int SEQ_CACHE = 4;
 struct SeqTiles {
   uint32_t t[SEQ_CACHE];
   bool cached;
@@ -156,7 +156,10 @@ __device__ __forceinline__ int64_t count_items(const DecodeArgs& a, const SeqTil
   return (int64_t)warp_sum64(n) * a.plan.n_hg;
 }
 
-// Warp-wide: tiles per item for this call.
+// Warp-wide: tiles per item for this call.  The search evaluates the item count
+// at one probe per pass (lo, then the longest sequence, then bisection), so the
+// count is inlined once: this runs once per CTA, and its code size, not its
+// arithmetic, is what it costs.
 __device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a, const SeqTiles& c) {
   uint64_t total = 0;
   uint32_t tmax = 0;
@@ -174,54 +177,74 @@ __device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a, const SeqTile
   const int64_t jobs = (int64_t)total * a.plan.n_hg;
   int64_t lo = (jobs + a.plan.target - 1) / a.plan.target;
   if (lo < 1) lo = 1;
-  if ((int64_t)tmax <= lo || count_items(a, c, (uint32_t)lo) <= a.plan.target) return lo;
-  if (count_items(a, c, tmax) > a.plan.target) return lo;  // more pairs than one wave holds
-  // invariant: count(lo) > target >= count(hi); the count falls as st grows
-  uint32_t l = (uint32_t)lo, h = tmax;
-  while (l + 1 < h) {
-    const uint32_t mid = l + (h - l) / 2;
-    if (count_items(a, c, mid) <= a.plan.target) h = mid;
-    else l = mid;
+  if ((int64_t)tmax <= lo) return lo;
+  // lo < tmax < 2^31 from here.  Invariant once bisecting: count(l) > target >=
+  // count(h); the count falls as the item length grows.
+  uint32_t l = (uint32_t)lo, h = tmax, probe = l;
+  int pass = 0;
+#pragma unroll 1
+  for (;;) {
+    const bool fits = count_items(a, c, probe) <= a.plan.target;
+    if (pass == 0) {
+      if (fits) return lo;
+      pass = 1;
+      probe = h;
+      continue;
+    }
+    if (pass == 1) {
+      if (!fits) return lo;  // more pairs than one wave holds
+      pass = 2;
+    } else if (fits) {
+      h = probe;
+    } else {
+      l = probe;
+    }
+    if (l + 1 >= h) return h;
+    probe = l + (h - l) / 2;
   }
-  return h;
 }
 
 // Warp-wide: the work item with index k; false if k is past the last item.  The
 // sequences are walked 32 at a time with the inclusive scan of their item counts.
+// Item counts and indices fit 32 bits (the grid holds every item), and so does a
+// sequence's tile count; only token offsets need 64 bits.
 __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it) {
   const int lane = threadIdx.x & 31;
   SeqTiles c;
   load_tiles(a, c);
   const int64_t st = item_tiles(a, c);
-  int64_t base = 0;
+  // st >= 2^31 only when every sequence is one item: ceil(tiles / st) is then 0 or 1
+  const uint32_t st32 = st < (int64_t(1) << 31) ? (uint32_t)st : 0x80000000u;
+  const uint32_t k32 = (uint32_t)k, n_hg = (uint32_t)a.plan.n_hg;
+  uint32_t base = 0;
   for (int kk = 0; 32 * kk < a.B; ++kk) {
     const int b = 32 * kk + lane;
-    const int64_t tiles = tiles_at(a, c, kk);
-    const int64_t ns = (tiles + st - 1) / st;
-    const int64_t cnt = ns * a.plan.n_hg;
-    int64_t inc = cnt;
+    const uint32_t tiles = tiles_at(a, c, kk);
+    const uint32_t ns = tiles / st32 + (tiles % st32 != 0u ? 1u : 0u);
+    const uint32_t cnt = ns * n_hg;
+    uint32_t inc = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int64_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += v;
     }
-    const int64_t first = base + inc - cnt;
-    const bool mine = (b < a.B) && k >= first && k < first + cnt;
+    const uint32_t first = base + inc - cnt;
+    const bool mine = (b < a.B) && k32 >= first && k32 < first + cnt;
     const unsigned m = __ballot_sync(0xffffffffu, mine);
     if (m) {
       const int src = __ffs(m) - 1;
       const int bb = __shfl_sync(0xffffffffu, b, src);
-      const int64_t fb = __shfl_sync(0xffffffffu, first, src);
-      const int64_t nsb = __shfl_sync(0xffffffffu, ns, src);
-      const int64_t r = k - fb;
-      const int64_t s = r % nsb;
+      const uint32_t fb = __shfl_sync(0xffffffffu, first, src);
+      const uint32_t nsb = __shfl_sync(0xffffffffu, ns, src);
+      const uint32_t r = k32 - fb;
+      const uint32_t s = r % nsb;
       it.b = bb;
       it.g = (int)(r / nsb);
-      it.t0 = s * st * TILE;
+      it.t0 = (int64_t)s * st * TILE;
       const int64_t T = seq_len_of(a, bb);
-      const int64_t e = (s + 1) * st * TILE;
+      const int64_t e = (int64_t)(s + 1) * st * TILE;
       it.t1 = e < T ? e : T;
-      it.first = fb + (int64_t)it.g * nsb;
+      it.first = (int64_t)fb + (int64_t)it.g * nsb;
       it.count = nsb;
       return true;
     }
