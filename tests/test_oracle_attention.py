@@ -161,6 +161,49 @@ def test_paged_layout_equals_contiguous():
     np.testing.assert_array_equal(lseb[0], l32)
 
 
+def test_batched_paged_oracle_per_sequence():
+    """Several sequences of different lengths, their pages scattered through one
+    pool: every sequence's output (batch index b > 0 included) equals the plain
+    f32 attention over that sequence's own contiguous rows, and a sequence of
+    length 0 gives out = 0, lse = -inf."""
+    bs = 64
+    lens = [0, 1, 64, 130, 3 * bs + 5]
+    H = 3
+    rng = np.random.default_rng(21)
+    nblk = [(t + bs - 1) // bs for t in lens]
+    maxb = max(nblk)
+    n_pool = sum(nblk) + 4
+    perm = rng.permutation(n_pool)
+    pool_c = np.zeros((n_pool * bs, D), np.uint8)
+    pool_s = np.zeros((n_pool * bs, 2), np.float32)
+    bt = np.full((len(lens), maxb), -1, np.int32)
+    qls, qrs, seqs = [], [], []
+    used = 0
+    for b, T in enumerate(lens):
+        ql, qr, codes, scales = make(T, H, 30 + b)
+        qls.append(ql)
+        qrs.append(qr)
+        seqs.append((codes, scales))
+        for j in range(nblk[b]):
+            phys = int(perm[used])
+            used += 1
+            bt[b, j] = phys
+            n = min(bs, T - j * bs)
+            pool_c[phys * bs: phys * bs + n] = codes[j * bs: j * bs + n]
+            pool_s[phys * bs: phys * bs + n] = scales[j * bs: j * bs + n]
+    bt[bt < 0] = 0  # entries past a sequence's pages are never read
+    out, lse = oracle.attention_batch_f32(np.stack(qls), np.stack(qrs), pool_c, pool_s, bt,
+                                          np.array(lens, np.int32), SM)
+    for b, T in enumerate(lens):
+        codes, scales = seqs[b]
+        if T == 0:
+            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        o32, l32 = oracle.attention_f32(qls[b], qrs[b], codes, scales, T, SM)
+        np.testing.assert_array_equal(out[b], o32)
+        np.testing.assert_array_equal(lse[b], l32)
+
+
 def test_empty_cache():
     ql, qr, codes, scales = make(0, 2, 13)
     out, lse = oracle.attention_f64(ql, qr, codes, scales, 0, SM)
