@@ -107,7 +107,8 @@ struct Cfg {
   static constexpr int B_ODONE = B_PFULL + 2;        // [2] context MMAs of a tile done
   static constexpr int B_G = B_ODONE + 2;            // [2] a softmax group's warps meet (4 arrivals)
   static constexpr int B_DRAIN = B_G + 2;            // [2] the issuers' final drains
-  static constexpr int NBAR = B_DRAIN + 2;
+  static constexpr int B_QREADY = B_DRAIN + 2;       // the next segment's query is in place (8 arrivals)
+  static constexpr int NBAR = B_QREADY + 1;
   // TMEM columns: two S buffers of [S_L hi | S_L lo | S_R hi | S_R lo] (N each),
   // then O: four d-blocks of [hi | lo] (N each)
   static constexpr int S_COLS = 4 * N;
@@ -200,23 +201,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ WorkItem s_it;
-  __shared__ int s_ok;
+  // This CTA's work: one or two segments (a range that runs from one (sequence,
+  // head group) pair into the next), or one per-sequence item.
+  __shared__ Range s_rg;
   if (warp == 0) {
-    WorkItem it;
-    const bool ok = find_item(a, blockIdx.x, it);
-    if (lane == 0 && ok) record_segment(a, blockIdx.x, it);
+    Range rg;
+    if (!find_range(a, blockIdx.x, rg)) {
+      WorkItem it;
+      const bool ok = find_item(a, blockIdx.x, it);
+      rg.n = ok ? 1 : 0;
+      if (ok) {
+        Segment& sg = rg.s[0];
+        sg.b = it.b;
+        sg.g = it.g;
+        sg.t0 = it.t0;
+        sg.t1 = it.t1;
+        sg.sid = blockIdx.x;
+        sg.first = it.first;
+        sg.count = it.count;
+        sg.starts = (int64_t)blockIdx.x == it.first;
+      }
+    }
     if (lane == 0) {
-      s_it = it;
-      s_ok = ok ? 1 : 0;
+      for (int j = 0; j < rg.n; ++j) record_range_segment(a, rg.s[j]);
+      s_rg = rg;
     }
   }
   __syncthreads();
-  if (!s_ok) return;  // past the last work item of this call
-  const int b = s_it.b;
-  const int64_t t0 = s_it.t0, t_end = s_it.t1;
-  const int n_tiles = (int)((t_end - t0 + TILE - 1) / TILE);
-  const int h0 = s_it.g * N;
+  const int nseg = s_rg.n;
+  if (nseg == 0) return;  // past the last work item of this call
+  auto seg_tiles = [&](int j) -> int {
+    return (int)((s_rg.s[j].t1 - s_rg.s[j].t0 + TILE - 1) / TILE);
+  };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_FLAGS);
@@ -235,32 +251,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
 
 
-  // ------------------------------------------------------------ set-up
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NTF; ++i) mbar_init(&bars[C::B_TFULL + i], 1);
-    for (int i = 0; i < RL; ++i) mbar_init(&bars[C::B_LEMPTY + i], 1);
-    for (int i = 0; i < RR; ++i) mbar_init(&bars[C::B_REMPTY + i], 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[C::B_SFULL + i], 1);
-      mbar_init(&bars[C::B_SEMPTY + i], NSOFT);
-      mbar_init(&bars[C::B_PFULL + i], NSOFT);
-      mbar_init(&bars[C::B_ODONE + i], 1);
-      mbar_init(&bars[C::B_G + i], NSOFT / 2);
-      mbar_init(&bars[C::B_DRAIN + i], 1);
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == W_TMA) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-    load_page_table(a, b, t0, t_end, pt, lane);
-  } else if (warp >= W_SOFT) {
-    grid_dependency_wait();  // the query-prep launch has completed
-    // The query of the group's heads in the score MMA's B form: K-block k (Lc
-    // channels 128k.., k = 4: Rc) holds NB rows of 128 bytes, row h the hi term of
-    // head h and row N + h its lo term (the Rc block has rows of 64 bytes).  Heads
-    // past H get zeros and c_h = 0.
+  // The query of segment j's heads in the score MMA's B form, by the softmax
+  // warps: K-block k (Lc channels 128k.., k = 4: Rc) holds NB rows, row h the hi
+  // term of head h and row N + h its lo term (rows of 128 bytes, 128-byte swizzle;
+  // the Rc block rows of 64 bytes, 64-byte swizzle), and c_h.  Heads past H get
+  // zeros and c_h = 0.
+  auto load_query = [&](int j) {
+    const int b = s_rg.s[j].b, h0 = s_rg.s[j].g * N;
     for (int k = threadIdx.x - W_SOFT * 32; k < N * 72; k += NSOFT * 32) {
       const int hh = k / 72, u = k % 72;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -281,6 +278,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int st = threadIdx.x - W_SOFT * 32;
     if (st < N) cs[st] = (h0 + st < a.H) ? __ldg(&a.cq[(int64_t)b * a.H + h0 + st]) : 0.f;
     fence_proxy_async_smem();
+  };
+
+  // ------------------------------------------------------------ set-up
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NTF; ++i) mbar_init(&bars[C::B_TFULL + i], 1);
+    for (int i = 0; i < RL; ++i) mbar_init(&bars[C::B_LEMPTY + i], 1);
+    for (int i = 0; i < RR; ++i) mbar_init(&bars[C::B_REMPTY + i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[C::B_SFULL + i], 1);
+      mbar_init(&bars[C::B_SEMPTY + i], NSOFT);
+      mbar_init(&bars[C::B_PFULL + i], NSOFT);
+      mbar_init(&bars[C::B_ODONE + i], 1);
+      mbar_init(&bars[C::B_G + i], NSOFT / 2);
+      mbar_init(&bars[C::B_DRAIN + i], 1);
+    }
+    mbar_init(&bars[C::B_QREADY], NSOFT);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == W_TMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+    load_page_table(a, s_rg.s[0].b, s_rg.s[0].t0, s_rg.s[0].t1, pt, lane);
+  } else if (warp >= W_SOFT) {
+    grid_dependency_wait();  // the query-prep launch has completed
+    load_query(0);
   }
   tc_fence_before();
   __syncthreads();
@@ -292,45 +315,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Per tile: the row scales (one 128-float box per page), then the Rc block
     // and Lc blocks 0..3, each page a 64-row box; all complete on the tile's
     // barrier, armed once with the tile's bytes.  A block's slot is free once the
-    // MMAs that last read it are done.  The whole warp walks the loop and waits;
-    // one elected lane issues.
+    // MMAs that last read it are done.  Tiles are counted across segments (gi),
+    // for the rings and the barriers' phases.  The whole warp walks the loop and
+    // waits; one elected lane issues.
     bool ok = true;
     int n_req = 0;  // tiles whose barrier has been armed
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
-      const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
-      const int tf = i % NTF, rs = i % RR;
-      uint64_t* tb = &bars[C::B_TFULL + tf];
-      if (!mbar_wait_warp(&bars[C::B_REMPTY + rs], ((i / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
-        ok = false;
-        break;
-      }
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        const int j = 4 * i + blk, ls = j % RL;
-        if (!mbar_wait_warp(&bars[C::B_LEMPTY + ls], ((j / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
+    int gi = 0;
+    for (int j = 0; ok && j < nseg; ++j) {
+      const int b = s_rg.s[j].b;
+      const int64_t t0 = s_rg.s[j].t0, t_end = s_rg.s[j].t1;
+      const int n_tiles = seg_tiles(j);
+      if (j > 0) load_page_table(a, b, t0, t_end, pt, lane);
+      for (int i = 0; i < n_tiles; ++i, ++gi) {
+        const TileRows tr = tile_rows(a, b, t0, t_end, i, pt);
+        const uint32_t pages = (tr.s0 >= 0 ? 1u : 0u) + (tr.s1 >= 0 ? 1u : 0u);
+        const int tf = gi % NTF, rs = gi % RR;
+        uint64_t* tb = &bars[C::B_TFULL + tf];
+        if (!mbar_wait_warp(&bars[C::B_REMPTY + rs], ((gi / RR) & 1) ^ 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
-        if (blk == 0) {
-          // the tile's page facts travel with its loads (the arrive releases them;
-          // every lane stores the same word, the elected one among them)
-          facts[tf] = pack_facts(tr);
-          mbar_arrive_expect_tx_warp(tb, pages * (2u * PAGE * 4u + 4u * PAGE * 128u + PAGE * 64u));
-          n_req = i + 1;
-          const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * RBLK;
-          if (tr.s0 >= 0) {
-            tma_load_1d_warp(sd, &smap, (int)(2 * tr.s0), tb);
-            tma_load_2d_warp(rd, &rmap, DL, (int)tr.s0, tb);
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          const int jb = 4 * gi + blk, ls = jb % RL;
+          if (!mbar_wait_warp(&bars[C::B_LEMPTY + ls], ((jb / RL) & 1) ^ 1, abort_flag, WAIT_NS)) {
+            ok = false;
+            break;
           }
-          if (tr.s1 >= 0) {
-            tma_load_1d_warp(sd + 2 * PAGE * 4, &smap, (int)(2 * tr.s1), tb);
-            tma_load_2d_warp(rd + PAGE * 64, &rmap, DL, (int)tr.s1, tb);
+          if (blk == 0) {
+            // the tile's page facts travel with its loads (the arrive releases them;
+            // every lane stores the same word, the elected one among them)
+            facts[tf] = pack_facts(tr);
+            mbar_arrive_expect_tx_warp(tb, pages * (2u * PAGE * 4u + 4u * PAGE * 128u + PAGE * 64u));
+            n_req = gi + 1;
+            const uint32_t sd = scr + tf * TILE * 8, rd = rring + rs * RBLK;
+            if (tr.s0 >= 0) {
+              tma_load_1d_warp(sd, &smap, (int)(2 * tr.s0), tb);
+              tma_load_2d_warp(rd, &rmap, DL, (int)tr.s0, tb);
+            }
+            if (tr.s1 >= 0) {
+              tma_load_1d_warp(sd + 2 * PAGE * 4, &smap, (int)(2 * tr.s1), tb);
+              tma_load_2d_warp(rd + PAGE * 64, &rmap, DL, (int)tr.s1, tb);
+            }
           }
+          const uint32_t ld = lring + ls * KBLK;
+          if (tr.s0 >= 0) tma_load_2d_warp(ld, &kmap, 128 * blk, (int)tr.s0, tb);
+          if (tr.s1 >= 0) tma_load_2d_warp(ld + PAGE * 128, &kmap, 128 * blk, (int)tr.s1, tb);
         }
-        const uint32_t ld = lring + ls * KBLK;
-        if (tr.s0 >= 0) tma_load_2d_warp(ld, &kmap, 128 * blk, (int)tr.s0, tb);
-        if (tr.s1 >= 0) tma_load_2d_warp(ld + PAGE * 128, &kmap, 128 * blk, (int)tr.s1, tb);
+        if (!ok) break;
       }
     }
     if (!ok) {
@@ -349,8 +381,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // channels per MMA), B = the query's block.  The whole warp walks the loop;
     // one elected lane issues.
     const uint32_t idS = idesc_f16(128, NB, false, false);  // e4m3 x e4m3 (format 0)
+    const int split = seg_tiles(0), n_all = split + (nseg > 1 ? seg_tiles(1) : 0);
     bool ok = true;
-    for (int i = 0; ok && i < n_tiles; ++i) {
+    for (int i = 0; ok && i < n_all; ++i) {  // tiles counted across segments
+      // the second segment's query: the softmax warps load it once they have read
+      // the first segment's last scores
+      if (i == split && !mbar_wait_warp(&bars[C::B_QREADY], 0, abort_flag, WAIT_NS)) {
+        ok = false;
+        break;
+      }
       const int buf = i & 1;
       if (!mbar_wait_warp(&bars[C::B_SEMPTY + buf], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS) ||
           !mbar_wait_warp(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, abort_flag, WAIT_NS)) {
@@ -390,8 +429,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // zeroed first (the score MMAs of the tile are done by then: its P'' follows
     // its S).  The whole warp walks the loop; one elected lane issues.
     const uint32_t idV = idesc_f16(128, NB, true, false);  // e4m3 (format 0), A MN-major
+    const int split = seg_tiles(0), n_all = split + (nseg > 1 ? seg_tiles(1) : 0);
     bool ok = true;
-    for (int i = 0; ok && i < n_tiles; ++i) {
+    for (int i = 0; ok && i < n_all; ++i) {  // tiles counted across segments
+      const bool first = (i == 0 || i == split);  // a segment's first tile starts its O
       const int buf = i & 1;
       if (!mbar_wait_warp(&bars[C::B_PFULL + buf], (i >> 1) & 1, abort_flag, WAIT_NS) ||
           !mbar_wait_warp(&bars[C::B_TFULL + i % NTF], (i / NTF) & 1, abort_flag, WAIT_NS)) {
@@ -418,7 +459,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_f8_warp(tmem + C::T_O + m * NB, smem_desc(vb + kk * 4096, KBLK, 1024, SW128),
-                      smem_desc(bp + kk * 32, 16, 1024, SW128), idV, (i > 0 || kk > 0) ? 1u : 0u);
+                      smem_desc(bp + kk * 32, 16, 1024, SW128), idV, (!first || kk > 0) ? 1u : 0u);
         mma_commit_warp(&bars[C::B_LEMPTY + ls]);
       }
       mma_commit_warp(&bars[C::B_ODONE + buf]);
@@ -444,13 +485,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // constant, the running max in use and the highest one so far.  Per thread:
     // the running denominator of its token rows.
     float c[NH], mu[NH], mhi[NH], lp[NH];
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      c[h] = cs[hb + h];
-      mu[h] = -INFINITY;
-      mhi[h] = -INFINITY;
-      lp[h] = 0.f;
-    }
     float sref = 0.f;
     int gph = 0;
     auto group_sync = [&]() -> bool {
@@ -471,10 +505,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return (uint32_t)((h >> 3) * 1024 + (h & 7) * 128 + (((row >> 4) ^ (h & 7)) << 4) + (row & 15));
     };
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int buf = i & 1, tf = i % NTF;
-      if (!mbar_wait_warp(&bars[C::B_TFULL + tf], (i / NTF) & 1, abort_flag, WAIT_NS) ||
-          !mbar_wait_warp(&bars[C::B_SFULL + buf], (i >> 1) & 1, abort_flag, WAIT_NS)) {
+    int gi = 0;  // tiles counted across segments (rings, buffers, barrier phases)
+    for (int seg = 0; ok && seg < nseg; ++seg) {
+    const int n_tiles = seg_tiles(seg);
+    const int h0 = s_rg.s[seg].g * N;
+    if (seg > 0) {
+      // the next segment's query, once this warp has read the last scores of the
+      // previous one (its score MMAs are all done); the barrier also shows every
+      // softmax warp the new c_h
+      load_query(seg);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_QREADY]);
+      if (!mbar_wait_warp(&bars[C::B_QREADY], 0, abort_flag, WAIT_NS)) {
+        ok = false;
+        break;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      c[h] = cs[hb + h];
+      mu[h] = -INFINITY;
+      mhi[h] = -INFINITY;
+      lp[h] = 0.f;
+    }
+    sref = 0.f;
+    if (seg + 1 < nseg && sw == 0) {
+      // the next segment's prepared query (contiguous in global memory) into L2
+      // now, so that loading it at the switch does not wait on DRAM
+      const Segment& nx = s_rg.s[seg + 1];
+      const int64_t q0 = (int64_t)nx.b * a.H + (int64_t)nx.g * N;
+      const int64_t nq = (a.H - nx.g * N) < N ? (a.H - nx.g * N) : N;
+      prefetch_l2_warp(a.q8 + q0 * Q8_BYTES, (uint32_t)(nq * Q8_BYTES));
+    }
+    for (int i = 0; i < n_tiles; ++i, ++gi) {
+      const int buf = gi & 1, tf = gi % NTF;
+      if (!mbar_wait_warp(&bars[C::B_TFULL + tf], (gi / NTF) & 1, abort_flag, WAIT_NS) ||
+          !mbar_wait_warp(&bars[C::B_SFULL + buf], (gi >> 1) & 1, abort_flag, WAIT_NS)) {
         ok = false;
         break;
       }
@@ -580,7 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (corr) {
         // O columns may change only once the previous tile's context MMAs are done
-        if (!mbar_wait_warp(&bars[C::B_ODONE + (buf ^ 1)], ((i - 1) >> 1) & 1, abort_flag, WAIT_NS)) {
+        if (!mbar_wait_warp(&bars[C::B_ODONE + (buf ^ 1)], ((gi - 1) >> 1) & 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
@@ -609,9 +675,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         tmem_wait_st();
-      } else if (i >= 2) {
-        // the P'' buffer is free once the context MMAs of tile i - 2 are done
-        if (!mbar_wait_warp(&bars[C::B_ODONE + buf], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
+      } else if (gi >= 2) {
+        // the P'' buffer is free once the context MMAs of tile gi - 2 are done
+        if (!mbar_wait_warp(&bars[C::B_ODONE + buf], ((gi >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
           ok = false;
           break;
         }
@@ -627,8 +693,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_PFULL + buf]);
     }
-    if (ok) {
-      ok = mbar_wait_warp(&bars[C::B_ODONE + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1,
+    if (!ok) break;
+    {
+      ok = mbar_wait_warp(&bars[C::B_ODONE + ((gi - 1) & 1)], ((gi - 1) >> 1) & 1,
                           abort_flag, WAIT_NS);
       if (ok) {
         // denominators: the per-thread partials of each head over the 128 rows
@@ -638,7 +705,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        const int64_t base = (int64_t)blockIdx.x * N;  // this item's partials
+        const int64_t base = s_rg.s[seg].sid * N;  // this segment's partials
         if (wq == 0 && lane < NH && h0 + hb + lane < a.H) {
           float m_h = mu[0];
 #pragma unroll
@@ -668,6 +735,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
+    }  // segments
     if (!ok && lane == 0) fail();
   }
 

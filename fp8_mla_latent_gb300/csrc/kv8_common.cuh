@@ -254,6 +254,135 @@ __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkIt
 }
 
 // ---------------------------------------------------------------------------
+// Ranges for the one-CTA tensor-core kernel.  The tiles of all (sequence, head
+// group) pairs, pair after pair, are cut into NC = min(target, total) ranges of
+// equal length (to one tile), one per CTA; a range may run from the end of one
+// pair's tiles into the start of the next.  This is used when every nonempty
+// pair has at least a range's worth of tiles (a range then holds at most two
+// segments) and when the per-sequence items would be longer than a range (64
+// sequences of 64 tiles on 152 SMs: items of 32 tiles against ranges of 27).
+// Segments are numbered in order, so the segments of a pair are consecutive and
+// the merge reads them as it reads items.
+
+struct Segment {
+  int b, g;
+  int64_t t0, t1;        // tokens [t0, t1) of sequence b
+  int64_t sid;           // partial index
+  int64_t first, count;  // the pair's segments (meaningful where starts)
+  bool starts;           // the pair's first segment
+};
+struct Range {
+  int n;                 // segments: 0 (no work), 1 or 2
+  Segment s[2];
+};
+
+// First tile of range k of NC over `total` tiles, and the range holding tile x.
+__device__ __forceinline__ int64_t range_start(int64_t k, int64_t NC, int64_t total) {
+  return k * total / NC;
+}
+__device__ __forceinline__ int64_t range_of(int64_t x, int64_t NC, int64_t total) {
+  return ((x + 1) * NC - 1) / total;
+}
+
+// Warp-wide: whether this call runs on ranges, and if so CTA k's range.  Returns
+// false when the per-sequence items (find_item) apply instead.
+__device__ __forceinline__ bool find_range(const DecodeArgs& a, int64_t k, Range& r) {
+  const int lane = threadIdx.x & 31;
+  SeqTiles c;
+  load_tiles(a, c);
+  const int n_hg = a.plan.n_hg;
+  uint64_t total = 0;
+  uint32_t tmin = 0xFFFFFFFFu;
+  for (int kk = 0; 32 * kk < a.B; ++kk) {
+    const uint32_t t = tiles_at(a, c, kk);
+    total += t;
+    if (t > 0u && t < tmin) tmin = t;
+  }
+  total = warp_sum64(total) * (uint64_t)n_hg;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t m = __shfl_xor_sync(0xffffffffu, tmin, o);
+    tmin = m < tmin ? m : tmin;
+  }
+  if (total == 0) return false;
+  const int64_t NC = (int64_t)total < a.plan.target ? (int64_t)total : a.plan.target;
+  const int64_t L = ((int64_t)total + NC - 1) / NC;
+  // the per-sequence items' length exceeds L exactly when items of L tiles do not
+  // fit in one wave (the count falls as the length grows, and L >= the lower
+  // bound of that search)
+  if ((int64_t)tmin < L || count_items(a, c, (uint32_t)L) <= a.plan.target) return false;
+  r.n = 0;
+  if (k >= NC) return true;  // no range for this CTA
+  const int64_t T0 = range_start(k, NC, total), T1 = range_start(k + 1, NC, total);
+  // Walk the pairs in order: the pair holding T0 (segment 0), the next one if
+  // the range reaches it (segment 1), and the pair starts before T0 that do not
+  // fall on a range start (each adds a segment to the numbering).
+  int64_t base = 0, extra = 0;
+  int found = 0;
+  for (int kk = 0; 32 * kk < a.B; ++kk) {
+    const int b = 32 * kk + lane;
+    const int64_t tl = tiles_at(a, c, kk);
+    const int64_t len = tl * n_hg;
+    int64_t inc = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const int64_t sb = base + inc - len;  // first tile of sequence b's pairs
+    int cnt = 0;
+    for (int g = 0; g < n_hg && tl > 0; ++g) {
+      const int64_t st = sb + g * tl;
+      if (st > 0 && st < T0 && range_start(range_of(st, NC, total), NC, total) != st) ++cnt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    extra += cnt;
+    // the sequences holding T0 and T1 - 1
+    for (int want = found; want < 2; ++want) {
+      const int64_t x = want == 0 ? T0 : T1 - 1;
+      const bool mine = (b < a.B) && tl > 0 && x >= sb && x < sb + len;
+      const unsigned m = __ballot_sync(0xffffffffu, mine);
+      if (!m) break;
+      const int src = __ffs(m) - 1;
+      const int bb = __shfl_sync(0xffffffffu, b, src);
+      const int64_t sbb = __shfl_sync(0xffffffffu, sb, src), tlb = __shfl_sync(0xffffffffu, tl, src);
+      const int g = (int)((x - sbb) / tlb);
+      const int64_t ps = sbb + g * tlb, pe = ps + tlb;  // the pair's tiles [ps, pe)
+      Segment& sg = r.s[want];
+      sg.b = bb;
+      sg.g = g;
+      const int64_t lo = (want == 0 ? T0 : ps) - ps;
+      const int64_t hi = (T1 < pe ? T1 : pe) - ps;
+      const int64_t T = seq_len_of(a, bb);
+      sg.t0 = lo * TILE;
+      sg.t1 = hi * TILE < T ? hi * TILE : T;
+      sg.starts = (lo == 0);
+      sg.first = 0;  // set below, with the numbering
+      sg.count = range_of(pe - 1, NC, total) - range_of(ps, NC, total) + 1;
+      found = want + 1;
+    }
+    base += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  // segment 1 exists when the range ends in another pair than it starts in
+  r.n = (found == 2 && (r.s[1].b != r.s[0].b || r.s[1].g != r.s[0].g)) ? 2 : 1;
+  r.s[0].sid = k + extra;
+  r.s[1].sid = k + extra + 1;
+  r.s[0].first = r.s[0].sid;
+  r.s[1].first = r.s[1].sid;
+  return true;
+}
+
+// The CTA holding a pair's first segment records the pair's segments for the merge.
+__device__ __forceinline__ void record_range_segment(const DecodeArgs& a, const Segment& s) {
+  if (s.starts) {
+    int64_t* e = a.seg + ((int64_t)s.b * a.plan.n_hg + s.g) * 2;
+    e[0] = s.first;
+    e[1] = s.count;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Pages of a work item, for the tensor-core kernels: the item's block-table
 // entries are read once into shared memory, and every tile's two pages become
 // cache slots (or -1) from there.

@@ -186,6 +186,44 @@ def test_split_phases_equal_the_fused_call(variant):
     assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("B,T,H", [(100, 640, 16), (100, 600, 16), (50, 1000, 64)])
+def test_ranges_across_sequences(B, T, H):
+    """Shapes where the one-CTA kernel cuts the tiles of all sequences into equal
+    ranges (a range runs from one sequence into the next): every sequence, on both
+    sides of each range boundary, against the oracle; and the automatic choice
+    gives the forced kernel's bits."""
+    if not tc_ready():
+        pytest.skip("tensor-core decode not built in this library")
+    rng = np.random.default_rng(B + T + H)
+    w = workloads.make("batched", scale=0.01, seed=5)
+    w.B, w.H = B, H
+    nb = (T + 63) // 64
+    w.seq_lens = np.full(B, T, np.int32)
+    w.n_slots = B * nb * 64
+    perm = rng.permutation(B * nb).astype(np.int32)
+    w.block_table = perm.reshape(B, nb)
+    rows = []
+    slots = []
+    for b in range(B):
+        x = rng.standard_normal((T, 576)).astype(np.float32)
+        rows.append(x)
+        pages = w.block_table[b]
+        slots.append(pages[np.arange(T) // 64].astype(np.int64) * 64 + np.arange(T) % 64)
+    w.cache_rows = np.concatenate(rows)
+    w.cache_slots = np.concatenate(slots)
+    w.fresh_rows = None
+    w.q_lat = rng.standard_normal((B, H, 512)).astype(np.float32)
+    w.q_rope = rng.standard_normal((B, H, 64)).astype(np.float32)
+    codes, scales = upload_cache(w)
+    out, lse = decode(w, codes, scales, pkg.KV8_DECODE_TCGEN05_CTA)
+    c, s_ = codes.cpu().numpy(), scales.cpu().numpy()
+    bs = sorted(set([0, 1, B // 2, B - 2, B - 1] + list(rng.choice(B, size=6, replace=False))))
+    check(w, out, lse, c, s_, [(int(b), (0, H)) for b in bs], pkg.KV8_DECODE_TCGEN05_CTA)
+    out_a, lse_a = decode(w, codes, scales, pkg.KV8_DECODE_TCGEN05)
+    assert np.array_equal(out_a.view(np.uint32), out.view(np.uint32))
+    assert np.array_equal(lse_a.view(np.uint32), lse.view(np.uint32))
+
+
 FULL = ["single", "long", "batched", "append"]
 
 
