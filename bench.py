@@ -5,7 +5,7 @@ By default one line per decode workload: tiny, single, batched, append, then the
 headline, long: B=2 sequences x T=262144 cached tokens, H=128 heads, kv_lora 512 +
 qk_rope 64 stored as e4m3 + two f32 scales per row (584 B/token, 306 MB of KV per
 step, over twice L2, so no flush is needed between steps; workloads under twice
-L2 are flushed by a 256 MB write).  One step = one decode query per sequence over
+L2 are flushed by writing and then reading 256 MB).  One step = one decode query per sequence over
 its whole cache (the "append" workload also quantizes 65536 fresh rows into the
 cache inside the step).
 
@@ -66,7 +66,8 @@ KERNEL_SOURCES = {
     "decode_pair": ["fp8_mla_latent_gb300/csrc/decode_pair.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh",
                     "fp8_mla_latent_gb300/csrc/tc_ptx.cuh"],
     "produce_rows": ["fp8_mla_latent_gb300/csrc/quantize.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
-    "wuv": ["fp8_mla_latent_gb300/csrc/wuv.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
+    "wuv": ["fp8_mla_latent_gb300/csrc/wuv.cu", "fp8_mla_latent_gb300/csrc/kv8_common.cuh",
+            "fp8_mla_latent_gb300/csrc/tc_ptx.cuh"],
     "prefill": ["fp8_mla_latent_gb300/csrc/prefill.cu", "fp8_mla_latent_gb300/csrc/tc_ptx.cuh",
                 "fp8_mla_latent_gb300/csrc/kv8_common.cuh"],
     "decode_simt": ["fp8_mla_latent_gb300/csrc/decode_simt.cu",
@@ -86,6 +87,13 @@ def traffic_for(kernel, workload):
     if not d or d.get("source_sha") != source_hash(KERNEL_SOURCES[kernel]):
         return None
     return float(d["bytes_per_launch"])
+
+
+def flush_l2(buf):
+    """Evict L2: write a buffer larger than L2, then read it back, so that the lines
+    left in L2 are clean and the timed kernel's loads write nothing back."""
+    buf.zero_()
+    buf.amax()
 
 
 def rank_sync():
@@ -278,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
     t_wall = time.perf_counter()
     for k in range(args.steps):
         if do_flush:
-            flush.zero_()  # evict L2 between timed steps (outside the step's events)
+            flush_l2(flush)  # evict L2 between timed steps (outside the step's events)
         step(evs[k])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -320,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
                for _ in range(args.steps)]
     for k in range(args.steps):
         if do_flush:
-            flush.zero_()
+            flush_l2(flush)
         e2e_evs[k][0].record(stream)
         e2e_step()
         e2e_evs[k][1].record(stream)
@@ -382,7 +390,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "scale": args.scale, "B": w.B, "H": w.H,
                    "T_total": w.total_tokens, "kv_lora": 512, "qk_rope": 64,
                    "variant": {1: "simt", 3: "tcgen05_cta", 4: "tcgen05_pair"}[plan_variant],
-                   "l2": ("flushed between steps (256 MB write)" if do_flush else
+                   "l2": ("flushed between steps (256 MB written, then read)" if do_flush else
                           f"no flush: the step's inputs ({in_bytes / 1e6:.0f} MB) are over twice "
                           "L2 (129 MB)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
@@ -444,7 +452,7 @@ def run_produce(args, rank, world, local_rank):
                              err_word=err)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         once()
     torch.cuda.synchronize()
     rank_sync()
@@ -452,7 +460,7 @@ def run_produce(args, rank, world, local_rank):
     sampler.start()
     times = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         once()
@@ -469,7 +477,7 @@ def run_produce(args, rank, world, local_rank):
     host_err = torch.zeros(1, dtype=torch.int32).pin_memory()
     e2e = []
     for k in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2(flush)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -490,7 +498,7 @@ def run_produce(args, rank, world, local_rank):
         "data": "synthetic (seeded; the append workload's value mix)",
         "rows_per_s": world * n / (ms * 1e-3),
         "config": {"workload": "produce", "rows": n, "max_pos": int(p.rope_cos.shape[0]),
-                   "l2": "flushed between steps (256 MB write); rows > L2",
+                   "l2": "flushed between steps (256 MB written, then read); rows > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
@@ -525,13 +533,13 @@ def run_wuv(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         pkg.mla_wuv_epilogue(o, w, y)
     torch.cuda.synchronize()
     rank_sync()
     times = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         pkg.mla_wuv_epilogue(o, w, y)
@@ -548,7 +556,7 @@ def run_wuv(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 accum",
         "data": "synthetic (seeded)",
-        "config": {"workload": "wuv", "B": B, "H": H, "V": V, "l2": "flushed between steps"},
+        "config": {"workload": "wuv", "B": B, "H": H, "V": V, "l2": "flushed between steps (256 MB written, then read)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for("wuv", "wuv"),
                      "kernel": "wuv",
@@ -595,7 +603,7 @@ def run_prefill(args, rank, world, local_rank):
         pkg.kv8_prefill_project(codes, scales, w, slots=slots, y=y, k_rope=k_rope, err_word=err)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         once()
     torch.cuda.synchronize()
     rank_sync()
@@ -603,7 +611,7 @@ def run_prefill(args, rank, world, local_rank):
     sampler.start()
     times = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         once()
@@ -625,7 +633,7 @@ def run_prefill(args, rank, world, local_rank):
     h_k = torch.empty((T, 64), dtype=torch.float32).pin_memory()
     e2e = []
     for k in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2(flush)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -649,7 +657,7 @@ def run_prefill(args, rank, world, local_rank):
         "data": "synthetic (seeded; Gaussian rows with log-normal channel gains, N(0,1/512) weights)",
         "tokens_per_s": world * T / (ms * 1e-3),
         "config": {"workload": "prefill", "T": T, "N": N, "heads": 128, "qk_nope": 128, "v_head": 128,
-                   "l2": "flushed between steps (256 MB write)",
+                   "l2": "flushed between steps (256 MB written, then read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],

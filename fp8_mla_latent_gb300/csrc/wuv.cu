@@ -8,15 +8,14 @@
 //
 // Decode has one query row per sequence, so the work is B x H dot products of
 // length 512 per output column: the weight stream (H x 512 x V bf16, 16 MB at
-// H = V = 128) bounds it, not arithmetic.  One CTA per (head, 128 output
-// columns), the sequences' context rows in shared memory.  When V is a multiple
-// of 8 (and the weights 16-byte aligned), thread (r, g) of 512 owns columns
-// 8g..8g+7 and the latent rows d = r, r+32, ...: one 16-byte load brings 8
-// weights, all sixteen rows' loads in flight; the 32 row groups are then added in a
-// fixed order through shared memory.  Otherwise thread (k, v) sums half k of the
-// latent rows for column v with 2-byte loads.  The bf16 -> f32 conversion is
-// exact.
+// H = V = 128) bounds it, not arithmetic.  When V is a multiple of 8 (and the
+// weights 16-byte aligned) the bulk path below streams the weights into shared
+// memory on clusters of four CTAs per (head, 128 output columns).  Otherwise one
+// CTA per (head, 128 output columns), the sequences' context rows in shared
+// memory, and thread (k, v) sums half k of the latent rows for column v with
+// 2-byte loads.  The bf16 -> f32 conversion is exact.
 #include "kv8_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace kv8 {
 namespace {
@@ -67,43 +66,98 @@ __global__ void __launch_bounds__(WT) wuv_kernel(const float* __restrict__ o,
   }
 }
 
-constexpr int VB = 4;     // sequences per pass of the vector path
-constexpr int VT = 512;   // threads of the vector path: 32 latent row groups x 16 column groups
-constexpr int VR = VT / 16;
-constexpr int V8_SMEM = (VB * DL + VR * VB * 128) * 4;  // context rows + partial sums
+// The bulk path (V a multiple of 8, weights 16-byte aligned).  A cluster of
+// SPLIT CTAs takes one (head, block of 128 output columns); CTA q of the cluster
+// holds latent rows [128 q, 128 q + 128).  Its weights (at most 32 KB) come in by
+// bulk copies into shared memory, in four chunks of 32 rows with a barrier each,
+// all in flight at once: a plain-load stream from a few SMs cannot keep enough
+// bytes in flight to fill HBM.  Thread (r, g) of 256 owns columns 8g..8g+7 and
+// rows 8r..8r+7 of the CTA's quarter; the partial sums are added in a fixed order:
+// the two row groups of a warp (a shuffle), then the warps in order, then the
+// cluster's CTAs in rank order (read from their shared memory).
+constexpr int SPLIT = 4;                // CTAs of a cluster, latent rows each: DL / SPLIT
+constexpr int QR = DL / SPLIT;          // 128 latent rows per CTA
+constexpr int BT = 256;                 // threads: 16 row groups x 16 column groups
+constexpr int BCH = 2;                  // sequences per pass
+constexpr int NCHUNK = 4;               // weight chunks (barriers) of QR / NCHUNK rows
+constexpr uint64_t WUV_WAIT_NS = 2000000000ull;
+constexpr int OFF_W = 0;                                  // [QR][pitch] bf16, pitch <= 256 B
+constexpr int OFF_O = OFF_W + QR * 256;                   // [BCH][QR] f32 contexts
+constexpr int OFF_PART = OFF_O + BCH * QR * 4;            // [BT / 32][BCH][128] f32
+constexpr int OFF_Y = OFF_PART + (BT / 32) * BCH * 128 * 4;  // [BCH][128] f32, this CTA's sums
+constexpr int OFF_BAR = OFF_Y + BCH * 128 * 4;
+constexpr int BULK_SMEM = OFF_BAR + NCHUNK * 8 + 8;
+static_assert(OFF_BAR % 8 == 0 && OFF_O % 16 == 0, "shared-memory layout");
 
-__global__ void __launch_bounds__(VT) wuv8_kernel(const float* __restrict__ o,
-                                                  const uint16_t* __restrict__ w, int B, int H,
-                                                  int V, float* __restrict__ y) {
-  const int h = blockIdx.x;
-  const int g = threadIdx.x & 15, r = threadIdx.x >> 4;  // column group, latent row group
-  const int v0 = blockIdx.y * 128 + g * 8;
-  extern __shared__ float wsm[];
-  float (*osh)[DL] = reinterpret_cast<float (*)[DL]>(wsm);
-  float (*part)[VB][128] = reinterpret_cast<float (*)[VB][128]>(wsm + VB * DL);
-  const uint16_t* wh = w + (int64_t)h * DL * V;
-  for (int b0 = 0; b0 < B; b0 += VB) {
-    const int nb = (B - b0) < VB ? (B - b0) : VB;
-    for (int i = threadIdx.x; i < nb * DL; i += VT) {
-      const int bb = i / DL, d = i % DL;
-      osh[bb][d] = o[((int64_t)(b0 + bb) * H + h) * DL + d];
+__global__ void __cluster_dims__(SPLIT, 1, 1) __launch_bounds__(BT, 4)
+    wuv_bulk_kernel(const float* __restrict__ o, const uint16_t* __restrict__ w, int B, int H,
+                    int V, float* __restrict__ y) {
+  extern __shared__ __align__(128) uint8_t wsm[];
+  const int h = blockIdx.x / SPLIT;
+  const uint32_t q = ptx::cluster_rank();
+  const int v0 = blockIdx.y * 128;
+  const int ncol = (V - v0) < 128 ? (V - v0) : 128;  // a multiple of 8
+  const uint32_t pitch = (uint32_t)ncol * 2u;          // bytes per weight row in shared memory
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane & 15, r = (warp << 1) | (lane >> 4);  // column group, row group
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + OFF_BAR);
+  volatile int* bad = reinterpret_cast<volatile int*>(wsm + OFF_BAR + NCHUNK * 8);
+  float* osh = reinterpret_cast<float*>(wsm + OFF_O);
+  float* part = reinterpret_cast<float*>(wsm + OFF_PART);
+  float* ycta = reinterpret_cast<float*>(wsm + OFF_Y);
+  const uint32_t wbase = ptx::smem_u32(wsm + OFF_W);
+  const uint16_t* wq = w + ((int64_t)h * DL + q * QR) * V + v0;
+
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < NCHUNK; ++c) ptx::mbar_init(&bars[c], 1);
+    bad[0] = 0;
+    bad[1] = 0;  // never set: the abort flag of the final wait
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // chunk c = rows [32 c, 32 c + 32): one copy when the rows are contiguous in
+    // global memory (ncol == V), else one per row, lane l taking row 32 c + l
+    constexpr int CR = QR / NCHUNK;
+    if (lane == 0)
+      for (int c = 0; c < NCHUNK; ++c) ptx::mbar_arrive_expect_tx(&bars[c], CR * pitch);
+    __syncwarp();
+    for (int c = 0; c < NCHUNK; ++c) {
+      if (ncol == V) {
+        if (lane == 0)
+          ptx::bulk_load_g2s(wbase + c * CR * pitch, wq + (int64_t)c * CR * V, CR * pitch, &bars[c]);
+      } else {
+        const int row = c * CR + lane;
+        ptx::bulk_load_g2s(wbase + row * pitch, wq + (int64_t)row * V, pitch, &bars[c]);
+      }
+    }
+  }
+  // this warp's rows 8r..8r+7 lie in chunk r / 4 (= warp / 2)
+  const int chunk = warp >> 1;
+  bool ready = false;
+  const bool active = g * 8 < ncol;
+  for (int b0 = 0; b0 < B; b0 += BCH) {
+    const int nb = (B - b0) < BCH ? (B - b0) : BCH;
+    for (int i = threadIdx.x; i < BCH * QR; i += BT) {
+      const int k = i / QR, d = i % QR;
+      osh[i] = k < nb ? __ldg(o + ((int64_t)(b0 + k) * H + h) * DL + q * QR + d) : 0.f;
     }
     __syncthreads();
-    float acc[VB][8];
+    if (!ready) {
+      ready = true;
+      if (!ptx::mbar_wait(&bars[chunk], 0, bad, WUV_WAIT_NS)) *bad = 1;
+    }
+    float acc[BCH][8];
 #pragma unroll
-    for (int k = 0; k < VB; ++k)
+    for (int k = 0; k < BCH; ++k)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[k][j] = 0.f;
-    if (v0 < V) {
-      // all DL / VR = 16 of this thread's weight rows in flight at once
-      uint4 q[DL / VR];
+    if (active) {
 #pragma unroll
-      for (int i = 0; i < DL / VR; ++i)
-        q[i] = __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)(r + i * VR) * V + v0));
-#pragma unroll
-      for (int i = 0; i < DL / VR; ++i) {
-        const int d = r + i * VR;
-        const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+      for (int i = 0; i < 8; ++i) {
+        const int d = r * 8 + i;
+        const uint4 u4 = lds128(wbase + d * pitch + g * 16);
+        const uint32_t u[4] = {u4.x, u4.y, u4.z, u4.w};
         float wf[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -111,30 +165,47 @@ __global__ void __launch_bounds__(VT) wuv8_kernel(const float* __restrict__ o,
           wf[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
         }
 #pragma unroll
-        for (int k = 0; k < VB; ++k) {
-          if (k < nb) {
-            const float ob = osh[k][d];
+        for (int k = 0; k < BCH; ++k) {
+          const float ob = osh[k * QR + d];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(ob, wf[j], acc[k][j]);
-          }
+          for (int j = 0; j < 8; ++j) acc[k][j] = fmaf(ob, wf[j], acc[k][j]);
         }
       }
     }
+    // row groups 2w and 2w + 1, then the warps in order
 #pragma unroll
-    for (int k = 0; k < VB; ++k)
+    for (int k = 0; k < BCH; ++k)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part[r][k][g * 8 + j] = acc[k][j];
-    __syncthreads();
-    // thread t < nb * 128: column t % 128 of sequence t / 128, row groups in order
-    for (int t = threadIdx.x; t < nb * 128; t += VT) {
-      const int k = t >> 7, c = t & 127;
-      const int v = blockIdx.y * 128 + c;
-      float sum = part[0][k][c];
+      for (int j = 0; j < 8; ++j) acc[k][j] += __shfl_xor_sync(0xffffffffu, acc[k][j], 16);
+    if (lane < 16) {
 #pragma unroll
-      for (int rr = 1; rr < VR; ++rr) sum += part[rr][k][c];
-      if (v < V) y[((int64_t)(b0 + k) * H + h) * V + v] = sum;
+      for (int k = 0; k < BCH; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[(warp * BCH + k) * 128 + g * 8 + j] = acc[k][j];
     }
     __syncthreads();
+    for (int t = threadIdx.x; t < BCH * 128; t += BT) {
+      float sum = part[t];
+#pragma unroll
+      for (int ww = 1; ww < BT / 32; ++ww) sum += part[ww * BCH * 128 + t];
+      ycta[t] = *bad ? __int_as_float(0x7fc00000) : sum;
+    }
+    ptx::cluster_sync();  // every CTA's sums are in its shared memory
+    // CTA q writes columns [32 q, 32 q + 32) of each sequence: the SPLIT sums in rank order
+    if (threadIdx.x < BCH * 32) {
+      const int k = threadIdx.x >> 5, c = (int)q * 32 + (threadIdx.x & 31);
+      const uint32_t src = ptx::smem_u32(ycta + k * 128 + c);
+      float sum = ptx::ld_cluster_f32(ptx::map_to(src, 0));
+#pragma unroll
+      for (int rr = 1; rr < SPLIT; ++rr) sum += ptx::ld_cluster_f32(ptx::map_to(src, rr));
+      if (k < nb && c < ncol) y[((int64_t)(b0 + k) * H + h) * V + v0 + c] = sum;
+    }
+    ptx::cluster_sync();  // the sums have been read before they are overwritten or freed
+  }
+  // the copies are complete before the CTA leaves (a copy that has not landed by
+  // the first wait's limit gets one more bounded wait)
+  if (warp == 0 && *bad) {
+    for (int c = 0; c < NCHUNK; ++c) ptx::mbar_wait(&bars[c], 0, bad + 1, WUV_WAIT_NS);
   }
 }
 
@@ -149,10 +220,11 @@ cudaError_t launch_wuv(const float* o, const uint16_t* w, int B, int H, int V, f
     int done = 0;
     const cudaError_t e = per_device(memo, [](int* v) {
       *v = 1;
-      return cudaFuncSetAttribute(wuv8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, V8_SMEM);
+      return cudaFuncSetAttribute(wuv_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  BULK_SMEM);
     }, &done);
     if (e != cudaSuccess) return e;
-    wuv8_kernel<<<grid, VT, V8_SMEM, s>>>(o, w, B, H, V, y);
+    wuv_bulk_kernel<<<dim3(H * SPLIT, (V + 127) / 128), BT, BULK_SMEM, s>>>(o, w, B, H, V, y);
   }
   else
     wuv_kernel<<<grid, WT, 0, s>>>(o, w, B, H, V, y);

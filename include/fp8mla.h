@@ -156,7 +156,8 @@ int kv8_produce_rows(const float* src, int64_t n_rows, int64_t src_row_stride,
  *   B, H, V  B >= 0, 1 <= H <= 1024, 1 <= V <= 4096.
  *   y        device f32 [B][H][V].
  * Tolerance: f32 sums of 512 products in a fixed order (partial sums over
- * interleaved latent rows, then added in row-group order):
+ * groups of latent rows, then added in a fixed order of groups), the same bits on
+ * every call:
  * max-abs error <= 1e-5 * max|y| against float64.
  * Errors: KV8_EINVAL, KV8_EALIGN, KV8_ECUDA.
  * ------------------------------------------------------------------------- */

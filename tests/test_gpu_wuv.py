@@ -21,7 +21,8 @@ def bf16_weights(rng, H, V):
 
 
 @pytest.mark.parametrize("B,H,V", [(1, 1, 1), (2, 128, 128), (3, 16, 128), (32, 128, 128),
-                                   (17, 7, 200), (64, 128, 64), (5, 3, 513)])
+                                   (17, 7, 200), (64, 128, 64), (5, 3, 513), (3, 2, 8),
+                                   (33, 4, 4096), (1, 1024, 16)])
 def test_wuv_matches_oracle(B, H, V):
     rng = np.random.default_rng(B * 1000 + H * 10 + V)
     d = torch.device("cuda:0")
@@ -48,3 +49,15 @@ def test_wuv_after_decode_output():
     torch.cuda.synchronize()
     ref = oracle.wuv_project(out, wt.view(torch.int16).numpy().view(np.uint16))
     assert np.abs(y.cpu().numpy() - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_wuv_deterministic():
+    """A fixed summation order: two calls give the same bits."""
+    rng = np.random.default_rng(5)
+    d = torch.device("cuda:0")
+    o = torch.from_numpy(rng.standard_normal((9, 64, 512)).astype(np.float32)).to(d)
+    w = bf16_weights(rng, 64, 136).to(d)
+    y1 = pkg.mla_wuv_epilogue(o, w)
+    y2 = pkg.mla_wuv_epilogue(o, w)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
