@@ -129,6 +129,7 @@ constexpr int TOTAL_S = OFF_STG + P_BYTES;
 constexpr int OFF_P = 4096;                  // context: 2 payloads / context operands
 constexpr int OFF_VRING = OFF_P + 2 * P_STRIDE;
 constexpr int TOTAL_C = OFF_VRING + NVT * VTILE;
+constexpr int O_ROW = 64 * 4 + 16;           // context epilogue: one head's 64 columns, padded
 constexpr int OFF_PT = TOTAL_S > TOTAL_C ? TOTAL_S : TOTAL_C;  // both CTAs: [PT_PAGES] int32
 constexpr int SMEM = OFF_PT + PT_PAGES * 4 + 1024;
 // score CTA TMEM columns: S_L, S_R (one tile), then the Lc query's hi and lo terms
@@ -139,7 +140,7 @@ static_assert(NBAR * 8 <= OFF_FLAGS && OFF_FACTS + 16 <= OFF_XMAX, "barriers, fl
 static_assert(P_BYTES <= P_STRIDE && (P_STRIDE % 1024) == 0 && (OFF_VRING % 1024) == 0,
               "payload layout");
 static_assert(2 * KBLK <= P_BYTES, "the context operand (hi and lo atoms) fits in its payload buffer");
-static_assert(N_LANE_WARPS * 32 * 33 * 4 <= 2 * P_STRIDE, "the epilogue's staging fits in the payload buffers");
+static_assert(OFF_P + N_LANE_WARPS * 32 * O_ROW <= TOTAL_C, "the epilogue's staging fits in the payloads and V ring");
 static_assert((CHUNK % 16) == 0 && (OFF_STG % 16) == 0, "bulk-copied chunks");
 static_assert(SMEM <= 232448, "shared memory above the per-CTA limit");
 
@@ -813,32 +814,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
       if (ok) {
         // epilogue: the partial's unnormalised o = acc * s_ref / P_TOP.  A thread's
-        // TMEM lane is one head, so each warp turns its 32 heads x 32 columns
-        // around in shared memory (the payload buffers, free now; rows padded to 33
-        // floats, no bank conflicts either way) and stores one head's 32 columns
-        // per instruction: 128 contiguous bytes instead of 32 rows 2 KB apart.
+        // TMEM lane is one head: it puts its head's 64 columns of an O half in a
+        // shared-memory row (the payload buffers and V ring, free now; rows 272
+        // bytes apart, so a quarter warp's 16-byte stores fall on distinct banks) and
+        // sends the row to the workspace with one 256-byte bulk copy.
         tc_fence_after();
         __syncwarp();
         const float oscale = sref_fin * (1.0f / P_TOP);
-        float* stage = reinterpret_cast<float*>(sm + OFF_P) + (warp - W_LANE) * (32 * 33);
-        float* dst = a.ws_o + (item * HG + q * 32) * DL;
+        const uint32_t stage = smem_u32(sm + OFF_P) + (uint32_t)(warp - W_LANE) * (32 * O_ROW);
+        const bool real = h0 + q * 32 + lane < a.H;
+        float* dst = a.ws_o + (item * HG + q * 32 + lane) * DL;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           const int cbase = half * 256 + part * 64;
+          if (half > 0) {
+            bulk_wait_read_all();  // this lane's row of the first half has been read
+            __syncwarp();
+          }
 #pragma unroll 1
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r[32];
-            __syncwarp();
             tmem_ld32(tmem + lane_addr + cbase + c0, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = __uint_as_float(r[k]) * oscale;
-            __syncwarp();
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j)
-              if (h0 + q * 32 + j < a.H) dst[(int64_t)j * DL + cbase + c0 + lane] = stage[j * 33 + lane];
+            for (int k = 0; k < 32; k += 4)
+              sts128(stage + lane * O_ROW + (c0 + k) * 4,
+                     make_uint4(__float_as_uint(__uint_as_float(r[k]) * oscale),
+                                __float_as_uint(__uint_as_float(r[k + 1]) * oscale),
+                                __float_as_uint(__uint_as_float(r[k + 2]) * oscale),
+                                __float_as_uint(__uint_as_float(r[k + 3]) * oscale)));
+          }
+          fence_proxy_async_smem();
+          if (real) {
+            bulk_store_s2g(dst + cbase, stage + lane * O_ROW, 64 * 4);
+            bulk_commit();
           }
         }
+        bulk_wait_all();  // the rows have landed before the CTA leaves
       } else {
         fail();
       }

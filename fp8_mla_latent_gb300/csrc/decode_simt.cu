@@ -29,10 +29,12 @@ decode_simt_kernel(DecodeArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ WorkItem s_it;
   __shared__ int s_ok;
+  __shared__ int32_t pt[PT_PAGES];  // the item's block-table entries
   if (warp == 0) {
     WorkItem it;
     const bool ok = find_item(a, blockIdx.x, it);
     if (lane == 0 && ok) record_segment(a, blockIdx.x, it);
+    if (ok) load_page_table(a, it.b, it.t0, it.t1, pt, lane);
     if (lane == 0) {
       s_it = it;
       s_ok = ok ? 1 : 0;
@@ -87,18 +89,24 @@ decode_simt_kernel(DecodeArgs a) {
 #pragma unroll
     for (int u = 0; u < AHEAD; ++u) {
       const int64_t t = tb + u * SWARPS;
-      const int64_t slot = t < t1 ? slot_of(a, b, t) : -1;  // a bad page reads as empty
+      const int64_t slot = t < t1 ? item_slot(a, b, t, t0, pt) : -1;  // a bad page reads as empty
       have[u] = slot >= 0;
       if (have[u]) {
         const uint8_t* row = a.codes + slot * D;
         cl[u] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
         cr[u] = __ldg(reinterpret_cast<const uint16_t*>(row + DL) + lane);
         sc[u] = __ldg(reinterpret_cast<const float2*>(a.scales + slot * 2));
+      } else {
+        cl[u] = make_uint4(0u, 0u, 0u, 0u);
+        cr[u] = 0;
+        sc[u] = make_float2(0.f, 0.f);
       }
     }
+    // the lane partials of all the group's scores, then their sums over the warp
+    // together (the butterflies of the sixteen (token, head) pairs interleave)
+    float z[AHEAD][HG_SIMT];
 #pragma unroll
     for (int u = 0; u < AHEAD; ++u) {
-      if (!have[u]) continue;
       float v[16], vr[2];
       e4m3x4_to_f32(cl[u].x, v); e4m3x4_to_f32(cl[u].y, v + 4);
       e4m3x4_to_f32(cl[u].z, v + 8); e4m3x4_to_f32(cl[u].w, v + 12);
@@ -114,12 +122,27 @@ decode_simt_kernel(DecodeArgs a) {
         for (int k = 0; k < 16; ++k) dl = fmaf(qL[j][k], v[k], dl);
         dr = fmaf(qR[j][0], vr[0], dr);
         dr = fmaf(qR[j][1], vr[1], dr);
-        float z = sc[u].x * dl + sc[u].y * dr;  // the row scales, outside the dot products
+        z[u][j] = sc[u].x * dl + sc[u].y * dr;  // the row scales, outside the dot products
+      }
+    }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-        const float mn = fmaxf(m[j], z);
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int u = 0; u < AHEAD; ++u)
+#pragma unroll
+        for (int j = 0; j < HG_SIMT; ++j) z[u][j] += __shfl_xor_sync(0xffffffffu, z[u][j], off);
+    // the online softmax, token by token (in the same order as before)
+#pragma unroll
+    for (int u = 0; u < AHEAD; ++u) {
+      if (!have[u]) continue;
+      float v[16];
+      e4m3x4_to_f32(cl[u].x, v); e4m3x4_to_f32(cl[u].y, v + 4);
+      e4m3x4_to_f32(cl[u].z, v + 8); e4m3x4_to_f32(cl[u].w, v + 12);
+#pragma unroll
+      for (int j = 0; j < HG_SIMT; ++j) {
+        const float mn = fmaxf(m[j], z[u][j]);
         const float alpha = exp2f(m[j] - mn);  // 0 on the first token (m = -inf)
-        const float p = exp2f(z - mn);
+        const float p = exp2f(z[u][j] - mn);
         l[j] = l[j] * alpha + p;
         const float w = p * sc[u].x;
 #pragma unroll
@@ -129,44 +152,54 @@ decode_simt_kernel(DecodeArgs a) {
     }
   }
 
-  // merge the 8 warps: max, then rescaled sums into shared memory
-  __shared__ float sm_m[SWARPS][HG_SIMT];
-  __shared__ float sm_M[HG_SIMT], sm_l[HG_SIMT];
-  __shared__ float sm_o[HG_SIMT][DL];
+  // merge the 8 warps: the common max, then the rescaled partials of warps w and
+  // w + 4 added into buffer w, then the four buffers added in order.  Channel
+  // 16 l + k of a head sits at k * 32 + l (the lanes of a warp on distinct banks).
+  __shared__ float sm_m[SWARPS][HG_SIMT], sm_l[SWARPS][HG_SIMT];
+  __shared__ float sm_o[SWARPS / 2][HG_SIMT][DL];
   if (lane == 0) {
 #pragma unroll
     for (int j = 0; j < HG_SIMT; ++j) sm_m[warp][j] = m[j];
   }
-  for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) (&sm_o[0][0])[i] = 0.f;
-  if (threadIdx.x < HG_SIMT) sm_l[threadIdx.x] = 0.f;
   __syncthreads();
-  if (threadIdx.x < HG_SIMT) {
-    float M = -INFINITY;
-    for (int w = 0; w < SWARPS; ++w) M = fmaxf(M, sm_m[w][threadIdx.x]);
-    sm_M[threadIdx.x] = M;
+  float M[HG_SIMT], f[HG_SIMT];
+#pragma unroll
+  for (int j = 0; j < HG_SIMT; ++j) {
+    M[j] = sm_m[0][j];
+#pragma unroll
+    for (int w = 1; w < SWARPS; ++w) M[j] = fmaxf(M[j], sm_m[w][j]);
+    f[j] = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - M[j]);
+    if (lane == 0) sm_l[warp][j] = l[j] * f[j];
+  }
+  float* buf = &sm_o[warp % (SWARPS / 2)][0][0];
+  if (warp < SWARPS / 2) {
+#pragma unroll
+    for (int j = 0; j < HG_SIMT; ++j)
+#pragma unroll
+      for (int k = 0; k < 16; ++k) buf[j * DL + k * 32 + lane] = o[j][k] * f[j];
   }
   __syncthreads();
-  // fixed-order sum over the warps (no atomics), so results are bitwise reproducible
-  for (int wr = 0; wr < SWARPS; ++wr) {
-    if (warp == wr) {
+  if (warp >= SWARPS / 2) {
 #pragma unroll
-      for (int j = 0; j < HG_SIMT; ++j) {
-        const float f = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - sm_M[j]);
+    for (int j = 0; j < HG_SIMT; ++j)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) sm_o[j][lane * 16 + k] += o[j][k] * f;
-        if (lane == 0) sm_l[j] += l[j] * f;
-      }
-    }
-    __syncthreads();
+      for (int k = 0; k < 16; ++k) buf[j * DL + k * 32 + lane] += o[j][k] * f[j];
   }
+  __syncthreads();
+  // fixed-order sums (no atomics), so results are bitwise reproducible
   const int64_t base = (int64_t)blockIdx.x * HG_SIMT;  // this item's partials
   for (int i = threadIdx.x; i < HG_SIMT * DL; i += blockDim.x) {
-    const int j = i / DL, d = i % DL;
-    if (h0 + j < a.H) a.ws_o[(base + j) * DL + d] = sm_o[j][d];
+    const int j = i / DL, r = i % DL;  // r = k * 32 + l: channel d = 16 l + k
+    const float* o0 = &sm_o[0][0][0];
+    const float v = (o0[i] + o0[HG_SIMT * DL + i]) + (o0[2 * HG_SIMT * DL + i] + o0[3 * HG_SIMT * DL + i]);
+    if (h0 + j < a.H) a.ws_o[(base + j) * DL + (r & 31) * 16 + (r >> 5)] = v;
   }
   if (threadIdx.x < HG_SIMT && h0 + threadIdx.x < a.H) {
-    a.ws_m[base + threadIdx.x] = sm_M[threadIdx.x];
-    a.ws_l[base + threadIdx.x] = sm_l[threadIdx.x];
+    const int j = threadIdx.x;
+    float L = 0.f;
+    for (int w = 0; w < SWARPS; ++w) L += sm_l[w][j];
+    a.ws_m[base + j] = M[j];
+    a.ws_l[base + j] = L;
   }
 }
 

@@ -41,18 +41,6 @@ __device__ __forceinline__ uint16_t f16x2_to_e4m3x2(__half2 v) {
   return r;
 }
 
-// Page-table lookup: cache slot of token t of sequence b, or -1 if the block
-// table entry is out of range (the error word records it).
-__device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int64_t t) {
-  if (a.block_table == nullptr) return t;
-  const int32_t blk = __ldg(&a.block_table[(int64_t)b * a.max_blocks + (t >> 6)]);
-  if (blk < 0 || (int64_t)blk >= a.n_blocks) {
-    atomicOr(a.err, ERR_BLOCK_TABLE);
-    return -1;
-  }
-  return (int64_t)blk * PAGE + (t & (PAGE - 1));
-}
-
 // Length of sequence b, clamped to what its block table can address.
 __device__ __forceinline__ int64_t seq_len_of(const DecodeArgs& a, int b) {
   if (a.seq_lens == nullptr) return a.T_contig;

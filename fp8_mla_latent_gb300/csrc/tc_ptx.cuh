@@ -416,6 +416,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to global memory, in the thread's bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
 // arrive on a barrier of any CTA of the cluster, raising its expected transaction bytes
 __device__ __forceinline__ void arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
   asm volatile(
