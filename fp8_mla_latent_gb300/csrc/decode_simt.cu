@@ -16,6 +16,7 @@
 // This is the kernel for small head counts (and a cross-check of the tensor-core
 // kernel): at H >= 16 its FP32 lanes, not HBM, bound it.
 #include "kv8_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace kv8 {
 namespace {
@@ -140,14 +141,20 @@ decode_simt_kernel(DecodeArgs a) {
       e4m3x4_to_f32(cl[u].z, v + 8); e4m3x4_to_f32(cl[u].w, v + 12);
 #pragma unroll
       for (int j = 0; j < HG_SIMT; ++j) {
-        const float mn = fmaxf(m[j], z[u][j]);
-        const float alpha = exp2f(m[j] - mn);  // 0 on the first token (m = -inf)
-        const float p = exp2f(z[u][j] - mn);
-        l[j] = l[j] * alpha + p;
+        // a new max rescales the running sums (the same in every lane: z is the
+        // warp's sum); 2^(m - mn) is 0 on the first token (m = -inf)
+        if (z[u][j] > m[j]) {
+          const float alpha = ptx::ex2_approx(m[j] - z[u][j]);
+          l[j] *= alpha;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[j][k] *= alpha;
+          m[j] = z[u][j];
+        }
+        const float p = ptx::ex2_approx(z[u][j] - m[j]);
+        l[j] += p;
         const float w = p * sc[u].x;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) o[j][k] = fmaf(w, v[k], o[j][k] * alpha);
-        m[j] = mn;
+        for (int k = 0; k < 16; ++k) o[j][k] = fmaf(w, v[k], o[j][k]);
       }
     }
   }
