@@ -251,18 +251,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
 
 
-  // The query of segment j's heads in the score MMA's B form, by the softmax
-  // warps: K-block k (Lc channels 128k.., k = 4: Rc) holds NB rows, row h the hi
-  // term of head h and row N + h its lo term (rows of 128 bytes, 128-byte swizzle;
-  // the Rc block rows of 64 bytes, 64-byte swizzle), and c_h.  Heads past H get
-  // zeros and c_h = 0.
-  auto load_query = [&](int j) {
+  // The query of segment j's heads in the score MMA's B form, by threads tid of
+  // nt (the softmax warps for the first segment, the load warp for the second):
+  // K-block k (Lc channels 128k.., k = 4: Rc) holds NB rows, row h the hi term of
+  // head h and row N + h its lo term (rows of 128 bytes, 128-byte swizzle; the Rc
+  // block rows of 64 bytes, 64-byte swizzle), and c_h.  Heads past H get zeros and
+  // c_h = 0.
+  auto load_query = [&](int j, int tid, int nt) {
     const int b = s_rg.s[j].b, h0 = s_rg.s[j].g * N;
-    for (int k = threadIdx.x - W_SOFT * 32; k < N * 72; k += NSOFT * 32) {
-      const int hh = k / 72, u = k % 72;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (h0 + hh < a.H)
-        v = __ldg(reinterpret_cast<const uint4*>(a.q8 + ((int64_t)b * a.H + h0 + hh) * Q8_BYTES) + u);
+    constexpr int QU = 8;  // 16-byte units in flight per thread
+    for (int k0 = tid; k0 < N * 72; k0 += QU * nt) {
+      uint4 vv[QU];
+#pragma unroll
+      for (int e = 0; e < QU; ++e) {
+        const int k = k0 + e * nt, hh = k / 72, u = k % 72;
+        vv[e] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < N * 72 && h0 + hh < a.H)
+          vv[e] = __ldg(reinterpret_cast<const uint4*>(a.q8 + ((int64_t)b * a.H + h0 + hh) * Q8_BYTES) + u);
+      }
+#pragma unroll
+      for (int e = 0; e < QU; ++e) {
+      const int k = k0 + e * nt, hh = k / 72, u = k % 72;
+      if (k >= N * 72) break;
+      const uint4 v = vv[e];
       int blk, r, uu;
       if (u < 32) {
         blk = u >> 3; uu = u & 7; r = hh;
@@ -274,9 +285,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         blk = 4; uu = u - 68; r = N + hh;
       }
       sts128(qb + blk * NB * 128 + (blk < 4 ? sw128(r, uu) : sw64(r, uu)), v);
+      }
     }
-    const int st = threadIdx.x - W_SOFT * 32;
-    if (st < N) cs[st] = (h0 + st < a.H) ? __ldg(&a.cq[(int64_t)b * a.H + h0 + st]) : 0.f;
+    for (int st = tid; st < N; st += nt)
+      cs[st] = (h0 + st < a.H) ? __ldg(&a.cq[(int64_t)b * a.H + h0 + st]) : 0.f;
     fence_proxy_async_smem();
   };
 
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     load_page_table(a, s_rg.s[0].b, s_rg.s[0].t0, s_rg.s[0].t1, pt, lane);
   } else if (warp >= W_SOFT) {
     grid_dependency_wait();  // the query-prep launch has completed
-    load_query(0);
+    load_query(0, threadIdx.x - W_SOFT * 32, NSOFT * 32);
   }
   tc_fence_before();
   __syncthreads();
@@ -384,8 +396,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int split = seg_tiles(0), n_all = split + (nseg > 1 ? seg_tiles(1) : 0);
     bool ok = true;
     for (int i = 0; ok && i < n_all; ++i) {  // tiles counted across segments
-      // the second segment's query: the softmax warps load it once they have read
-      // the first segment's last scores
+      // the second segment's query: the softmax warps put it in place once they
+      // have read the first segment's last scores, before that segment's epilogue
       if (i == split && !mbar_wait_warp(&bars[C::B_QREADY], 0, abort_flag, WAIT_NS)) {
         ok = false;
         break;
@@ -510,12 +522,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int n_tiles = seg_tiles(seg);
     const int h0 = s_rg.s[seg].g * N;
     if (seg > 0) {
-      // the next segment's query, once this warp has read the last scores of the
-      // previous one (its score MMAs are all done); the barrier also shows every
-      // softmax warp the new c_h
-      load_query(seg);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C::B_QREADY]);
+      // every softmax warp has put its share of the query and c_h in place
       if (!mbar_wait_warp(&bars[C::B_QREADY], 0, abort_flag, WAIT_NS)) {
         ok = false;
         break;
@@ -694,6 +701,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(&bars[C::B_PFULL + buf]);
     }
     if (!ok) break;
+    if (seg + 1 < nseg) {
+      // the next segment's query: this warp has seen this segment's last scores,
+      // so the score MMAs that read the query are done; the next segment's first
+      // scores then overlap this segment's last context MMAs and epilogue
+      load_query(seg + 1, threadIdx.x - W_SOFT * 32, NSOFT * 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_QREADY]);
+    }
     {
       ok = mbar_wait_warp(&bars[C::B_ODONE + ((gi - 1) & 1)], ((gi - 1) >> 1) & 1,
                           abort_flag, WAIT_NS);

@@ -92,7 +92,8 @@ __device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b) {
 // at the start of a call instead of several.)
 constexpr int SEQ_CACHE = 4;
 struct SeqTiles {
-  uint32_t t[SEQ_CACHE];
+  uint32_t t[SEQ_CACHE];  // tiles
+  uint32_t n[SEQ_CACHE];  // tokens (clamped lengths, below 2^31)
   bool cached;
 };
 
@@ -103,8 +104,22 @@ __device__ __forceinline__ void load_tiles(const DecodeArgs& a, SeqTiles& c) {
 #pragma unroll
   for (int k = 0; k < SEQ_CACHE; ++k) {
     const int b = lane + 32 * k;
-    c.t[k] = (c.cached && b < a.B) ? tiles_of(a, b) : 0u;
+    const uint32_t n = (c.cached && b < a.B) ? (uint32_t)seq_len_of(a, b) : 0u;
+    c.n[k] = n;
+    c.t[k] = (n + (uint32_t)(TILE - 1)) / (uint32_t)TILE;
   }
+}
+
+// Length of sequence 32 k + lane (0 past the last sequence).
+__device__ __forceinline__ uint32_t len_at(const DecodeArgs& a, const SeqTiles& c, int k) {
+  if (c.cached) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int j = 0; j < SEQ_CACHE; ++j) v = (j == k) ? c.n[j] : v;
+    return v;
+  }
+  const int b = 32 * k + (int)(threadIdx.x & 31);
+  return b < a.B ? (uint32_t)seq_len_of(a, b) : 0u;
 }
 
 // Tiles of sequence 32 k + lane (0 past the last sequence).
@@ -229,7 +244,7 @@ __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkIt
       it.b = bb;
       it.g = (int)(r / nsb);
       it.t0 = (int64_t)s * st * TILE;
-      const int64_t T = seq_len_of(a, bb);
+      const int64_t T = __shfl_sync(0xffffffffu, len_at(a, c, kk), src);
       const int64_t e = (int64_t)(s + 1) * st * TILE;
       it.t1 = e < T ? e : T;
       it.first = (int64_t)fb + (int64_t)it.g * nsb;
@@ -264,12 +279,13 @@ struct Range {
   Segment s[2];
 };
 
-// First tile of range k of NC over `total` tiles, and the range holding tile x.
-__device__ __forceinline__ int64_t range_start(int64_t k, int64_t NC, int64_t total) {
-  return k * total / NC;
+// First tile of range k of NC over `total` tiles, and the range holding tile x
+// (s32: total * NC < 2^32, so every product and quotient fits 32 bits).
+__device__ __forceinline__ int64_t range_start(int64_t k, int64_t NC, int64_t total, bool s32) {
+  return s32 ? (int64_t)((uint32_t)(k * total) / (uint32_t)NC) : k * total / NC;
 }
-__device__ __forceinline__ int64_t range_of(int64_t x, int64_t NC, int64_t total) {
-  return ((x + 1) * NC - 1) / total;
+__device__ __forceinline__ int64_t range_of(int64_t x, int64_t NC, int64_t total, bool s32) {
+  return s32 ? (int64_t)((uint32_t)((x + 1) * NC - 1) / (uint32_t)total) : ((x + 1) * NC - 1) / total;
 }
 
 // Warp-wide: whether this call runs on ranges, and if so CTA k's range.  Returns
@@ -301,7 +317,8 @@ __device__ __forceinline__ bool find_range(const DecodeArgs& a, int64_t k, Range
   if ((int64_t)tmin < L || count_items(a, c, (uint32_t)L) <= a.plan.target) return false;
   r.n = 0;
   if (k >= NC) return true;  // no range for this CTA
-  const int64_t T0 = range_start(k, NC, total), T1 = range_start(k + 1, NC, total);
+  const bool s32 = total * (uint64_t)NC < (uint64_t(1) << 32);
+  const int64_t T0 = range_start(k, NC, total, s32), T1 = range_start(k + 1, NC, total, s32);
   // Walk the pairs in order: the pair holding T0 (segment 0), the next one if
   // the range reaches it (segment 1), and the pair starts before T0 that do not
   // fall on a range start (each adds a segment to the numbering).
@@ -321,7 +338,7 @@ __device__ __forceinline__ bool find_range(const DecodeArgs& a, int64_t k, Range
     int cnt = 0;
     for (int g = 0; g < n_hg && tl > 0; ++g) {
       const int64_t st = sb + g * tl;
-      if (st > 0 && st < T0 && range_start(range_of(st, NC, total), NC, total) != st) ++cnt;
+      if (st > 0 && st < T0 && range_start(range_of(st, NC, total, s32), NC, total, s32) != st) ++cnt;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -335,19 +352,19 @@ __device__ __forceinline__ bool find_range(const DecodeArgs& a, int64_t k, Range
       const int src = __ffs(m) - 1;
       const int bb = __shfl_sync(0xffffffffu, b, src);
       const int64_t sbb = __shfl_sync(0xffffffffu, sb, src), tlb = __shfl_sync(0xffffffffu, tl, src);
-      const int g = (int)((x - sbb) / tlb);
+      const int g = s32 ? (int)((uint32_t)(x - sbb) / (uint32_t)tlb) : (int)((x - sbb) / tlb);
       const int64_t ps = sbb + g * tlb, pe = ps + tlb;  // the pair's tiles [ps, pe)
       Segment& sg = r.s[want];
       sg.b = bb;
       sg.g = g;
       const int64_t lo = (want == 0 ? T0 : ps) - ps;
       const int64_t hi = (T1 < pe ? T1 : pe) - ps;
-      const int64_t T = seq_len_of(a, bb);
+      const int64_t T = __shfl_sync(0xffffffffu, len_at(a, c, kk), src);
       sg.t0 = lo * TILE;
       sg.t1 = hi * TILE < T ? hi * TILE : T;
       sg.starts = (lo == 0);
       sg.first = 0;  // set below, with the numbering
-      sg.count = range_of(pe - 1, NC, total) - range_of(ps, NC, total) + 1;
+      sg.count = range_of(pe - 1, NC, total, s32) - range_of(ps, NC, total, s32) + 1;
       found = want + 1;
     }
     base += __shfl_sync(0xffffffffu, inc, 31);
