@@ -23,6 +23,9 @@ namespace {
 
 constexpr int HG_SIMT = 4;
 constexpr int SWARPS = 8;
+// Items are cut in units of 32 tokens (one group of four tokens per warp), not
+// whole tiles, so that a short cache spreads over many SMs.
+constexpr int LOG2_UNIT = 5;
 constexpr float LOG2E = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(SWARPS * 32, 1)
@@ -33,7 +36,7 @@ decode_simt_kernel(DecodeArgs a) {
   __shared__ int32_t pt[PT_PAGES];  // the item's block-table entries
   if (warp == 0) {
     WorkItem it;
-    const bool ok = find_item(a, blockIdx.x, it);
+    const bool ok = find_item(a, blockIdx.x, it, LOG2_UNIT);
     if (lane == 0 && ok) record_segment(a, blockIdx.x, it);
     if (ok) load_page_table(a, it.b, it.t0, it.t1, pt, lane);
     if (lane == 0) {

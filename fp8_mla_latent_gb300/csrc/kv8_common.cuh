@@ -78,10 +78,10 @@ __device__ __forceinline__ void record_segment(const DecodeArgs& a, int64_t k, c
   }
 }
 
-__device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b) {
+__device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b, int lg = LOG2_TILE) {
   // a length is at most max_blocks * PAGE (or the contiguous cache's rows, below
   // 2^31), so the count of 128-token tiles fits 32 bits
-  return (uint32_t)((seq_len_of(a, b) + TILE - 1) / TILE);
+  return (uint32_t)((seq_len_of(a, b) + (int64_t(1) << lg) - 1) >> lg);
 }
 
 // Tile counts of the sequences, held in registers: lane l keeps sequences l,
@@ -92,21 +92,23 @@ __device__ __forceinline__ uint32_t tiles_of(const DecodeArgs& a, int b) {
 // at the start of a call instead of several.)
 constexpr int SEQ_CACHE = 4;
 struct SeqTiles {
-  uint32_t t[SEQ_CACHE];  // tiles
+  uint32_t t[SEQ_CACHE];  // units of 2^lg tokens (tiles, unless a kernel cuts finer)
   uint32_t n[SEQ_CACHE];  // tokens (clamped lengths, below 2^31)
+  int lg;
   bool cached;
 };
 
 // Warp-wide (all 32 lanes).
-__device__ __forceinline__ void load_tiles(const DecodeArgs& a, SeqTiles& c) {
+__device__ __forceinline__ void load_tiles(const DecodeArgs& a, SeqTiles& c, int lg = LOG2_TILE) {
   const int lane = threadIdx.x & 31;
+  c.lg = lg;
   c.cached = a.B <= 32 * SEQ_CACHE;
 #pragma unroll
   for (int k = 0; k < SEQ_CACHE; ++k) {
     const int b = lane + 32 * k;
     const uint32_t n = (c.cached && b < a.B) ? (uint32_t)seq_len_of(a, b) : 0u;
     c.n[k] = n;
-    c.t[k] = (n + (uint32_t)(TILE - 1)) / (uint32_t)TILE;
+    c.t[k] = (n + ((1u << lg) - 1u)) >> lg;
   }
 }
 
@@ -131,7 +133,7 @@ __device__ __forceinline__ uint32_t tiles_at(const DecodeArgs& a, const SeqTiles
     return v;
   }
   const int b = 32 * k + (int)(threadIdx.x & 31);
-  return b < a.B ? tiles_of(a, b) : 0u;
+  return b < a.B ? tiles_of(a, b, c.lg) : 0u;
 }
 
 __device__ __forceinline__ uint64_t warp_sum64(uint64_t v) {
@@ -207,14 +209,16 @@ __device__ __forceinline__ int64_t item_tiles(const DecodeArgs& a, const SeqTile
   }
 }
 
-// Warp-wide: the work item with index k; false if k is past the last item.  The
+// Warp-wide: the work item with index k; false if k is past the last item.  Items
+// are whole units of 2^lg tokens (tiles, unless a kernel asks for finer cuts).  The
 // sequences are walked 32 at a time with the inclusive scan of their item counts.
 // Item counts and indices fit 32 bits (the grid holds every item), and so does a
 // sequence's tile count; only token offsets need 64 bits.
-__device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it) {
+__device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkItem& it,
+                                          int lg = LOG2_TILE) {
   const int lane = threadIdx.x & 31;
   SeqTiles c;
-  load_tiles(a, c);
+  load_tiles(a, c, lg);
   const int64_t st = item_tiles(a, c);
   // st >= 2^31 only when every sequence is one item: ceil(tiles / st) is then 0 or 1
   const uint32_t st32 = st < (int64_t(1) << 31) ? (uint32_t)st : 0x80000000u;
@@ -243,9 +247,9 @@ __device__ __forceinline__ bool find_item(const DecodeArgs& a, int64_t k, WorkIt
       const uint32_t s = r % nsb;
       it.b = bb;
       it.g = (int)(r / nsb);
-      it.t0 = (int64_t)s * st * TILE;
+      it.t0 = ((int64_t)s * st) << lg;
       const int64_t T = __shfl_sync(0xffffffffu, len_at(a, c, kk), src);
-      const int64_t e = (int64_t)(s + 1) * st * TILE;
+      const int64_t e = ((int64_t)(s + 1) * st) << lg;
       it.t1 = e < T ? e : T;
       it.first = (int64_t)fb + (int64_t)it.g * nsb;
       it.count = nsb;

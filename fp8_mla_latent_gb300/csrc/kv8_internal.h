@@ -14,6 +14,8 @@ constexpr int DR = 64;     // qk_rope width
 constexpr int D = 576;     // bytes per cached row
 constexpr int PAGE = 64;   // tokens per page in the paged layout
 constexpr int TILE = 128;  // tokens per decode tile (the M of the score MMA)
+constexpr int LOG2_TILE = 7;
+static_assert((1 << LOG2_TILE) == TILE, "tile size");
 constexpr int NUM_SMS = 152;  // GB300: 2 dies x 76 SMs
 
 // Device-side error bits written into the workspace header.
