@@ -34,7 +34,8 @@
 //   sixteen warps turn the received p into the context operand in place,
 //   P''[h][t] = p w_t (f16) as two e4m3 terms, hi + lo; zero the V rows without
 //   data; rescale the O rows of heads whose factor moved, one half of O while the
-//   MMAs of the other half run; and write the partial o at the end.
+//   MMAs of the other half run; and write the partial o at the end (each head's
+//   O half-row put in a padded shared-memory row and sent by one bulk copy).
 //   O[h][d] += sum_t P''[h][t] V[t][d]   kind::f8f6f4, M = 128 heads, N = 256
 //             latent channels (two halves of 512), K = 32 tokens per MMA, hi and
 //             lo terms into the same accumulator (all 512 TMEM columns).  V is the

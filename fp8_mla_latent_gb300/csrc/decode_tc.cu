@@ -10,6 +10,12 @@
 //   o   = sum_t softmax(z)_t sLc_t dec(Lc_t)
 //
 // One CTA = one work item (sequence, group of N heads, range of 128-token tiles).
+// When every (sequence, head group) pair holds at least a range's worth of tiles,
+// the items are instead equal ranges of the tiles of all pairs in order, one per
+// CTA: a range that reaches the end of its pair continues into the next one, as a
+// second segment with its own query, page table and partial (the softmax warps put
+// the next query in place as soon as they have seen the first segment's last
+// scores, so the next scores overlap the first segment's epilogue).
 // Every byte of a tile is loaded once, by TMA: the four Lc blocks into a ring of
 // [128 tokens x 128 bytes] slots (128-byte swizzle), the Rc block into a ring of
 // [128 tokens x 64 bytes] slots (64-byte swizzle).  Both contractions read those

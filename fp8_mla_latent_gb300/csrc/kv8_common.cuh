@@ -61,7 +61,9 @@ __device__ __forceinline__ int64_t seq_len_of(const DecodeArgs& a, int b) {
 // there are more (sequence, head group) pairs than one wave holds, the items are
 // ceil(total / target) tiles long and spread over several waves.  Items are
 // numbered by sequence, then head group, then position; every kernel of a call
-// derives the same numbering from the sequence lengths, on the device.
+// derives the same numbering from the sequence lengths, on the device.  The
+// tensor-core kernels count in 128-token tiles; the CUDA-core kernel in 32-token
+// units, so that a short cache spreads over more SMs.
 
 struct WorkItem {
   int b, g;        // sequence, head group
