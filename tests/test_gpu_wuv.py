@@ -61,3 +61,21 @@ def test_wuv_deterministic():
     y2 = pkg.mla_wuv_epilogue(o, w)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+def test_wuv_weights_not_16_byte_aligned():
+    """Weights 2 bytes past a 16-byte boundary take the plain path (no bulk copies)."""
+    rng = np.random.default_rng(11)
+    d = torch.device("cuda:0")
+    B, H, V = 3, 4, 128
+    o = rng.standard_normal((B, H, 512)).astype(np.float32)
+    w = bf16_weights(rng, H, V)
+    flat = torch.empty(H * 512 * V + 8, dtype=torch.bfloat16, device=d)
+    wd = flat[1:1 + H * 512 * V].view(H, 512, V)
+    wd.copy_(w.to(d))
+    assert wd.data_ptr() % 16 == 2
+    y = pkg.mla_wuv_epilogue(torch.from_numpy(o).to(d), wd)
+    torch.cuda.synchronize()
+    ref = oracle.wuv_project(o, w.view(torch.int16).numpy().view(np.uint16))
+    err = np.abs(y.cpu().numpy() - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert err <= 1e-5, err
