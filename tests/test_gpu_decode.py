@@ -74,7 +74,7 @@ def test_workloads_small(name, scale, variant):
     check(w, out, lse, c, s, pairs, variant)
 
 
-@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 1000])
+@pytest.mark.parametrize("T", [1, 2, 31, 33, 63, 64, 65, 127, 128, 129, 255, 300, 1000])
 @pytest.mark.parametrize("H", [1, 3, 16, 17, 64, 100, 128])
 def test_ragged_lengths_and_head_counts(T, H, variant):
     if H * T > 128 * 300 and T > 300:
