@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 
   // The query of segment j's heads in the score MMA's B form, by threads tid of
-  // nt (the softmax warps for the first segment, the load warp for the second):
+  // nt (the softmax warps, for the first segment and for the second alike):
   // K-block k (Lc channels 128k.., k = 4: Rc) holds NB rows, row h the hi term of
   // head h and row N + h its lo term (rows of 128 bytes, 128-byte swizzle; the Rc
   // block rows of 64 bytes, 64-byte swizzle), and c_h.  Heads past H get zeros and
