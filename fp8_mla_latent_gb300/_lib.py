@@ -109,6 +109,17 @@ def _need(t, name, dtype, ndim=None, device=True):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def _need_workspace(ws):
+    """A caller's workspace: a contiguous CUDA tensor of any dtype (its size is
+    checked by the library against the call's need)."""
+    if not isinstance(ws, torch.Tensor):
+        raise TypeError("workspace must be a torch.Tensor")
+    if not ws.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor (the library has no CPU path)")
+    if not ws.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+
+
 def _check(fn, status):
     if status != 0:
         raise Kv8Error(fn, status)
@@ -260,11 +271,16 @@ def mla_absorb_decode_fp8(q_lat, q_rope, kv_codes, kv_scales, T, sm_scale, out=N
     if out is None:
         out = torch.empty((H, KV8_DL), dtype=torch.float32, device=q_lat.device)
     _need(out, "out", torch.float32, 2)
+    if tuple(out.shape) != (H, KV8_DL):
+        raise ValueError("out must be [H,512]")
     if lse is not None:
         _need(lse, "lse", torch.float32, 1)
+        if lse.shape[0] != H:
+            raise ValueError("lse must be [H]")
     need = mla_absorb_decode_fp8_workspace_size(T, H, variant)
     if workspace is None:
         workspace = alloc_workspace(need, q_lat.device)
+    _need_workspace(workspace)
     st = lib().mla_absorb_decode_fp8(_ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales),
                                      int(T), H, float(sm_scale), _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -315,6 +331,7 @@ def mla_absorb_decode_fp8_batch(q_lat, q_rope, kv_codes, kv_scales, block_table,
     need = mla_absorb_decode_fp8_batch_workspace_size(B, H, max_blocks, block_size, variant)
     if workspace is None:
         workspace = alloc_workspace(need, q_lat.device)
+    _need_workspace(workspace)
     st = lib().mla_absorb_decode_fp8_batch(
         _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
         _ptr(seq_lens), B, H, max_blocks, int(block_size), int(n_blocks), float(sm_scale),
@@ -331,6 +348,7 @@ def mla_absorb_decode_fp8_batch_partials(q_lat, q_rope, kv_codes, kv_scales, blo
     """Split phase 1: the split-T kernel only; partials stay in ``workspace``."""
     B, H, _ = _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens,
                             outputs=False)
+    _need_workspace(workspace)
     st = lib().mla_absorb_decode_fp8_batch_partials(
         _ptr(q_lat), _ptr(q_rope), _ptr(kv_codes), _ptr(kv_scales), _ptr(block_table),
         _ptr(seq_lens), B, H, block_table.shape[1], int(block_size),
@@ -343,6 +361,16 @@ def mla_absorb_decode_fp8_batch_combine(seq_lens, H, max_blocks, out, lse, works
                                         variant=KV8_DECODE_AUTO, block_size=KV8_BLOCK,
                                         stream=None):
     """Split phase 2: merge the workspace partials into ``out`` / ``lse``."""
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = seq_lens.shape[0]
+    _need(out, "out", torch.float32, 3)
+    if tuple(out.shape) != (B, int(H), KV8_DL):
+        raise ValueError("out must be [B,H,512], B = len(seq_lens)")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+        if tuple(lse.shape) != (B, int(H)):
+            raise ValueError("lse must be [B,H]")
+    _need_workspace(workspace)
     st = lib().mla_absorb_decode_fp8_batch_combine(
         _ptr(seq_lens), seq_lens.shape[0], int(H), int(max_blocks), int(block_size), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), int(variant),
@@ -351,6 +379,7 @@ def mla_absorb_decode_fp8_batch_combine(seq_lens, H, max_blocks, out, lse, works
 
 
 def kv8_workspace_error(workspace, stream=None) -> int:
+    _need_workspace(workspace)
     return int(lib().kv8_workspace_error(_ptr(workspace), _stream(stream)))
 
 

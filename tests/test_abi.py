@@ -6,6 +6,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import fp8_mla_latent_gb300 as pkg
 
@@ -154,6 +155,22 @@ def test_decode_rejects_bad_arguments_on_host():
     a[3] = P(g + 8)
     assert b(*a) == EALIGN
     assert b(*([P(g)] * 6 + [0, 4, 8, 64, 16, 0.1, P(g), None, P(g), 1 << 30, 0, None])) == 0
+
+
+def test_wrappers_refuse_host_tensors_before_the_library():
+    """A host pointer handed to a kernel would fault the device, so the binding
+    refuses host tensors by name before anything reaches the library (without a
+    GPU every tensor is a host tensor)."""
+    ws = torch.empty(64, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.kv8_workspace_error(ws)
+    with pytest.raises(TypeError, match="^workspace"):
+        pkg.kv8_workspace_error(bytes(64))
+    sl = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(TypeError, match="^seq_lens"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl.long(), 4, 2, None, None, ws)
+    with pytest.raises(ValueError, match="^seq_lens"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl, 4, 2, None, None, ws)
 
 
 @pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])

@@ -266,3 +266,43 @@ def test_report_worst_error():
     """Not a check: prints the worst err/max|out| seen per kernel in this session."""
     from gpu_helpers import NAMES, WORST
     print("worst err / max|out|: " + ", ".join(f"{NAMES[k]} {v:.2e}" for k, v in sorted(WORST.items())))
+
+
+def test_wrappers_reject_host_buffers_and_bad_shapes():
+    """Arguments a kernel would misread are refused in Python, before any launch: a
+    host workspace (a host pointer in a kernel faults the device), and out / lse /
+    seq_lens of the wrong shape or type."""
+    d = torch.device("cuda:0")
+    H, B, MB = 16, 2, 4
+    codes = torch.zeros((B * MB * 64, 576), dtype=torch.uint8, device=d)
+    scales = torch.zeros((B * MB * 64, 2), device=d)
+    host_ws = torch.empty(1 << 20, dtype=torch.uint8)
+    q = torch.zeros((H, 512), device=d)
+    r = torch.zeros((H, 64), device=d)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.mla_absorb_decode_fp8(q, r, codes, scales, 10, 0.1, workspace=host_ws)
+    with pytest.raises(ValueError, match="^out"):
+        pkg.mla_absorb_decode_fp8(q, r, codes, scales, 10, 0.1, out=torch.empty((H, 256), device=d))
+    with pytest.raises(ValueError, match="^lse"):
+        pkg.mla_absorb_decode_fp8(q, r, codes, scales, 10, 0.1, lse=torch.empty(H + 1, device=d))
+    ql = torch.zeros((B, H, 512), device=d)
+    qr = torch.zeros((B, H, 64), device=d)
+    bt = torch.arange(B * MB, dtype=torch.int32, device=d).reshape(B, MB)
+    sl = torch.full((B,), 100, dtype=torch.int32, device=d)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.mla_absorb_decode_fp8_batch(ql, qr, codes, scales, bt, sl, 0.1, workspace=host_ws)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.mla_absorb_decode_fp8_batch_partials(ql, qr, codes, scales, bt, sl, 0.1, host_ws)
+    out = torch.empty((B, H, 512), device=d)
+    lse = torch.empty((B, H), device=d)
+    ws = pkg.alloc_workspace(1 << 20, d)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl, H, MB, out, lse, host_ws)
+    with pytest.raises(ValueError, match="^out"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl, H + 1, MB, out, lse, ws)
+    with pytest.raises(ValueError, match="^lse"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl, H, MB, out, lse[:1], ws)
+    with pytest.raises(TypeError, match="^seq_lens"):
+        pkg.mla_absorb_decode_fp8_batch_combine(sl.long(), H, MB, out, lse, ws)
+    with pytest.raises(ValueError, match="^workspace"):
+        pkg.kv8_workspace_error(host_ws)
