@@ -96,12 +96,17 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _is_device(t) -> bool:
+    """Whether a tensor lives in device memory (the one place the binding asks)."""
+    return t.is_cuda
+
+
 def _need(t, name, dtype, ndim=None, device=True):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if device and not t.is_cuda:
+    if device and not _is_device(t):
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -109,12 +114,20 @@ def _need(t, name, dtype, ndim=None, device=True):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def _need_cache(kv_codes, kv_scales):
+    """The cache: codes uint8 [slots, 576] and their row scales f32 [slots, 2]."""
+    _need(kv_codes, "kv_codes", torch.uint8, 2)
+    _need(kv_scales, "kv_scales", torch.float32, 2)
+    if kv_codes.shape[1] != KV8_D or tuple(kv_scales.shape) != (kv_codes.shape[0], 2):
+        raise ValueError("kv_codes must be [slots,576] and kv_scales [slots,2]")
+
+
 def _need_workspace(ws):
     """A caller's workspace: a contiguous CUDA tensor of any dtype (its size is
     checked by the library against the call's need)."""
     if not isinstance(ws, torch.Tensor):
         raise TypeError("workspace must be a torch.Tensor")
-    if not ws.is_cuda:
+    if not _is_device(ws):
         raise ValueError("workspace must be a CUDA tensor (the library has no CPU path)")
     if not ws.is_contiguous():
         raise ValueError("workspace must be contiguous")
@@ -128,11 +141,11 @@ def _check(fn, status):
 # ----------------------------------------------------------------- quantizer
 def kv8_quantize_rows(src, kv_codes, kv_scales, dst_slot=None, stream=None):
     """Quantize f32 rows src [n, >=576] (row stride = src.stride(0)) into the cache."""
-    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and src.is_cuda
-            and src.dim() == 2 and src.stride(1) == 1):
+    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and _is_device(src)
+            and src.dim() == 2 and src.stride(1) == 1
+            and src.shape[1] >= KV8_D):
         raise ValueError("src must be a CUDA float32 [n, >=576] tensor with unit column stride")
-    _need(kv_codes, "kv_codes", torch.uint8, 2)
-    _need(kv_scales, "kv_scales", torch.float32, 2)
+    _need_cache(kv_codes, kv_scales)
     if dst_slot is not None:
         _need(dst_slot, "dst_slot", torch.int64, 1)
         if dst_slot.numel() != src.shape[0]:
@@ -146,15 +159,15 @@ def kv8_quantize_rows(src, kv_codes, kv_scales, dst_slot=None, stream=None):
 def kv8_produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, kv_codes, kv_scales,
                      dst_slot=None, err_word=None, stream=None):
     """Fused producer: RMS norm (Lc) + rotary pairs (Rc) + quantize raw rows src [n, >=576]."""
-    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and src.is_cuda
-            and src.dim() == 2 and src.stride(1) == 1):
+    if not (isinstance(src, torch.Tensor) and src.dtype == torch.float32 and _is_device(src)
+            and src.dim() == 2 and src.stride(1) == 1
+            and src.shape[1] >= KV8_D):
         raise ValueError("src must be a CUDA float32 [n, >=576] tensor with unit column stride")
     _need(norm_weight, "norm_weight", torch.float32, 1)
     _need(positions, "positions", torch.int64, 1)
     _need(rope_cos, "rope_cos", torch.float32, 2)
     _need(rope_sin, "rope_sin", torch.float32, 2)
-    _need(kv_codes, "kv_codes", torch.uint8, 2)
-    _need(kv_scales, "kv_scales", torch.float32, 2)
+    _need_cache(kv_codes, kv_scales)
     if norm_weight.numel() != KV8_DL:
         raise ValueError("norm_weight must have 512 entries")
     if positions.numel() != src.shape[0]:
@@ -165,7 +178,8 @@ def kv8_produce_rows(src, norm_weight, eps, positions, rope_cos, rope_sin, kv_co
         _need(dst_slot, "dst_slot", torch.int64, 1)
         if dst_slot.numel() != src.shape[0]:
             raise ValueError("dst_slot must have one entry per source row")
-    if err_word is not None and not (err_word.is_cuda and err_word.dtype == torch.int32):
+    if err_word is not None and not (isinstance(err_word, torch.Tensor) and _is_device(err_word)
+                                     and err_word.dtype == torch.int32 and err_word.numel() >= 1):
         raise ValueError("err_word must be a CUDA int32 tensor")
     st = lib().kv8_produce_rows(_ptr(src), src.shape[0], src.stride(0), _ptr(norm_weight),
                                 float(eps), _ptr(positions), _ptr(rope_cos), _ptr(rope_sin),
@@ -179,9 +193,8 @@ def kv8_prefill_project(kv_codes, kv_scales, w_ukv, T=None, slots=None, y=None, 
                         err_word=None, stream=None):
     """Y [T, N] bf16 = dequantized cached latent (slots or 0..T-1) @ W_UKV (bf16 [512, N]);
     k_rope (optional f32 [T, 64]) receives the dequantized rope keys."""
-    _need(kv_codes, "kv_codes", torch.uint8, 2)
-    _need(kv_scales, "kv_scales", torch.float32, 2)
-    if not (isinstance(w_ukv, torch.Tensor) and w_ukv.is_cuda and w_ukv.dim() == 2
+    _need_cache(kv_codes, kv_scales)
+    if not (isinstance(w_ukv, torch.Tensor) and _is_device(w_ukv) and w_ukv.dim() == 2
             and w_ukv.dtype == torch.bfloat16 and w_ukv.is_contiguous() and w_ukv.shape[0] == KV8_DL):
         raise ValueError("w_ukv must be a contiguous CUDA bfloat16 [512, N] tensor")
     if slots is not None:
@@ -192,12 +205,13 @@ def kv8_prefill_project(kv_codes, kv_scales, w_ukv, T=None, slots=None, y=None, 
     N = w_ukv.shape[1]
     if y is None:
         y = torch.empty((T, N), dtype=torch.bfloat16, device=kv_codes.device)
-    if not (y.dtype == torch.bfloat16 and y.is_cuda and y.is_contiguous() and tuple(y.shape) == (T, N)):
+    if not (y.dtype == torch.bfloat16 and _is_device(y) and y.is_contiguous() and tuple(y.shape) == (T, N)):
         raise ValueError("y must be a contiguous CUDA bfloat16 [T, N] tensor")
-    if k_rope is not None and not (k_rope.dtype == torch.float32 and k_rope.is_cuda
+    if k_rope is not None and not (k_rope.dtype == torch.float32 and _is_device(k_rope)
                                    and k_rope.is_contiguous() and tuple(k_rope.shape) == (T, KV8_DR)):
         raise ValueError("k_rope must be a contiguous CUDA float32 [T, 64] tensor")
-    if err_word is not None and not (err_word.is_cuda and err_word.dtype == torch.int32):
+    if err_word is not None and not (isinstance(err_word, torch.Tensor) and _is_device(err_word)
+                                     and err_word.dtype == torch.int32 and err_word.numel() >= 1):
         raise ValueError("err_word must be a CUDA int32 tensor")
     st = lib().kv8_prefill_project(_ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0], _ptr(slots),
                                    int(T), _ptr(w_ukv), int(N), _ptr(y), _ptr(k_rope),
@@ -217,7 +231,7 @@ def kv8_selftest_wait_timeout(workspace, limit_us: int, stream=None):
 def mla_wuv_epilogue(o, w_uv, y=None, stream=None):
     """Per-head value projection y[b,h,:] = o[b,h,:] @ W_UV[h]; o f32 [B,H,512], w_uv bf16 [H,512,V]."""
     _need(o, "o", torch.float32, 3)
-    if not (isinstance(w_uv, torch.Tensor) and w_uv.is_cuda and w_uv.dim() == 3
+    if not (isinstance(w_uv, torch.Tensor) and _is_device(w_uv) and w_uv.dim() == 3
             and w_uv.dtype in (torch.bfloat16, torch.int16, torch.uint16)
             and w_uv.is_contiguous()):
         raise ValueError("w_uv must be a contiguous CUDA bfloat16 [H, 512, V] tensor")
@@ -228,6 +242,8 @@ def mla_wuv_epilogue(o, w_uv, y=None, stream=None):
     if y is None:
         y = torch.empty((B, H, V), dtype=torch.float32, device=o.device)
     _need(y, "y", torch.float32, 3)
+    if tuple(y.shape) != (B, H, V):
+        raise ValueError("y must be [B, H, V]")
     st = lib().mla_wuv_epilogue(_ptr(o), _ptr(w_uv), B, H, V, _ptr(y), _stream(stream))
     _check("mla_wuv_epilogue", st)
     return y
@@ -261,8 +277,7 @@ def mla_absorb_decode_fp8(q_lat, q_rope, kv_codes, kv_scales, T, sm_scale, out=N
     """One query (q_lat [H,512], q_rope [H,64]) against kv rows 0..T-1 -> out [H,512]."""
     _need(q_lat, "q_lat", torch.float32, 2)
     _need(q_rope, "q_rope", torch.float32, 2)
-    _need(kv_codes, "kv_codes", torch.uint8, 2)
-    _need(kv_scales, "kv_scales", torch.float32, 2)
+    _need_cache(kv_codes, kv_scales)
     H = q_lat.shape[0]
     if q_lat.shape[1] != KV8_DL or tuple(q_rope.shape) != (H, KV8_DR):
         raise ValueError("q_lat must be [H,512] and q_rope [H,64]")
@@ -296,15 +311,12 @@ def _batch_inputs(q_lat, q_rope, kv_codes, kv_scales, block_table, seq_lens, out
     allocated if None."""
     _need(q_lat, "q_lat", torch.float32, 3)
     _need(q_rope, "q_rope", torch.float32, 3)
-    _need(kv_codes, "kv_codes", torch.uint8, 2)
-    _need(kv_scales, "kv_scales", torch.float32, 2)
+    _need_cache(kv_codes, kv_scales)
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     B, H = q_lat.shape[:2]
     if q_lat.shape[2] != KV8_DL or tuple(q_rope.shape) != (B, H, KV8_DR):
         raise ValueError("q_lat must be [B,H,512] and q_rope [B,H,64]")
-    if kv_codes.shape[1] != KV8_D or tuple(kv_scales.shape) != (kv_codes.shape[0], 2):
-        raise ValueError("kv_codes must be [slots,576] and kv_scales [slots,2]")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table and seq_lens need one row per sequence")
     if not outputs:
