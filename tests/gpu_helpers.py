@@ -11,9 +11,9 @@ import oracle
 
 # max-abs error <= TOL * max|out| per sequence against the f64 oracle on the same codes:
 #   CUDA-core kernel (f32 operands and accumulation): 2e-3;
-#   tensor-core kernels (reduced-precision MMA operands: the query as fp16 (one-CTA kernel)
-#   or as two e4m3 terms (pair kernel) for the scores, the softmax weights as two e4m3
-#   terms for the context; f32 accumulation): 1e-2.
+#   tensor-core kernels (reduced-precision MMA operands: the query as two e4m3 terms on a
+#   per-head power-of-two scale for the scores, in both kernels, and the softmax weights as
+#   two e4m3 terms for the context; f32 accumulation): 1e-2.
 TOLS = {1: 2e-3, 2: 1e-2, 3: 1e-2, 4: 1e-2}
 NAMES = {1: "simt", 2: "tcgen05", 3: "tcgen05_cta", 4: "tcgen05_pair"}
 LSE_TOL = 2e-3   # natural-log units

@@ -5,8 +5,8 @@ v2"), PR description (absorbed attention over the e4m3 latent rows, each row
 scale applied outside its dot product) and closing note (split-T).  Tolerance:
 max-abs error <= 2e-3 * max|out| per sequence for the CUDA-core kernel (f32 throughout) and
 <= 1e-2 * max|out| for the tensor-core kernels (reduced-precision MMA operands:
-the query as fp16 (one-CTA kernel) or two e4m3 terms (SM-pair kernel) for the
-scores, the softmax weights as two e4m3 terms for the context; f32
+the query as two e4m3 terms on a per-head power-of-two scale for the scores, in
+both kernels, the softmax weights as two e4m3 terms for the context; f32
 accumulation); lse within 2e-3.  Every test runs the three kernels: CUDA-core,
 one-CTA tensor-core and SM-pair tensor-core (the last two forced at any H).
 Caches are filled by the library's quantizer and the oracle reads the same
